@@ -1,0 +1,225 @@
+"""GB300-native fused all-gather matmul: Python binding of libagmm.
+
+Thin ctypes marshalling over the C ABI in ``include/agmm.h``; every step of
+the operation runs in the library's CUDA kernels.  PyTorch only provides the
+device memory and the current stream.  There is no fallback: if the compiled
+library is missing, every call raises.
+
+    a_gathered, out = ag_matmul(shards, b, bias=None, layout="k_contiguous", rank=0)
+
+``shards`` is a list of D CUDA tensors [m_per_shard, K] (bf16 or fp16, the
+D row shards of A, each its own allocation); ``b`` is [K, N] of the same
+dtype; ``bias`` an optional fp32 [N].  ``a_gathered`` = concat(shards) and
+``out`` = a_gathered @ b (+ bias), computed with fp32 accumulation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import _build
+
+__all__ = [
+    "AgmmError", "AgOptions", "ag_matmul", "ag_then_matmul", "ag_matmul_raw",
+    "device_error", "workspace_size", "release_workspace", "num_sms", "library",
+    "LAYOUTS", "STATUS",
+]
+
+STATUS = {0: "AG_OK", 1: "AG_ERR_INVALID_ARG", 2: "AG_ERR_UNSUPPORTED", 3: "AG_ERR_CUDA",
+          4: "AG_ERR_TIMEOUT", 5: "AG_ERR_WORKSPACE"}
+LAYOUTS = {"k_contiguous": 0, "m_contiguous": 1}
+DTYPES = {"bf16": 0, "fp16": 1}
+EXPORTS = ("ag_options_default", "ag_matmul", "ag_then_matmul", "ag_matmul_ex",
+           "ag_then_matmul_ex", "ag_workspace_size", "ag_get_device_error",
+           "ag_release_workspace", "ag_status_string", "ag_num_sms")
+
+
+class AgmmError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)} ({_status_text(status)})")
+
+
+class AgOptions(ctypes.Structure):
+    """Mirror of ``struct ag_options``."""
+    _fields_ = [
+        ("dtype", ctypes.c_int32),
+        ("layout", ctypes.c_int32),
+        ("rank", ctypes.c_int32),
+        ("k_per_flag", ctypes.c_int32),
+        ("num_sms", ctypes.c_int32),
+        ("inject_skip_flag", ctypes.c_int32),
+        ("timeout_ns", ctypes.c_int64),
+        ("trace", ctypes.c_void_p),
+        ("trace_words", ctypes.c_int64),
+        ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_int64),
+    ]
+
+
+_lib = None
+
+
+def library(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libagmm.so (building it first if it is missing or stale)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB_PATH
+    if build_if_missing and _build.is_stale():
+        _build.build()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libagmm.so not found at {path}; build it with "
+                           "__graft_entry__.build() (nvcc, sm_103a)")
+    lib = ctypes.CDLL(path)
+    vp, i32 = ctypes.c_void_p, ctypes.c_int
+    core = [ctypes.POINTER(vp), i32, i32, i32, vp, i32, vp, vp, vp, vp]
+    for name in ("ag_matmul", "ag_then_matmul"):
+        getattr(lib, name).argtypes = core
+        getattr(lib, name).restype = i32
+    for name in ("ag_matmul_ex", "ag_then_matmul_ex"):
+        getattr(lib, name).argtypes = core + [ctypes.POINTER(AgOptions)]
+        getattr(lib, name).restype = i32
+    lib.ag_options_default.argtypes = [ctypes.POINTER(AgOptions)]
+    lib.ag_options_default.restype = None
+    lib.ag_workspace_size.argtypes = [i32, i32, i32, i32, ctypes.POINTER(AgOptions)]
+    lib.ag_workspace_size.restype = ctypes.c_size_t
+    lib.ag_get_device_error.argtypes = [vp, ctypes.POINTER(i32), ctypes.POINTER(i32)]
+    lib.ag_get_device_error.restype = i32
+    lib.ag_release_workspace.argtypes = []
+    lib.ag_release_workspace.restype = i32
+    lib.ag_status_string.argtypes = [i32]
+    lib.ag_status_string.restype = ctypes.c_char_p
+    lib.ag_num_sms.argtypes = []
+    lib.ag_num_sms.restype = i32
+    _lib = lib
+    return lib
+
+
+def _status_text(status: int) -> str:
+    try:
+        return library().ag_status_string(status).decode()
+    except Exception:  # pragma: no cover - library unavailable while formatting
+        return "?"
+
+
+def default_options() -> AgOptions:
+    o = AgOptions()
+    library().ag_options_default(ctypes.byref(o))
+    return o
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dtype_name(t) -> str:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return "bf16"
+    if t.dtype == torch.float16:
+        return "fp16"
+    raise TypeError(f"unsupported dtype {t.dtype}; use bfloat16 or float16")
+
+
+def ag_matmul_raw(fused: bool, shard_ptrs, D, m_per_shard, K, b_ptr, N, bias_ptr, ag_ptr, out_ptr,
+                  stream_handle, options: AgOptions | None = None) -> int:
+    """Direct call of the C entry point with integer pointers; returns the status."""
+    lib = library()
+    arr = (ctypes.c_void_p * max(D, 1))(*[ctypes.c_void_p(p) for p in shard_ptrs])
+    args = [arr, D, m_per_shard, K, ctypes.c_void_p(b_ptr), N,
+            ctypes.c_void_p(bias_ptr) if bias_ptr else None, ctypes.c_void_p(ag_ptr),
+            ctypes.c_void_p(out_ptr), stream_handle]
+    if options is None:
+        return (lib.ag_matmul if fused else lib.ag_then_matmul)(*args)
+    fn = lib.ag_matmul_ex if fused else lib.ag_then_matmul_ex
+    return fn(*args, ctypes.byref(options))
+
+
+def _call(fused, shards, b, bias, a_gathered, out, stream, layout, rank, k_per_flag, num_sms,
+          timeout_ns, inject_skip_flag, trace, workspace):
+    import torch
+    if not shards:
+        raise ValueError("need at least one shard")
+    D = len(shards)
+    m, K = shards[0].shape
+    K2, N = b.shape
+    dt = _dtype_name(b)
+    for s in shards:
+        if s.shape != (m, K) or s.dtype != b.dtype or not s.is_cuda or not s.is_contiguous():
+            raise ValueError("shards must be contiguous CUDA tensors of one shape and b's dtype")
+    if K2 != K or not b.is_cuda or not b.is_contiguous():
+        raise ValueError("b must be a contiguous CUDA tensor [K, N]")
+    M = D * m
+    if a_gathered is None:
+        a_gathered = torch.empty((M, K), dtype=b.dtype, device=b.device)
+    if out is None:
+        out = torch.empty((M, N), dtype=b.dtype, device=b.device)
+    if bias is not None and (bias.dtype != torch.float32 or bias.shape != (N,) or not bias.is_cuda):
+        raise ValueError("bias must be a CUDA fp32 tensor [N]")
+    o = default_options()
+    o.dtype = DTYPES[dt]
+    o.layout = LAYOUTS[layout]
+    o.rank = rank
+    o.k_per_flag = k_per_flag
+    o.num_sms = num_sms
+    o.timeout_ns = timeout_ns
+    o.inject_skip_flag = inject_skip_flag
+    if trace is not None:
+        o.trace = trace.data_ptr()
+        o.trace_words = trace.numel()
+    if workspace is not None:
+        o.workspace = workspace.data_ptr()
+        o.workspace_bytes = workspace.numel() * workspace.element_size()
+    st = ag_matmul_raw(fused, [s.data_ptr() for s in shards], D, m, K, b.data_ptr(), N,
+                       bias.data_ptr() if bias is not None else 0, a_gathered.data_ptr(),
+                       out.data_ptr(), _stream_handle(stream), o)
+    if st != 0:
+        raise AgmmError(st, "ag_matmul" if fused else "ag_then_matmul")
+    return a_gathered, out
+
+
+def ag_matmul(shards, b, bias=None, *, a_gathered=None, out=None, stream=None,
+              layout: str = "k_contiguous", rank: int = 0, k_per_flag: int = 16,
+              num_sms: int = 0, timeout_ns: int = 0, inject_skip_flag: int = -1, trace=None,
+              workspace=None):
+    """Fused all-gather matmul (one persistent kernel).  Returns (a_gathered, out)."""
+    return _call(True, shards, b, bias, a_gathered, out, stream, layout, rank, k_per_flag,
+                 num_sms, timeout_ns, inject_skip_flag, trace, workspace)
+
+
+def ag_then_matmul(shards, b, bias=None, *, a_gathered=None, out=None, stream=None,
+                   num_sms: int = 0, timeout_ns: int = 0, trace=None):
+    """Barrier baseline: gather kernel, then GEMM kernel.  Returns (a_gathered, out)."""
+    return _call(False, shards, b, bias, a_gathered, out, stream, "k_contiguous", 0, 16,
+                 num_sms, timeout_ns, -1, trace, None)
+
+
+def device_error(stream=None):
+    """Synchronise the stream; return (code, info) of the newest unreported device error."""
+    code, info = ctypes.c_int(0), ctypes.c_int(0)
+    st = library().ag_get_device_error(_stream_handle(stream), ctypes.byref(code),
+                                       ctypes.byref(info))
+    if st != 0:
+        raise AgmmError(st, "ag_get_device_error")
+    return code.value, info.value
+
+
+def workspace_size(D, m_per_shard, K, N, layout: str = "k_contiguous", k_per_flag: int = 16) -> int:
+    o = default_options()
+    o.layout = LAYOUTS[layout]
+    o.k_per_flag = k_per_flag
+    return int(library().ag_workspace_size(D, m_per_shard, K, N, ctypes.byref(o)))
+
+
+def release_workspace() -> None:
+    st = library().ag_release_workspace()
+    if st != 0:
+        raise AgmmError(st, "ag_release_workspace")
+
+
+def num_sms() -> int:
+    return int(library().ag_num_sms())

@@ -1,0 +1,467 @@
+// Host side of libagmm: argument validation, workspace and epoch management,
+// TMA tensor-map encoding and the kernel launches behind the C ABI declared in
+// include/agmm.h.  Everything the operation computes runs in the kernels of
+// kernels.cuh; this file only prepares and enqueues them.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "agmm.h"
+#include "kernels.cuh"
+
+using namespace agmm;
+
+static_assert(AG_MAX_SHARDS == kMaxShards, "header and kernel shard limits differ");
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kDefaultTimeoutNs = 2000000000LL;
+constexpr int kDefaultKPerFlag = 16;
+
+thread_local char t_cuda_msg[320] = "no CUDA error recorded on this thread";
+
+int cuda_fail(cudaError_t e, const char* what) {
+  snprintf(t_cuda_msg, sizeof t_cuda_msg, "%s failed: %s (%s)", what, cudaGetErrorName(e),
+           cudaGetErrorString(e));
+  return AG_ERR_CUDA;
+}
+
+#define AG_CK(call)                                     \
+  do {                                                  \
+    cudaError_t e_ = (call);                            \
+    if (e_ != cudaSuccess) return cuda_fail(e_, #call); \
+  } while (0)
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// Library-owned state, one per device.
+struct DevState {
+  bool init = false;
+  bool supported = false;
+  int sms = 0;
+  unsigned long long* err = nullptr;  // [2] device error word
+  uint64_t* flags = nullptr;
+  size_t flags_cap = 0;  // words
+  uint16_t* staging = nullptr;
+  size_t staging_cap = 0;  // elements
+  uint64_t reported_epoch = 0;
+};
+
+std::mutex g_mu;
+DevState g_dev[kMaxDevices];
+// One epoch counter for the whole process: flags in any workspace on any
+// device compare against it, so a workspace never needs clearing between calls.
+std::atomic<uint64_t> g_epoch{0};
+
+struct Shape {
+  int D, mps, K, N;
+  int64_t M;
+  int num_mb, num_nb, num_kb, kpf, G;
+};
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
+  uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + bn && y < x + an;
+}
+
+// Validation that needs no CUDA call.  Fills `sh`.
+int validate(const void** a_shards, int D, int m_per_shard, int K, const void* b, int N,
+             const void* bias, void* a_gathered, void* out, const ag_options& o, bool fused,
+             Shape* sh) {
+  if (!a_shards || !b || !a_gathered || !out) return AG_ERR_INVALID_ARG;
+  if (D < 1 || m_per_shard < 1 || K < 8 || N < 8) return AG_ERR_INVALID_ARG;
+  if (K % 8 || N % 8) return AG_ERR_INVALID_ARG;
+  if (D > AG_MAX_SHARDS) return AG_ERR_UNSUPPORTED;
+  const int64_t M = (int64_t)D * m_per_shard;
+  if (M > INT32_MAX) return AG_ERR_INVALID_ARG;
+  if (o.dtype != AG_DTYPE_BF16 && o.dtype != AG_DTYPE_FP16) return AG_ERR_INVALID_ARG;
+  if (o.layout != AG_LAYOUT_K_CONTIGUOUS && o.layout != AG_LAYOUT_M_CONTIGUOUS)
+    return AG_ERR_INVALID_ARG;
+  if (o.rank < 0 || o.rank >= D) return AG_ERR_INVALID_ARG;
+  if (o.k_per_flag < 0 || o.num_sms < 0 || o.timeout_ns < 0 || o.trace_words < 0 ||
+      o.workspace_bytes < 0)
+    return AG_ERR_INVALID_ARG;
+  if (o.trace && (o.trace_words < 1 || !aligned(o.trace, 8))) return AG_ERR_INVALID_ARG;
+  if (fused && o.layout == AG_LAYOUT_M_CONTIGUOUS && (M % 8)) return AG_ERR_UNSUPPORTED;
+  if (!aligned(b, 16) || !aligned(a_gathered, 16) || !aligned(out, 16)) return AG_ERR_INVALID_ARG;
+  if (bias && !aligned(bias, 4)) return AG_ERR_INVALID_ARG;
+  const size_t shard_bytes = (size_t)m_per_shard * K * 2;
+  const size_t ag_bytes = (size_t)M * K * 2, out_bytes = (size_t)M * N * 2;
+  const size_t b_bytes = (size_t)K * N * 2, bias_bytes = (size_t)N * 4;
+  for (int r = 0; r < D; ++r) {
+    if (!a_shards[r] || !aligned(a_shards[r], 16)) return AG_ERR_INVALID_ARG;
+    if (overlaps(a_shards[r], shard_bytes, a_gathered, ag_bytes) ||
+        overlaps(a_shards[r], shard_bytes, out, out_bytes))
+      return AG_ERR_INVALID_ARG;
+  }
+  if (overlaps(a_gathered, ag_bytes, out, out_bytes) || overlaps(b, b_bytes, a_gathered, ag_bytes) ||
+      overlaps(b, b_bytes, out, out_bytes))
+    return AG_ERR_INVALID_ARG;
+  if (bias && (overlaps(bias, bias_bytes, a_gathered, ag_bytes) ||
+               overlaps(bias, bias_bytes, out, out_bytes)))
+    return AG_ERR_INVALID_ARG;
+  sh->D = D;
+  sh->mps = m_per_shard;
+  sh->K = K;
+  sh->N = N;
+  sh->M = M;
+  sh->num_mb = (int)((M + kBM - 1) / kBM);
+  sh->num_nb = (N + kBN - 1) / kBN;
+  sh->num_kb = (K + kBK - 1) / kBK;
+  sh->kpf = o.k_per_flag ? o.k_per_flag : kDefaultKPerFlag;
+  sh->G = (sh->num_kb + sh->kpf - 1) / sh->kpf;
+  if ((int64_t)sh->num_mb * sh->num_nb > INT32_MAX || (int64_t)sh->num_mb * sh->G > 0xFFFFFF)
+    return AG_ERR_UNSUPPORTED;
+  return AG_OK;
+}
+
+size_t flags_bytes(const Shape& s) {
+  return (((size_t)s.num_mb * s.G * 8) + 1023) & ~size_t(1023);
+}
+
+// Device pointers must be device (or managed) memory of the current device:
+// a host pointer handed to a kernel would fault.
+int check_device_ptr(const void* p, int dev) {
+  cudaPointerAttributes at;
+  cudaError_t e = cudaPointerGetAttributes(&at, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return AG_ERR_INVALID_ARG;
+  }
+  if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged) return AG_ERR_INVALID_ARG;
+  if (at.type == cudaMemoryTypeDevice && at.device != dev) return AG_ERR_INVALID_ARG;
+  return AG_OK;
+}
+
+int device_init(DevState& ds, int dev) {
+  if (ds.init) return ds.supported ? AG_OK : AG_ERR_UNSUPPORTED;
+  int major = 0, minor = 0, sms = 0;
+  AG_CK(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev));
+  AG_CK(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev));
+  AG_CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  ds.sms = sms;
+  // The kernels are built for sm_103a only; a missing image is "unsupported".
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, agmm_gemm_kernel<true>) != cudaSuccess || major != 10) {
+    cudaGetLastError();
+    ds.init = true;
+    ds.supported = false;
+    return AG_ERR_UNSUPPORTED;
+  }
+  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes));
+  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
+  AG_CK(cudaMalloc(&ds.err, 2 * sizeof(unsigned long long)));
+  AG_CK(cudaMemset(ds.err, 0, 2 * sizeof(unsigned long long)));
+  ds.init = true;
+  ds.supported = true;
+  return AG_OK;
+}
+
+int grow_workspace(DevState& ds, const Shape& s, bool need_staging, cudaStream_t stream) {
+  const size_t words = flags_bytes(s) / 8;
+  const size_t stage_elems = need_staging ? (size_t)s.K * s.M : 0;
+  if (words > ds.flags_cap || stage_elems > ds.staging_cap) {
+    // Older calls may still use the old buffers.
+    AG_CK(cudaDeviceSynchronize());
+  }
+  if (words > ds.flags_cap) {
+    if (ds.flags) AG_CK(cudaFree(ds.flags));
+    ds.flags = nullptr;
+    ds.flags_cap = 0;
+    AG_CK(cudaMalloc(&ds.flags, words * 8));
+    AG_CK(cudaMemsetAsync(ds.flags, 0, words * 8, stream));
+    ds.flags_cap = words;
+  }
+  if (stage_elems > ds.staging_cap) {
+    if (ds.staging) AG_CK(cudaFree(ds.staging));
+    ds.staging = nullptr;
+    ds.staging_cap = 0;
+    AG_CK(cudaMalloc(&ds.staging, stage_elems * 2));
+    ds.staging_cap = stage_elems;
+  }
+  return AG_OK;
+}
+
+int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+             uint32_t box_outer) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) {
+    snprintf(t_cuda_msg, sizeof t_cuda_msg, "cuTensorMapEncodeTiled entry point unavailable");
+    return AG_ERR_CUDA;
+  }
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(t_cuda_msg, sizeof t_cuda_msg, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    return AG_ERR_CUDA;
+  }
+  return AG_OK;
+}
+
+int run(bool fused, const void** a_shards, int D, int m_per_shard, int K, const void* b, int N,
+        const void* bias, void* a_gathered, void* out, cudaStream_t stream,
+        const ag_options* opt_in) {
+  ag_options o;
+  ag_options_default(&o);
+  if (opt_in) o = *opt_in;
+  Shape s;
+  int st = validate(a_shards, D, m_per_shard, K, b, N, bias, a_gathered, out, o, fused, &s);
+  if (st != AG_OK) return st;
+  const bool layout_m = fused && o.layout == AG_LAYOUT_M_CONTIGUOUS;
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  AG_CK(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices) return AG_ERR_UNSUPPORTED;
+  DevState& ds = g_dev[dev];
+  st = device_init(ds, dev);
+  if (st != AG_OK) return st;
+
+  for (int r = 0; r < D; ++r)
+    if ((st = check_device_ptr(a_shards[r], dev)) != AG_OK) return st;
+  if ((st = check_device_ptr(b, dev)) != AG_OK || (st = check_device_ptr(a_gathered, dev)) != AG_OK ||
+      (st = check_device_ptr(out, dev)) != AG_OK)
+    return st;
+  if (bias && (st = check_device_ptr(bias, dev)) != AG_OK) return st;
+  if (o.trace && (st = check_device_ptr(o.trace, dev)) != AG_OK) return st;
+
+  // Workspace: flags (+ [K, M] staging for the m-contiguous layout).
+  uint64_t* flags = nullptr;
+  uint16_t* staging = nullptr;
+  if (fused) {
+    if (o.workspace) {
+      const size_t need = flags_bytes(s) + (layout_m ? (size_t)s.K * s.M * 2 : 0);
+      if ((size_t)o.workspace_bytes < need) return AG_ERR_WORKSPACE;
+      if (!aligned(o.workspace, 256)) return AG_ERR_INVALID_ARG;
+      if ((st = check_device_ptr(o.workspace, dev)) != AG_OK) return st;
+      flags = static_cast<uint64_t*>(o.workspace);
+      staging = layout_m ? reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(o.workspace) +
+                                                       flags_bytes(s))
+                         : nullptr;
+    } else {
+      if ((st = grow_workspace(ds, s, layout_m, stream)) != AG_OK) return st;
+      flags = ds.flags;
+      staging = layout_m ? ds.staging : nullptr;
+    }
+  }
+
+  const uint64_t epoch = g_epoch.fetch_add(1) + 1;
+  const int64_t timeout = o.timeout_ns ? o.timeout_ns : kDefaultTimeoutNs;
+  const int cap = o.num_sms ? std::min(o.num_sms, ds.sms) : ds.sms;
+
+  if (!fused) {
+    GatherParams gp;
+    memset(&gp, 0, sizeof gp);
+    for (int r = 0; r < D; ++r) gp.shards[r] = static_cast<const uint16_t*>(a_shards[r]);
+    gp.a_gathered = static_cast<uint16_t*>(a_gathered);
+    gp.vec_per_shard = (int64_t)m_per_shard * K / 8;
+    gp.trace = o.trace;
+    gp.trace_words = o.trace_words;
+    const int64_t per_shard_blocks = (gp.vec_per_shard + 255) / 256;
+    int gx = (int)std::max<int64_t>(1, std::min<int64_t>((ds.sms * 4 + D - 1) / D, per_shard_blocks));
+    agmm_gather_kernel<<<dim3(gx, D), 256, 0, stream>>>(gp);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "gather kernel launch");
+  }
+
+  GemmParams p;
+  memset(&p, 0, sizeof p);
+  if ((st = make_map(&p.tm_a, a_gathered, (uint64_t)K, (uint64_t)s.M, kBK, kBM)) != AG_OK) return st;
+  if ((st = make_map(&p.tm_b, b, (uint64_t)N, (uint64_t)K, 64, kBK)) != AG_OK) return st;
+  if ((st = make_map(&p.tm_out, out, (uint64_t)N, (uint64_t)s.M, kEpiCols, kEpiRows)) != AG_OK)
+    return st;
+  if (fused) {
+    if ((st = make_map(&p.tm_local, a_shards[o.rank], (uint64_t)K, (uint64_t)m_per_shard, kBK,
+                       kBM)) != AG_OK)
+      return st;
+    if (layout_m &&
+        (st = make_map(&p.tm_a_mk, staging, (uint64_t)s.M, (uint64_t)K, 64, kBK)) != AG_OK)
+      return st;
+  }
+  for (int r = 0; r < D; ++r) p.shards[r] = static_cast<const uint16_t*>(a_shards[r]);
+  p.a_gathered = static_cast<uint16_t*>(a_gathered);
+  p.staging_mk = staging;
+  p.bias = static_cast<const float*>(bias);
+  p.flags = flags;
+  p.err = ds.err;
+  p.trace = o.trace;
+  p.trace_words = o.trace_words;
+  p.epoch = epoch;
+  p.timeout_ns = timeout;
+  p.pipe_timeout_ns = 4 * timeout + 2000000000LL;
+  p.M = (int)s.M;
+  p.N = N;
+  p.K = K;
+  p.D = D;
+  p.mps = m_per_shard;
+  p.rank = fused ? o.rank : 0;
+  p.num_mb = s.num_mb;
+  p.num_nb = s.num_nb;
+  p.num_kb = s.num_kb;
+  p.num_tiles = s.num_mb * s.num_nb;
+  p.kpf = s.kpf;
+  p.G = s.G;
+  p.mb_start = fused ? (int)(((int64_t)o.rank * m_per_shard) / kBM) : 0;
+  p.layout_m = layout_m ? 1 : 0;
+  p.fp16 = o.dtype == AG_DTYPE_FP16 ? 1 : 0;
+  p.inject_skip_flag = fused ? o.inject_skip_flag : -1;
+
+  const int grid = std::max(1, std::min(cap, p.num_tiles));
+  if (fused)
+    agmm_gemm_kernel<true><<<grid, kFusedThreads, kSmemBytes, stream>>>(p);
+  else
+    agmm_gemm_kernel<false><<<grid, kGemmThreads, kSmemBytes, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, fused ? "fused kernel launch" : "gemm kernel launch");
+  return AG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+void ag_options_default(ag_options* opt) {
+  if (!opt) return;
+  memset(opt, 0, sizeof *opt);
+  opt->dtype = AG_DTYPE_BF16;
+  opt->layout = AG_LAYOUT_K_CONTIGUOUS;
+  opt->rank = 0;
+  opt->k_per_flag = kDefaultKPerFlag;
+  opt->num_sms = 0;
+  opt->inject_skip_flag = -1;
+  opt->timeout_ns = kDefaultTimeoutNs;
+}
+
+int ag_matmul(const void** a_shards, int D, int m_per_shard, int K, const void* b, int N,
+              const void* bias_or_null, void* a_gathered, void* out, cudaStream_t stream) {
+  return run(true, a_shards, D, m_per_shard, K, b, N, bias_or_null, a_gathered, out, stream,
+             nullptr);
+}
+
+int ag_then_matmul(const void** a_shards, int D, int m_per_shard, int K, const void* b, int N,
+                   const void* bias_or_null, void* a_gathered, void* out, cudaStream_t stream) {
+  return run(false, a_shards, D, m_per_shard, K, b, N, bias_or_null, a_gathered, out, stream,
+             nullptr);
+}
+
+int ag_matmul_ex(const void** a_shards, int D, int m_per_shard, int K, const void* b, int N,
+                 const void* bias_or_null, void* a_gathered, void* out, cudaStream_t stream,
+                 const ag_options* opt) {
+  return run(true, a_shards, D, m_per_shard, K, b, N, bias_or_null, a_gathered, out, stream, opt);
+}
+
+int ag_then_matmul_ex(const void** a_shards, int D, int m_per_shard, int K, const void* b, int N,
+                      const void* bias_or_null, void* a_gathered, void* out, cudaStream_t stream,
+                      const ag_options* opt) {
+  return run(false, a_shards, D, m_per_shard, K, b, N, bias_or_null, a_gathered, out, stream, opt);
+}
+
+size_t ag_workspace_size(int D, int m_per_shard, int K, int N, const ag_options* opt) {
+  ag_options o;
+  ag_options_default(&o);
+  if (opt) o = *opt;
+  if (D < 1 || D > AG_MAX_SHARDS || m_per_shard < 1 || K < 8 || N < 8 || K % 8 || N % 8 ||
+      o.k_per_flag < 0)
+    return 0;
+  const int64_t M = (int64_t)D * m_per_shard;
+  if (M > INT32_MAX) return 0;
+  Shape s;
+  s.M = M;
+  s.K = K;
+  s.num_mb = (int)((M + kBM - 1) / kBM);
+  s.num_kb = (K + kBK - 1) / kBK;
+  s.kpf = o.k_per_flag ? o.k_per_flag : kDefaultKPerFlag;
+  s.G = (s.num_kb + s.kpf - 1) / s.kpf;
+  return flags_bytes(s) + (o.layout == AG_LAYOUT_M_CONTIGUOUS ? (size_t)K * M * 2 : 0);
+}
+
+int ag_get_device_error(cudaStream_t stream, int* code, int* info) {
+  if (code) *code = AG_OK;
+  if (info) *info = 0;
+  int dev = 0;
+  AG_CK(cudaGetDevice(&dev));
+  AG_CK(cudaStreamSynchronize(stream));
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (dev < 0 || dev >= kMaxDevices || !g_dev[dev].err) return AG_OK;
+  DevState& ds = g_dev[dev];
+  unsigned long long host[2];
+  AG_CK(cudaMemcpy(host, ds.err, sizeof host, cudaMemcpyDeviceToHost));
+  if (host[0] > ds.reported_epoch) {
+    ds.reported_epoch = host[0];
+    if (code) *code = (int)(host[1] >> 32);
+    if (info) *info = (int)(host[1] & 0xFFFFFFFFull);
+  }
+  return AG_OK;
+}
+
+int ag_release_workspace(void) {
+  int dev = 0;
+  AG_CK(cudaGetDevice(&dev));
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (dev < 0 || dev >= kMaxDevices) return AG_OK;
+  DevState& ds = g_dev[dev];
+  if (!ds.flags && !ds.staging) return AG_OK;
+  AG_CK(cudaDeviceSynchronize());
+  if (ds.flags) AG_CK(cudaFree(ds.flags));
+  if (ds.staging) AG_CK(cudaFree(ds.staging));
+  ds.flags = nullptr;
+  ds.staging = nullptr;
+  ds.flags_cap = ds.staging_cap = 0;
+  return AG_OK;
+}
+
+const char* ag_status_string(int status) {
+  switch (status) {
+    case AG_OK: return "ok";
+    case AG_ERR_INVALID_ARG: return "invalid argument";
+    case AG_ERR_UNSUPPORTED: return "unsupported by this build or device";
+    case AG_ERR_CUDA: return t_cuda_msg;
+    case AG_ERR_TIMEOUT: return "device-side wait timed out";
+    case AG_ERR_WORKSPACE: return "caller workspace too small";
+    default: return "unknown status";
+  }
+}
+
+int ag_num_sms(void) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return sms;
+}
+
+}  // extern "C"

@@ -1,0 +1,183 @@
+/*
+ * agmm -- fused all-gather matmul for one GB300 (sm_103a).  C ABI.
+ *
+ * The operation ("Add all gather matmul benchmark", pytorch/helion PR #400,
+ * statement of the op):
+ *
+ *     (a, out) = ag_matmul(a_shared, b),  a = all_gather(a_shared),  out = a @ b
+ *
+ * Here the D row shards of A are D separate device allocations on the same
+ * GPU (they stand in for D ranks).  The library writes the gathered matrix
+ * a_gathered = concat_rows(a_shards[0..D-1]) ([M, K], M = D * m_per_shard) and
+ * out = a_gathered @ b (+ bias) ([M, N]).  Inputs and outputs are 16-bit
+ * (bf16 by default, or fp16); products are summed in fp32 and rounded once,
+ * to nearest even, after the optional fp32 bias is added ("Fused
+ * all-gather+GEMM HBM-buffer kernel for iris.ops", ROCm/iris #346, section
+ * "New kernel": optional bias in the epilogue).
+ *
+ * ag_matmul runs the fused design of that Iris kernel (section "New kernel"
+ * and its description): one persistent kernel in which producer warps copy A
+ * tiles from the shards into an HBM staging buffer and publish per-tile ready
+ * flags, while tensor-core consumer warps wait on those flags and compute each
+ * output tile as soon as its A rows are staged -- no whole-gather barrier.
+ * Tiles that lie inside the local shard (option `rank`) are read straight from
+ * that shard without waiting (the local-tile shortcut described in the Helion
+ * PR).  ag_then_matmul is the barrier baseline of the Iris result tables
+ * ("Baseline" column): gather everything, then run the GEMM.
+ *
+ * Common argument contract (every entry point below that takes these):
+ *   a_shards      HOST array of D DEVICE pointers; shard r is row-major
+ *                 [m_per_shard, K], contiguous, 16-byte aligned.  Read only.
+ *   D             number of shards, 1 <= D <= AG_MAX_SHARDS.
+ *   m_per_shard   rows per shard, >= 1.  M = D * m_per_shard <= 2^31 - 1.
+ *   K             columns of A / rows of b; >= 8 and a multiple of 8 (row
+ *                 pitches must be multiples of 16 bytes for TMA).
+ *   b             DEVICE pointer, row-major [K, N], 16-byte aligned.  Read only.
+ *   N             columns of b and out; >= 8 and a multiple of 8.
+ *   bias_or_null  DEVICE pointer to N fp32 values (4-byte aligned) or NULL.
+ *   a_gathered    DEVICE pointer, row-major [M, K], 16-byte aligned.  Written.
+ *   out           DEVICE pointer, row-major [M, N], 16-byte aligned.  Written.
+ *   stream        CUDA stream the work is enqueued on (0 = legacy default).
+ * The caller allocates and owns every pointer argument.  Outputs must not
+ * overlap each other or any input.  The dtype of a_shards, b, a_gathered and
+ * out is the same (ag_options.dtype; bf16 for the entry points without
+ * options).
+ *
+ * Semantics: asynchronous.  A call validates its arguments, enqueues one
+ * (fused) or two (barrier) kernels on `stream` and returns; it never
+ * synchronises the host.  On any error return nothing has been enqueued.
+ * Inputs must stay unchanged until the stream has executed the call.
+ *
+ * Errors: the return value is an ag_status.  Device-side failures (a ready
+ * flag or pipeline wait that exceeded its time limit) cannot be returned by
+ * an asynchronous call; the kernel records them and ag_get_device_error()
+ * reports them.  No kernel of this library traps or faults on purpose: every
+ * device-side wait is bounded by a time limit.
+ *
+ * Workspace: the fused path needs per-tile ready flags (8 bytes per
+ * (128-row block, k-group)) and, for the m-contiguous layout, a [K, M]
+ * staging buffer.  By default the library owns them (one set per device,
+ * grown on demand; growing synchronises the device).  Calls that use the
+ * library workspace on the same device must be ordered (same stream, or
+ * ordered by events); calls that may overlap on the GPU need separate
+ * caller workspaces (ag_options.workspace).
+ */
+#ifndef AGMM_H_
+#define AGMM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define AG_MAX_SHARDS 64
+
+/* Return codes. */
+typedef enum ag_status {
+  AG_OK = 0,
+  AG_ERR_INVALID_ARG = 1, /* bad pointer, size, alignment, overlap or option value */
+  AG_ERR_UNSUPPORTED = 2, /* valid request this build cannot run (device, dtype/layout combo, D > AG_MAX_SHARDS) */
+  AG_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed; see ag_status_string */
+  AG_ERR_TIMEOUT = 4,     /* device-side: a bounded wait ran out (reported by ag_get_device_error) */
+  AG_ERR_WORKSPACE = 5    /* caller workspace smaller than ag_workspace_size() */
+} ag_status;
+
+typedef enum ag_dtype { AG_DTYPE_BF16 = 0, AG_DTYPE_FP16 = 1 } ag_dtype;
+
+/* Layout of the staged A in HBM ("Fused all-gather+GEMM HBM-buffer kernel for
+ * iris.ops", section "New kernel": k_contiguous and m_contiguous staged-A
+ * layouts; the page names them without defining them).  Reading used here:
+ *   AG_LAYOUT_K_CONTIGUOUS  staged A is [M, K] row-major (K fastest); this is
+ *                           a_gathered itself.
+ *   AG_LAYOUT_M_CONTIGUOUS  staged A is additionally written as [K, M]
+ *                           row-major (M fastest) and the GEMM reads it from
+ *                           there; requires M % 8 == 0.
+ * a_gathered is [M, K] row-major in both cases. */
+typedef enum ag_layout { AG_LAYOUT_K_CONTIGUOUS = 0, AG_LAYOUT_M_CONTIGUOUS = 1 } ag_layout;
+
+/* Options of the *_ex entry points.  Start from ag_options_default(). */
+typedef struct ag_options {
+  int32_t dtype;            /* ag_dtype of a_shards, b, a_gathered, out (default bf16) */
+  int32_t layout;           /* ag_layout of the staged A (fused path only; default k-contiguous) */
+  int32_t rank;             /* the local shard, 0 <= rank < D (default 0) */
+  int32_t k_per_flag;       /* 64-column K blocks covered by one ready flag; 0 = 16 */
+  int32_t num_sms;          /* cap on the persistent grid (CTAs); 0 = every SM */
+  int32_t inject_skip_flag; /* fault injection: the producer never publishes this flag index
+                               (-1 = off); the consumer wait then times out */
+  int64_t timeout_ns;       /* limit of one device-side ready-flag wait; 0 = 2 s.  Pipeline
+                               waits inside a CTA use 4x this plus 2 s. */
+  uint64_t* trace;          /* DEVICE buffer for timeline records or NULL; see ag_trace_* */
+  int64_t trace_words;      /* capacity of `trace` in 64-bit words */
+  void* workspace;          /* caller-owned DEVICE workspace or NULL (library-owned) */
+  int64_t workspace_bytes;  /* its size; must be >= ag_workspace_size() */
+} ag_options;
+
+/* Fill `opt` with the defaults listed above.  Never fails (NULL is ignored). */
+void ag_options_default(ag_options* opt);
+
+/* Fused all-gather matmul, bf16, k-contiguous staging, rank 0.
+ * Equivalent to ag_matmul_ex with ag_options_default(). */
+int ag_matmul(const void** a_shards, int D, int m_per_shard, int K, const void* b, int N,
+              const void* bias_or_null, void* a_gathered, void* out, cudaStream_t stream);
+
+/* Barrier baseline: a gather kernel writes a_gathered, then a GEMM kernel
+ * (the same tensor-core mainloop and epilogue, without flags) reads it.
+ * Results are bit-identical to ag_matmul's.  bf16. */
+int ag_then_matmul(const void** a_shards, int D, int m_per_shard, int K, const void* b, int N,
+                   const void* bias_or_null, void* a_gathered, void* out, cudaStream_t stream);
+
+/* As above with options (opt may be NULL for the defaults).  ag_then_matmul_ex
+ * honours dtype, num_sms, timeout_ns and trace; it always gathers into the
+ * [M, K] a_gathered and ignores layout, rank, k_per_flag and the workspace. */
+int ag_matmul_ex(const void** a_shards, int D, int m_per_shard, int K, const void* b, int N,
+                 const void* bias_or_null, void* a_gathered, void* out, cudaStream_t stream,
+                 const ag_options* opt);
+int ag_then_matmul_ex(const void** a_shards, int D, int m_per_shard, int K, const void* b, int N,
+                      const void* bias_or_null, void* a_gathered, void* out, cudaStream_t stream,
+                      const ag_options* opt);
+
+/* Bytes a caller workspace must hold for a fused call of this shape and
+ * these options (flags, plus the [K, M] staging for the m-contiguous layout).
+ * The workspace must be 256-byte aligned and zero-filled before its first use
+ * with this library; after that the library owns its contents.  Returns 0 on
+ * invalid sizes. */
+size_t ag_workspace_size(int D, int m_per_shard, int K, int N, const ag_options* opt);
+
+/* Synchronises `stream`, then reports the newest device-side error recorded
+ * on the current device by a call made since the previous report.  *code is
+ * AG_OK when there is none; *info is the flag index or pipeline site that
+ * timed out.  Either pointer may be NULL.  Returns AG_OK or AG_ERR_CUDA. */
+int ag_get_device_error(cudaStream_t stream, int* code, int* info);
+
+/* Frees the library-owned workspace of the current device (synchronises the
+ * device first).  The next call allocates it again. */
+int ag_release_workspace(void);
+
+/* Static description of a status code; for AG_ERR_CUDA the text of the most
+ * recent CUDA failure seen by this thread.  Never NULL. */
+const char* ag_status_string(int status);
+
+/* Number of SMs the persistent kernels size their grid by on the current
+ * device (0 if no device). */
+int ag_num_sms(void);
+
+/* Timeline records.  When ag_options.trace is set, word 0 of the buffer is an
+ * atomic record counter (the caller zeroes it) and record i occupies words
+ * 1 + 4*i .. 4 + 4*i: {t_start_ns, t_end_ns, meta, 0}, times from the GPU's
+ * global nanosecond timer.  meta = role << 56 | cta << 40 | a << 20 | b with
+ * the roles below.  Records beyond the capacity are dropped (the counter
+ * still counts them). */
+#define AG_TRACE_FETCH 1u  /* producer staged chunk (a = 128-row block, b = k-group) */
+#define AG_TRACE_WAIT 2u   /* consumer waited for a ready flag (a = block, b = k-group) */
+#define AG_TRACE_TILE 3u   /* epilogue stored an output tile (a = row block, b = column block) */
+#define AG_TRACE_GATHER 4u /* barrier path: the gather kernel's CTA ran (a = CTA, b = 0) */
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* AGMM_H_ */

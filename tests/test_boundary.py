@@ -1,0 +1,135 @@
+"""The C-ABI boundary on the CPU: the library builds, loads, exports every
+function include/agmm.h declares, and rejects bad arguments with the
+documented status before touching CUDA (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import all_gather_gemm_gb300 as agmm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "agmm.h")
+
+INVALID, UNSUPPORTED, CUDA, WORKSPACE = 1, 2, 3, 5
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return agmm.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\*?(ag_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_expected_entry_points():
+    names = declared_functions()
+    assert set(agmm.EXPORTS) <= set(names), names
+    assert {"ag_matmul", "ag_then_matmul"} <= set(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_options_default_matches_header(lib):
+    o = agmm.AgOptions()
+    ctypes.memset(ctypes.byref(o), 0x5A, ctypes.sizeof(o))
+    lib.ag_options_default(ctypes.byref(o))
+    assert (o.dtype, o.layout, o.rank, o.k_per_flag, o.num_sms) == (0, 0, 0, 16, 0)
+    assert o.inject_skip_flag == -1 and o.timeout_ns == 2_000_000_000
+    assert not o.trace and o.trace_words == 0 and not o.workspace and o.workspace_bytes == 0
+    assert ctypes.sizeof(o) == 64
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        s = lib.ag_status_string(code)
+        assert isinstance(s, bytes) and s
+    assert lib.ag_status_string(99) == b"unknown status"
+
+
+def test_workspace_size(lib):
+    # 8 row blocks x ceil(128 k-blocks / 16) = 8 flags of 8 bytes, rounded to 1 KiB
+    assert agmm.workspace_size(8, 128, 8192, 3584) == 1024
+    # 128 row blocks x 8 flags x 8 bytes = 8 KiB, plus [K, M] staging for m-contiguous
+    assert agmm.workspace_size(8, 2048, 8192, 3584) == 8192
+    assert agmm.workspace_size(8, 2048, 8192, 3584, "m_contiguous") == 8192 + 16384 * 8192 * 2
+    assert agmm.workspace_size(8, 2048, 8192, 3584, k_per_flag=1) == 128 * 128 * 8
+    assert agmm.workspace_size(0, 1, 8, 8) == 0
+    assert agmm.workspace_size(1, 1, 12, 8) == 0
+
+
+# Fake, well-aligned, non-overlapping "device" addresses: validation rejects
+# these calls before any CUDA call, so nothing is ever dereferenced.
+BASE = 0x7F0000000000
+
+
+def _call(lib, fused=True, D=2, m=128, K=256, N=256, shards=None, b=BASE + (1 << 30),
+          bias=None, ag=BASE + (2 << 30), out=BASE + (3 << 30), opt=None):
+    if shards is None:
+        shards = [BASE + (r << 24) for r in range(D)]
+    return agmm.ag_matmul_raw(fused, shards, D, m, K, b, N, bias, ag, out, None, opt)
+
+
+def opts(**kw):
+    o = agmm.default_options()
+    for k, v in kw.items():
+        setattr(o, k, v)
+    return o
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_invalid_arguments_are_rejected_before_cuda(lib, fused):
+    assert _call(lib, fused, b=0) == INVALID
+    assert _call(lib, fused, ag=0) == INVALID
+    assert _call(lib, fused, out=0) == INVALID
+    assert _call(lib, fused, shards=[BASE, 0]) == INVALID
+    assert _call(lib, fused, D=0, shards=[]) == INVALID
+    assert _call(lib, fused, m=0) == INVALID
+    assert _call(lib, fused, K=0) == INVALID
+    assert _call(lib, fused, K=250) == INVALID           # K % 8
+    assert _call(lib, fused, N=12) == INVALID            # N % 8
+    assert _call(lib, fused, b=BASE + (1 << 30) + 8) == INVALID   # not 16-byte aligned
+    assert _call(lib, fused, shards=[BASE + 4, BASE + (1 << 24)]) == INVALID
+    assert _call(lib, fused, bias=BASE + (4 << 30) + 2) == INVALID  # bias not 4-byte aligned
+    # outputs overlapping inputs or each other
+    assert _call(lib, fused, out=BASE + (2 << 30) + 4096) == INVALID
+    assert _call(lib, fused, ag=BASE + 1024) == INVALID
+    assert _call(lib, fused, out=BASE + (1 << 30)) == INVALID
+    assert _call(lib, fused, opt=opts(rank=2)) == INVALID
+    assert _call(lib, fused, opt=opts(rank=-1)) == INVALID
+    assert _call(lib, fused, opt=opts(dtype=7)) == INVALID
+    assert _call(lib, fused, opt=opts(layout=3)) == INVALID
+    assert _call(lib, fused, opt=opts(timeout_ns=-5)) == INVALID
+    assert _call(lib, fused, opt=opts(k_per_flag=-1)) == INVALID
+    D = 65
+    assert _call(lib, fused, D=D, m=1, shards=[BASE + (r << 24) for r in range(D)]) == UNSUPPORTED
+
+
+def test_m_contiguous_needs_m_multiple_of_8(lib):
+    assert _call(lib, True, D=3, m=3, opt=opts(layout=1)) == UNSUPPORTED
+
+
+def test_valid_call_without_a_gpu_reports_cuda_not_a_crash(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("this check is for hosts without a GPU")
+    assert _call(lib, True) in (CUDA, UNSUPPORTED)
+    assert _call(lib, False) in (CUDA, UNSUPPORTED)
+    assert lib.ag_num_sms() == 0
+    code, info = ctypes.c_int(-1), ctypes.c_int(-1)
+    assert lib.ag_get_device_error(None, ctypes.byref(code), ctypes.byref(info)) == CUDA
+    assert code.value == 0
+
+
+def test_python_binding_fails_loudly_without_cuda_tensors():
+    import torch
+    s = [torch.zeros(4, 8, dtype=torch.bfloat16)]
+    with pytest.raises((ValueError, RuntimeError)):
+        agmm.ag_matmul(s, torch.zeros(8, 8, dtype=torch.bfloat16))

@@ -1,0 +1,301 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+a_gathered must be bit-exact; out must satisfy, elementwise,
+    |out_gpu - out_ref_f32| <= 1e-2 * (|a|.|b|)_ij + 1e-3
+where out_ref_f32 is the oracle's fp32 sum (+ bias) and (|a|.|b|)_ij the sum
+of |a_ik||b_kj|.  At the full benchmark sizes the oracle computes sampled
+rows (shard and tile boundaries plus random rows); everything smaller is
+checked in full.  The fused kernel and the barrier baseline share the MMA
+core and the k order, so their outputs must also be bitwise equal, and so
+must outputs for every choice of local rank and staging layout.
+"""
+import numpy as np
+import pytest
+import torch
+
+import all_gather_gemm_gb300 as agmm
+from all_gather_gemm_gb300 import inputs as inp
+
+pytestmark = pytest.mark.gpu
+
+REL, ATOL = 1e-2, 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+    agmm.library()
+    yield
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def to_device(x: inp.Inputs):
+    shards = [s.cuda() for s in x.shards]
+    b = x.b.cuda()
+    bias = x.bias.cuda() if x.bias is not None else None
+    return shards, b, bias
+
+
+def sample_rows(w: inp.Workload, n_random: int = 24, seed: int = 0) -> np.ndarray:
+    M, m = w.M, w.m_per_shard
+    rows = {0, M - 1}
+    for r in range(w.D):
+        rows |= {r * m, r * m + m - 1, min(M - 1, r * m + m // 2)}
+    for t in (127, 128, 255, 256, M - 128, M - 129):
+        if 0 <= t < M:
+            rows.add(t)
+    rng = np.random.default_rng(seed)
+    rows |= set(int(v) for v in rng.integers(0, M, size=n_random))
+    return np.array(sorted(rows), np.int64)
+
+
+def check(oracle, x: inp.Inputs, a_dev, out_dev, rows=None, what=""):
+    exp_a = oracle.all_gather(x.shard_bits())
+    got_a = bits(a_dev)
+    assert np.array_equal(got_a, exp_a), f"{what}: a_gathered differs at {np.argwhere(got_a != exp_a)[:3]}"
+    ref32, _, _abs, _ = oracle.gemm_rows(exp_a, x.b_bits(), x.bias_np(), dtype=x.workload.dtype,
+                                         rows=rows)
+    got = out_dev if rows is None else out_dev[torch.as_tensor(rows, device=out_dev.device)]
+    got32 = got.float().cpu().numpy()
+    ok, ratio, idx = oracle.within_tolerance(got32, ref32, _abs, REL, ATOL)
+    r = None if idx is None else (int(rows[idx[0]]) if rows is not None else idx[0], idx[1])
+    assert ok, f"{what}: out outside tolerance (worst err/bound {ratio:.3g}) at (row, col) {r}"
+    return ratio
+
+
+def run_both(x, layout="k_contiguous", rank=0, **kw):
+    shards, b, bias = to_device(x)
+    a_f, o_f = agmm.ag_matmul(shards, b, bias, layout=layout, rank=rank, **kw)
+    a_b, o_b = agmm.ag_then_matmul(shards, b, bias)
+    torch.cuda.synchronize()
+    code, info = agmm.device_error()
+    assert code == 0, f"device error {code} info {info:#x}"
+    return (a_f, o_f), (a_b, o_b)
+
+
+def assert_bitwise(t1, t2, what):
+    assert torch.equal(t1.view(torch.int16), t2.view(torch.int16)), what
+
+
+# ---------------------------------------------------------------- the five workloads
+
+def test_small_two_shard(oracle_mod):
+    x = inp.make_inputs(inp.small_two_shard())
+    (a_f, o_f), (a_b, o_b) = run_both(x)
+    check(oracle_mod, x, a_f, o_f, what="fused")
+    check(oracle_mod, x, a_b, o_b, what="barrier")
+    assert_bitwise(o_f, o_b, "fused vs barrier")
+
+
+@pytest.mark.parametrize("n", list(range(256, 4096 + 1, 128)))
+def test_cube_sweep(oracle_mod, n):
+    w = inp.cube(n)
+    x = inp.make_inputs(w)
+    (a_f, o_f), (a_b, o_b) = run_both(x)
+    rows = None if n <= 768 else sample_rows(w, seed=n)
+    check(oracle_mod, x, a_f, o_f, rows, what=f"fused cube {n}")
+    assert_bitwise(a_f, a_b, "a_gathered fused vs barrier")
+    assert_bitwise(o_f, o_b, f"cube {n}: fused vs barrier")
+
+
+@pytest.mark.parametrize("D", [2, 4, 8])
+def test_iris_m1024(oracle_mod, D):
+    w = inp.iris_m1024(D)
+    x = inp.make_inputs(w)
+    (a_f, o_f), (a_b, o_b) = run_both(x)
+    check(oracle_mod, x, a_f, o_f, sample_rows(w, 64, seed=D), what=f"m1024 D={D}")
+    assert_bitwise(o_f, o_b, "fused vs barrier")
+
+
+def test_iris_m16384_both_layouts(oracle_mod):
+    w = inp.iris_m16384()
+    x = inp.make_inputs(w)
+    shards, b, _ = to_device(x)
+    rows = sample_rows(w, 24, seed=16384)
+    a_k, o_k = agmm.ag_matmul(shards, b, layout="k_contiguous")
+    a_m, o_m = agmm.ag_matmul(shards, b, layout="m_contiguous")
+    a_b, o_b = agmm.ag_then_matmul(shards, b)
+    assert agmm.device_error() == (0, 0)
+    check(oracle_mod, x, a_k, o_k, rows, what="k_contiguous")
+    assert_bitwise(a_m, a_k, "a_gathered m vs k")
+    assert_bitwise(o_m, o_k, "out m_contiguous vs k_contiguous")
+    assert_bitwise(o_b, o_k, "out barrier vs fused")
+
+
+def test_iris_m4096_bias_m_contiguous(oracle_mod):
+    w = inp.iris_m4096_bias()
+    x = inp.make_inputs(w)
+    (a_f, o_f), (a_b, o_b) = run_both(x, layout="m_contiguous")
+    check(oracle_mod, x, a_f, o_f, sample_rows(w, 48, seed=4096), what="bias m_contiguous")
+    assert_bitwise(o_f, o_b, "fused vs barrier")
+
+
+# ---------------------------------------------------------------- edge cases
+
+RAGGED = [
+    # (D, m_per_shard, K, N, dtype)
+    (1, 1, 8, 8, "bf16"),
+    (3, 37, 200, 136, "bf16"),
+    (2, 64, 1032, 264, "fp16"),
+    (5, 130, 72, 520, "bf16"),
+    (8, 16, 64, 64, "fp16"),
+    (1, 300, 128, 1000, "bf16"),
+    (7, 100, 3000, 40, "fp16"),
+]
+
+
+@pytest.mark.parametrize("D,m,K,N,dt", RAGGED)
+def test_ragged_shapes(oracle_mod, D, m, K, N, dt):
+    w = inp.Workload(f"ragged_{D}_{m}_{K}_{N}", D=D, m_per_shard=m, K=K, N=N, dtype=dt,
+                     a_dist="uniform", b_dist="uniform", b_scale="one", bias=(D % 2 == 1))
+    x = inp.make_inputs(w)
+    for rank in sorted({0, D - 1}):
+        (a_f, o_f), (a_b, o_b) = run_both(x, rank=rank)
+        check(oracle_mod, x, a_f, o_f, what=f"fused rank {rank}")
+        check(oracle_mod, x, a_b, o_b, what="barrier")
+        assert_bitwise(o_f, o_b, "fused vs barrier")
+        if w.M % 8 == 0:
+            shards, b, bias = to_device(x)
+            a_m, o_m = agmm.ag_matmul(shards, b, bias, layout="m_contiguous", rank=rank)
+            assert agmm.device_error() == (0, 0)
+            assert_bitwise(a_m, a_f, "a_gathered m vs k")
+            assert_bitwise(o_m, o_f, "m_contiguous vs k_contiguous")
+
+
+@pytest.mark.parametrize("dt", ["bf16", "fp16"])
+def test_integer_inputs_exact(oracle_mod, dt):
+    """Integer entries in [-4, 4] and K=256: every partial sum is an exact
+    fp32 integer, so the GPU result must equal the oracle bit for bit."""
+    g = torch.Generator().manual_seed(5)
+    tdt = torch.bfloat16 if dt == "bf16" else torch.float16
+    D, m, K, N = 2, 192, 256, 384
+    a = torch.randint(-4, 5, (D * m, K), generator=g).to(tdt)
+    b = torch.randint(-4, 5, (K, N), generator=g).to(tdt)
+    shards = [a[r * m:(r + 1) * m].contiguous().cuda() for r in range(D)]
+    a_g, out = agmm.ag_matmul(shards, b.cuda(), rank=1)
+    assert agmm.device_error() == (0, 0)
+    exact = (a.to(torch.int64) @ b.to(torch.int64)).to(torch.float32).to(tdt)
+    assert_bitwise(out.cpu(), exact, "integer GEMM")
+    _, _, obits, _ = oracle_mod.ag_matmul([bits(s) for s in shards], bits(b), dtype=dt,
+                                          want_abs=False)
+    assert np.array_equal(bits(out), obits)
+
+
+def test_identity_b_returns_gathered_a():
+    g = torch.Generator().manual_seed(6)
+    D, m, K = 4, 96, 384
+    shards = [torch.randn(m, K, generator=g).to(torch.bfloat16).cuda() for _ in range(D)]
+    eye = torch.eye(K, dtype=torch.bfloat16, device="cuda")
+    a_g, out = agmm.ag_matmul(shards, eye, rank=2)
+    assert agmm.device_error() == (0, 0)
+    assert_bitwise(out, a_g, "a @ I")
+    assert_bitwise(a_g, torch.cat(shards), "a_gathered")
+
+
+def test_rank_invariance(oracle_mod):
+    w = inp.cube(1024)
+    x = inp.make_inputs(w)
+    shards, b, _ = to_device(x)
+    ref_a, ref_o = agmm.ag_matmul(shards, b, rank=0)
+    for rank in (1, 3, 7):
+        for layout in ("k_contiguous", "m_contiguous"):
+            a_r, o_r = agmm.ag_matmul(shards, b, rank=rank, layout=layout)
+            assert agmm.device_error() == (0, 0)
+            assert_bitwise(a_r, ref_a, f"a_gathered rank {rank} {layout}")
+            assert_bitwise(o_r, ref_o, f"out rank {rank} {layout}")
+    check(oracle_mod, x, ref_a, ref_o, sample_rows(w, 16), what="cube 1024 rank 0")
+
+
+@pytest.mark.parametrize("num_sms,kpf", [(1, 16), (3, 1), (7, 4), (0, 2)])
+def test_small_grids_and_flag_granularity(oracle_mod, num_sms, kpf):
+    """Few CTAs (or 1) must still complete: a CTA's own fetch warps stage every
+    chunk its tiles need, so no CTA waits on a CTA that is not running."""
+    w = inp.Workload("grid", D=4, m_per_shard=160, K=1024, N=512, dtype="bf16")
+    x = inp.make_inputs(w)
+    shards, b, _ = to_device(x)
+    for rank in (0, 2):
+        a_f, o_f = agmm.ag_matmul(shards, b, rank=rank, num_sms=num_sms, k_per_flag=kpf)
+        assert agmm.device_error() == (0, 0)
+        check(oracle_mod, x, a_f, o_f, what=f"num_sms={num_sms} kpf={kpf} rank={rank}")
+
+
+def test_repeat_calls_are_deterministic():
+    x = inp.make_inputs(inp.cube(1536))
+    shards, b, _ = to_device(x)
+    a1, o1 = agmm.ag_matmul(shards, b, rank=5)
+    outs = [agmm.ag_matmul(shards, b, rank=5)[1] for _ in range(5)]
+    assert agmm.device_error() == (0, 0)
+    for o in outs:
+        assert_bitwise(o, o1, "repeat")
+
+
+def test_caller_workspace(oracle_mod):
+    w = inp.Workload("ws", D=4, m_per_shard=256, K=512, N=768, dtype="fp16", bias=True)
+    x = inp.make_inputs(w)
+    shards, b, bias = to_device(x)
+    for layout in ("k_contiguous", "m_contiguous"):
+        nbytes = agmm.workspace_size(w.D, w.m_per_shard, w.K, w.N, layout)
+        ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+        ref_a, ref_o = agmm.ag_matmul(shards, b, bias, layout=layout)
+        for _ in range(2):
+            a_w, o_w = agmm.ag_matmul(shards, b, bias, layout=layout, workspace=ws, rank=1)
+            assert agmm.device_error() == (0, 0)
+            assert_bitwise(o_w, ref_o, f"workspace {layout}")
+            assert_bitwise(a_w, ref_a, f"workspace a {layout}")
+        small = torch.zeros(max(nbytes - 1024, 256), dtype=torch.uint8, device="cuda")
+        with pytest.raises(agmm.AgmmError) as e:
+            agmm.ag_matmul(shards, b, bias, layout=layout, workspace=small)
+        assert e.value.status == 5
+    check(oracle_mod, x, ref_a, ref_o, what="workspace")
+
+
+def test_host_pointer_is_rejected():
+    s = [torch.zeros(128, 64, dtype=torch.bfloat16, device="cuda")]
+    b = torch.zeros(64, 64, dtype=torch.bfloat16)  # host memory
+    st = agmm.ag_matmul_raw(True, [s[0].data_ptr()], 1, 128, 64, b.data_ptr(), 64, 0,
+                            torch.empty(128, 64, dtype=torch.bfloat16, device="cuda").data_ptr(),
+                            torch.empty(128, 64, dtype=torch.bfloat16, device="cuda").data_ptr(),
+                            None)
+    assert st == 1
+
+
+# ---------------------------------------------------------------- failure detection
+
+def test_ready_flag_timeout_is_reported_and_context_survives(oracle_mod):
+    """Fault injection on the host side of the protocol: the producer never
+    publishes flag 0 (a row block of the non-local shard), so the consumer's
+    bounded wait runs out; the kernel records AG_ERR_TIMEOUT with the flag
+    index, finishes, and the next call on the same context is correct."""
+    w = inp.Workload("inject", D=2, m_per_shard=128, K=256, N=256, dtype="bf16")
+    x = inp.make_inputs(w)
+    shards, b, _ = to_device(x)
+    agmm.device_error()  # clear anything older
+    agmm.ag_matmul(shards, b, rank=1, inject_skip_flag=0, timeout_ns=20_000_000)
+    code, info = agmm.device_error()
+    assert (code, info) == (4, 0)
+    a_g, out = agmm.ag_matmul(shards, b, rank=1)
+    assert agmm.device_error() == (0, 0)
+    check(oracle_mod, x, a_g, out, what="after timeout")
+
+
+def test_trace_records_overlap_roles():
+    w = inp.cube(2048)
+    x = inp.make_inputs(w)
+    shards, b, _ = to_device(x)
+    tr = torch.zeros(1 + 4 * 8192, dtype=torch.int64, device="cuda")
+    agmm.ag_matmul(shards, b, rank=0, trace=tr)
+    assert agmm.device_error() == (0, 0)
+    t = tr.cpu().numpy().view(np.uint64)
+    n = int(t[0])
+    rec = t[1:1 + 4 * min(n, 8192)].reshape(-1, 4)
+    roles = set(int(r) >> 56 for r in rec[:, 2])
+    assert {1, 2, 3} <= roles
+    assert np.all(rec[:, 1] >= rec[:, 0])
+    fetch = rec[(rec[:, 2] >> np.uint64(56)) == 1]
+    # every (row block, k-group) chunk is staged exactly once
+    num_mb, G = 2048 // 128, (2048 // 64 + 15) // 16
+    keys = ((fetch[:, 2] >> np.uint64(20)) & np.uint64(0xFFFFF)) * np.uint64(G) + (fetch[:, 2] & np.uint64(0xFFFFF))
+    assert sorted(keys.tolist()) == list(range(num_mb * G))
