@@ -24,7 +24,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int64_t kDefaultTimeoutNs = 2000000000LL;
-constexpr int kDefaultKPerFlag = 16;
+constexpr int kDefaultKPerFlag = 4;
 
 thread_local char t_cuda_msg[320] = "no CUDA error recorded on this thread";
 
@@ -100,11 +100,12 @@ int validate(const void** a_shards, int D, int m_per_shard, int K, const void* b
   if (o.layout != AG_LAYOUT_K_CONTIGUOUS && o.layout != AG_LAYOUT_M_CONTIGUOUS)
     return AG_ERR_INVALID_ARG;
   if (o.rank < 0 || o.rank >= D) return AG_ERR_INVALID_ARG;
-  if (o.k_per_flag < 0 || o.num_sms < 0 || o.timeout_ns < 0 || o.trace_words < 0 ||
-      o.workspace_bytes < 0)
+  if (o.k_per_flag < 0 || o.k_per_flag > 65536 || o.num_sms < 0 || o.timeout_ns < 0 ||
+      o.trace_words < 0 || o.workspace_bytes < 0)
     return AG_ERR_INVALID_ARG;
   if (o.trace && (o.trace_words < 1 || !aligned(o.trace, 8))) return AG_ERR_INVALID_ARG;
-  if (fused && o.layout == AG_LAYOUT_M_CONTIGUOUS && (M % 8)) return AG_ERR_UNSUPPORTED;
+  (void)fused;
+  if (o.layout == AG_LAYOUT_M_CONTIGUOUS && (M % 8)) return AG_ERR_UNSUPPORTED;
   if (!aligned(b, 16) || !aligned(a_gathered, 16) || !aligned(out, 16)) return AG_ERR_INVALID_ARG;
   if (bias && !aligned(bias, 4)) return AG_ERR_INVALID_ARG;
   const size_t shard_bytes = (size_t)m_per_shard * K * 2;
@@ -137,8 +138,13 @@ int validate(const void** a_shards, int D, int m_per_shard, int K, const void* b
   return AG_OK;
 }
 
+size_t round_kib(size_t n) { return (n + 1023) & ~size_t(1023); }
+
+// Fused-path metadata: ready flags [num_mb * G], then the per-tile started
+// words [num_mb * num_nb]; both 8 bytes each.
+size_t flags_region(const Shape& s) { return round_kib((size_t)s.num_mb * s.G * 8); }
 size_t flags_bytes(const Shape& s) {
-  return (((size_t)s.num_mb * s.G * 8) + 1023) & ~size_t(1023);
+  return flags_region(s) + round_kib((size_t)s.num_mb * s.num_nb * 8);
 }
 
 // Device pointers must be device (or managed) memory of the current device:
@@ -164,15 +170,19 @@ int device_init(DevState& ds, int dev) {
   ds.sms = sms;
   // The kernels are built for sm_103a only; a missing image is "unsupported".
   cudaFuncAttributes fa;
-  if (cudaFuncGetAttributes(&fa, agmm_gemm_kernel<true>) != cudaSuccess || major != 10) {
+  if (cudaFuncGetAttributes(&fa, agmm_gemm_kernel<kFusedK>) != cudaSuccess || major != 10) {
     cudaGetLastError();
     ds.init = true;
     ds.supported = false;
     return AG_ERR_UNSUPPORTED;
   }
-  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kGemmK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemBytes));
-  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<false>,
+  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kGemmM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes));
+  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kFusedK>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
+  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kFusedM>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
   AG_CK(cudaMalloc(&ds.err, 2 * sizeof(unsigned long long)));
   AG_CK(cudaMemset(ds.err, 0, 2 * sizeof(unsigned long long)));
@@ -181,8 +191,9 @@ int device_init(DevState& ds, int dev) {
   return AG_OK;
 }
 
-int grow_workspace(DevState& ds, const Shape& s, bool need_staging, cudaStream_t stream) {
-  const size_t words = flags_bytes(s) / 8;
+int grow_workspace(DevState& ds, const Shape& s, bool need_flags, bool need_staging,
+                   cudaStream_t stream) {
+  const size_t words = need_flags ? flags_bytes(s) / 8 : 0;
   const size_t stage_elems = need_staging ? (size_t)s.K * s.M : 0;
   if (words > ds.flags_cap || stage_elems > ds.staging_cap) {
     // Older calls may still use the old buffers.
@@ -204,6 +215,14 @@ int grow_workspace(DevState& ds, const Shape& s, bool need_staging, cudaStream_t
     ds.staging_cap = stage_elems;
   }
   return AG_OK;
+}
+
+template <typename Kernel>
+int launch(Kernel k, int grid, int threads, cudaStream_t stream, const GemmParams& p,
+           const char* what) {
+  k<<<grid, threads, kSmemBytes, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? AG_OK : cuda_fail(e, what);
 }
 
 int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
@@ -236,7 +255,6 @@ int run(bool fused, const void** a_shards, int D, int m_per_shard, int K, const 
   Shape s;
   int st = validate(a_shards, D, m_per_shard, K, b, N, bias, a_gathered, out, o, fused, &s);
   if (st != AG_OK) return st;
-  const bool layout_m = fused && o.layout == AG_LAYOUT_M_CONTIGUOUS;
 
   std::lock_guard<std::mutex> lock(g_mu);
   int dev = 0;
@@ -254,24 +272,23 @@ int run(bool fused, const void** a_shards, int D, int m_per_shard, int K, const 
   if (bias && (st = check_device_ptr(bias, dev)) != AG_OK) return st;
   if (o.trace && (st = check_device_ptr(o.trace, dev)) != AG_OK) return st;
 
-  // Workspace: flags (+ [K, M] staging for the m-contiguous layout).
+  // Workspace: flags (fused) and the [K, M] staging (m-contiguous layout).
+  const bool layout_m = o.layout == AG_LAYOUT_M_CONTIGUOUS;
   uint64_t* flags = nullptr;
   uint16_t* staging = nullptr;
-  if (fused) {
-    if (o.workspace) {
-      const size_t need = flags_bytes(s) + (layout_m ? (size_t)s.K * s.M * 2 : 0);
-      if ((size_t)o.workspace_bytes < need) return AG_ERR_WORKSPACE;
-      if (!aligned(o.workspace, 256)) return AG_ERR_INVALID_ARG;
-      if ((st = check_device_ptr(o.workspace, dev)) != AG_OK) return st;
-      flags = static_cast<uint64_t*>(o.workspace);
-      staging = layout_m ? reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(o.workspace) +
-                                                       flags_bytes(s))
-                         : nullptr;
-    } else {
-      if ((st = grow_workspace(ds, s, layout_m, stream)) != AG_OK) return st;
-      flags = ds.flags;
-      staging = layout_m ? ds.staging : nullptr;
-    }
+  if (fused && o.workspace) {
+    const size_t need = flags_bytes(s) + (layout_m ? (size_t)s.K * s.M * 2 : 0);
+    if ((size_t)o.workspace_bytes < need) return AG_ERR_WORKSPACE;
+    if (!aligned(o.workspace, 256)) return AG_ERR_INVALID_ARG;
+    if ((st = check_device_ptr(o.workspace, dev)) != AG_OK) return st;
+    flags = static_cast<uint64_t*>(o.workspace);
+    staging = layout_m ? reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(o.workspace) +
+                                                     flags_bytes(s))
+                       : nullptr;
+  } else if (fused || layout_m) {
+    if ((st = grow_workspace(ds, s, fused, layout_m, stream)) != AG_OK) return st;
+    flags = fused ? ds.flags : nullptr;
+    staging = layout_m ? ds.staging : nullptr;
   }
 
   const uint64_t epoch = g_epoch.fetch_add(1) + 1;
@@ -283,12 +300,23 @@ int run(bool fused, const void** a_shards, int D, int m_per_shard, int K, const 
     memset(&gp, 0, sizeof gp);
     for (int r = 0; r < D; ++r) gp.shards[r] = static_cast<const uint16_t*>(a_shards[r]);
     gp.a_gathered = static_cast<uint16_t*>(a_gathered);
+    gp.staging_mk = staging;
     gp.vec_per_shard = (int64_t)m_per_shard * K / 8;
+    gp.M = (int)s.M;
+    gp.K = K;
+    gp.mps = m_per_shard;
     gp.trace = o.trace;
     gp.trace_words = o.trace_words;
-    const int64_t per_shard_blocks = (gp.vec_per_shard + 255) / 256;
-    int gx = (int)std::max<int64_t>(1, std::min<int64_t>((ds.sms * 4 + D - 1) / D, per_shard_blocks));
-    agmm_gather_kernel<<<dim3(gx, D), 256, 0, stream>>>(gp);
+    if (layout_m) {
+      const int64_t slots = ((s.M / 8 + 15) / 16) * ((K / 8 + 1) / 2) * 32;
+      const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>(ds.sms * 8, (slots + 255) / 256));
+      agmm_gather_mk_kernel<<<blocks, 256, 0, stream>>>(gp);
+    } else {
+      const int64_t per_shard_blocks = (gp.vec_per_shard + 255) / 256;
+      const int gx = (int)std::max<int64_t>(
+          1, std::min<int64_t>((ds.sms * 4 + D - 1) / D, per_shard_blocks));
+      agmm_gather_kernel<<<dim3(gx, D), 256, 0, stream>>>(gp);
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "gather kernel launch");
   }
@@ -299,23 +327,33 @@ int run(bool fused, const void** a_shards, int D, int m_per_shard, int K, const 
   if ((st = make_map(&p.tm_b, b, (uint64_t)N, (uint64_t)K, 64, kBK)) != AG_OK) return st;
   if ((st = make_map(&p.tm_out, out, (uint64_t)N, (uint64_t)s.M, kEpiCols, kEpiRows)) != AG_OK)
     return st;
+  if (layout_m &&
+      (st = make_map(&p.tm_a_mk, staging, (uint64_t)s.M, (uint64_t)K, 64, kBK)) != AG_OK)
+    return st;
   if (fused) {
-    if ((st = make_map(&p.tm_local, a_shards[o.rank], (uint64_t)K, (uint64_t)m_per_shard, kBK,
-                       kBM)) != AG_OK)
-      return st;
-    if (layout_m &&
-        (st = make_map(&p.tm_a_mk, staging, (uint64_t)s.M, (uint64_t)K, 64, kBK)) != AG_OK)
-      return st;
+    // Row blocks that straddle shards are loaded in 8-row boxes when the shard
+    // boundaries fall on multiples of 8 rows.
+    const bool straddle8 = D > 1 && (m_per_shard % kBM) != 0 && (m_per_shard % 8) == 0;
+    for (int r = 0; r < D; ++r) {
+      if ((st = make_map(&p.tm_shard[r], a_shards[r], (uint64_t)K, (uint64_t)m_per_shard, kBK,
+                         kBM)) != AG_OK)
+        return st;
+      if (straddle8 && (st = make_map(&p.tm_shard8[r], a_shards[r], (uint64_t)K,
+                                      (uint64_t)m_per_shard, kBK, 8)) != AG_OK)
+        return st;
+    }
   }
   for (int r = 0; r < D; ++r) p.shards[r] = static_cast<const uint16_t*>(a_shards[r]);
   p.a_gathered = static_cast<uint16_t*>(a_gathered);
   p.staging_mk = staging;
   p.bias = static_cast<const float*>(bias);
   p.flags = flags;
+  p.started = flags ? flags + flags_region(s) / 8 : nullptr;
   p.err = ds.err;
   p.trace = o.trace;
   p.trace_words = o.trace_words;
   p.epoch = epoch;
+  p.fbase = epoch << kFlagShift;
   p.timeout_ns = timeout;
   p.pipe_timeout_ns = 4 * timeout + 2000000000LL;
   p.M = (int)s.M;
@@ -331,18 +369,17 @@ int run(bool fused, const void** a_shards, int D, int m_per_shard, int K, const 
   p.kpf = s.kpf;
   p.G = s.G;
   p.mb_start = fused ? (int)(((int64_t)o.rank * m_per_shard) / kBM) : 0;
-  p.layout_m = layout_m ? 1 : 0;
   p.fp16 = o.dtype == AG_DTYPE_FP16 ? 1 : 0;
   p.inject_skip_flag = fused ? o.inject_skip_flag : -1;
 
   const int grid = std::max(1, std::min(cap, p.num_tiles));
+  if (fused && layout_m)
+    return launch(agmm_gemm_kernel<kFusedM>, grid, mode_threads(kFusedM), stream, p, "fused kernel");
   if (fused)
-    agmm_gemm_kernel<true><<<grid, kFusedThreads, kSmemBytes, stream>>>(p);
-  else
-    agmm_gemm_kernel<false><<<grid, kGemmThreads, kSmemBytes, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, fused ? "fused kernel launch" : "gemm kernel launch");
-  return AG_OK;
+    return launch(agmm_gemm_kernel<kFusedK>, grid, mode_threads(kFusedK), stream, p, "fused kernel");
+  if (layout_m)
+    return launch(agmm_gemm_kernel<kGemmM>, grid, mode_threads(kGemmM), stream, p, "gemm kernel");
+  return launch(agmm_gemm_kernel<kGemmK>, grid, mode_threads(kGemmK), stream, p, "gemm kernel");
 }
 
 }  // namespace
@@ -397,7 +434,9 @@ size_t ag_workspace_size(int D, int m_per_shard, int K, int N, const ag_options*
   Shape s;
   s.M = M;
   s.K = K;
+  s.N = N;
   s.num_mb = (int)((M + kBM - 1) / kBM);
+  s.num_nb = (N + kBN - 1) / kBN;
   s.num_kb = (K + kBK - 1) / kBK;
   s.kpf = o.k_per_flag ? o.k_per_flag : kDefaultKPerFlag;
   s.G = (s.num_kb + s.kpf - 1) / s.kpf;

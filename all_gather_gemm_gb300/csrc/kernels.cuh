@@ -1,27 +1,47 @@
 // Device code of the fused all-gather matmul and of its barrier baseline.
 //
-// The design follows "Fused all-gather+GEMM HBM-buffer kernel for iris.ops"
-// (ROCm/iris #346, section "New kernel"): fetchers copy A tiles into an HBM
-// staging buffer and publish per-tile ready flags; GEMM workers wait on the
-// flags and compute tiles as they arrive.  On sm_103a both roles live in one
-// persistent CTA per SM as specialised warps:
+// The design keeps the protocol of "Fused all-gather+GEMM HBM-buffer kernel
+// for iris.ops" (ROCm/iris #346, section "New kernel") -- A tiles are staged
+// into an HBM buffer, per-tile ready flags are published, GEMM workers wait on
+// the flags and compute tiles as soon as their rows are staged -- and maps it
+// onto one persistent sm_103a CTA per SM with specialised warps:
 //
-//   warp 0      TMA issuer: waits for a tile's ready flag (or takes the local
-//               shard directly), then streams A and B k-blocks into a 4-stage
-//               shared-memory ring with cp.async.bulk.tensor.
-//   warp 1      MMA issuer: tcgen05.mma 128x256x16 (bf16/fp16 in, fp32 out)
-//               into one of two TMEM accumulators (2 x 256 columns).
+//   warp 0      TMA issuer.  Every (row block, k-group) chunk has an owner:
+//               the column block whose tile starts its k-loop there (tiles
+//               of one row block start at evenly spread k-groups).  The
+//               owner loads the chunk straight from the shard that holds it
+//               and has it staged; the other tiles of the row block follow:
+//               they wait on the chunk's ready flag (acquire loads, read one
+//               chunk ahead) and load the staged copy.  Chunks of the local
+//               shard are always read straight from it, never waited on.
+//   warp 1      MMA issuer: tcgen05.mma 128x256x16 (bf16/fp16 in, fp32
+//               accumulate) into one of two TMEM accumulators.
 //   warps 2-5   epilogue: tcgen05.ld, + fp32 bias, round to 16 bits,
 //               128-byte-swizzled shared memory, TMA store of the out tile.
-//   warps 6-7   fetchers (fused kernel only): claim (row block, k-group)
-//               chunks with a CAS on the chunk's flag, copy them from the
-//               shards into a_gathered (and, for the m-contiguous layout,
-//               transposed into the [K, M] staging), then release the flag.
+//   warp 6      stager (fused only): TMA-stores each landed box an owner
+//               loaded into a_gathered (the k-contiguous staging buffer) and,
+//               once every box of the chunk is written, publishes the chunk.
+//   warp 7      register fetcher (fused only): copies chunks that TMA cannot
+//               load from a single shard (a row block straddling shards whose
+//               row count is not a multiple of 8) and publishes them.
+//   warps 8-11  transposers (fused, m-contiguous staging only): write each
+//               owner-loaded box transposed into the [K, M] staging, which is
+//               what followers read; the stager publishes once they are done.
 //
-// Flags are 64-bit and epoch-valued: for a call with epoch e, a flag below
-// 2e-1 is untouched, 2e-1 is claimed and 2e is ready; nothing needs clearing
-// between calls.  Every wait is bounded by a time limit; on expiry the kernel
-// records an error word and finishes without hanging.
+// Each staged box is therefore read from its shard once, by the CTA that also
+// multiplies it ("fetch once, write through"), and no atomic sits on the
+// issuer's path.  If a follower finds a chunk unpublished while its owner
+// tile has not started yet (its CTA is still busy with an earlier tile, or the
+// grid is small), it takes the chunk over: one atom.max decides between
+// competing followers, and the winner loads, stages and publishes it.  A chunk
+// staged twice (owner and taker) is harmless: both write identical bytes and
+// publish the same value, and each publishes only after all of its own writes.
+//
+// Flags are 64-bit.  A call with epoch e uses base = e << 20: a flag below base
+// is untouched by this call, base means taken over, base + boxes means
+// published (ready).  Nothing is cleared between calls.  Every wait is bounded
+// by a time limit; on expiry the kernel records an error word and finishes
+// without hanging.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -42,56 +62,82 @@ constexpr int kBStageBytes = kBN * kBK * 2;  // 32 KB
 constexpr int kStageBytes = kAStageBytes + kBStageBytes;
 constexpr int kMnChunkBytes = 64 * kBK * 2;  // one 64-wide MN chunk of an MN-major operand (8 KB)
 constexpr int kEpiWarps = 4;
-constexpr int kEpiRows = 32;                          // rows per epilogue warp
-constexpr int kEpiCols = 64;                          // columns per store box (128 bytes)
+constexpr int kEpiRows = 32;                           // rows per epilogue warp
+constexpr int kEpiCols = 64;                           // columns per store box (128 bytes)
 constexpr int kEpiBufBytes = kEpiRows * kEpiCols * 2;  // 4 KB
 constexpr int kEpiBufs = 2;
 constexpr int kTmemCols = 2 * kBN;
-constexpr int kFetchWarps = 2;
-constexpr int kGemmThreads = 32 * (2 + kEpiWarps);
-constexpr int kFusedThreads = kGemmThreads + 32 * kFetchWarps;
-constexpr int kMaxShards = 64;
+constexpr int kTransposeWarps = 4;  // one per pipeline stage
+constexpr int kMaxShards = 16;
+constexpr int kFlagShift = 20;      // flag base = epoch << 20; boxes per chunk < 2^20
+constexpr int kStagerLag = 4;       // bulk groups the stager may leave in flight
+
+// Kernel variants: barrier-path GEMM (A from a_gathered or the [K, M] staging)
+// and the fused kernel, each for both staging layouts.
+enum Mode : int { kGemmK = 0, kGemmM = 1, kFusedK = 2, kFusedM = 3 };
+
+__host__ __device__ constexpr bool mode_fused(int m) { return m >= kFusedK; }
+__host__ __device__ constexpr bool mode_layout_m(int m) { return m == kGemmM || m == kFusedM; }
+__host__ __device__ constexpr int mode_threads(int m) {
+  return 32 * (2 + kEpiWarps + (mode_fused(m) ? 2 : 0) + (m == kFusedM ? kTransposeWarps : 0));
+}
+
+// Per-stage record written by the TMA issuer before it arms the stage's full
+// barrier (so readers that waited on that barrier see it).
+constexpr uint32_t kInfoStage = 1u;    // A box is to be stored into a_gathered
+constexpr uint32_t kInfoPublish = 2u;  // ... and its chunk published once staged
+constexpr uint32_t kInfoAmn = 4u;      // A box in shared memory is MN-major
+constexpr uint32_t kInfoLast = 8u;     // last box of its chunk
+
 constexpr int kNumBars = 2 * kStages + 4 + 1;
 constexpr int kSmemData = kStages * kStageBytes + kEpiWarps * kEpiBufs * kEpiBufBytes;
-constexpr int kSmemBytes = 1024 + kSmemData + 8 * kNumBars + 64;
+constexpr int kSmemBytes = 1024 + kSmemData + 8 * kNumBars + 16 * kStages + 4 * kStages + 64;
 static_assert(kSmemBytes <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
 
-// Error codes written to the device error word (match ag_status).
+// Error code written to the device error word (matches ag_status).
 constexpr uint32_t kErrTimeout = 4;
 // Sites reported with a pipeline timeout (ready-flag timeouts report the flag index).
 constexpr uint32_t kSiteEmpty = 0xF00001, kSiteFull = 0xF00002, kSiteTmemEmpty = 0xF00003,
-                   kSiteTmemFull = 0xF00004, kSiteDrain = 0xF00005;
+                   kSiteTmemFull = 0xF00004, kSiteStager = 0xF00005, kSiteTranspose = 0xF00006;
+
+// Trace roles (see include/agmm.h).
+constexpr uint32_t kTraceClaim = 1, kTraceWait = 2, kTraceTile = 3, kTraceGather = 4,
+                   kTraceRegFetch = 5;
 
 struct GemmParams {
-  CUtensorMap tm_a;      // a_gathered [M, K]: box {64, 128}, 128B swizzle (K-major A)
-  CUtensorMap tm_a_mk;   // staging [K, M]: box {64, 64}, 128B swizzle (MN-major A)
-  CUtensorMap tm_local;  // local shard [m_per_shard, K]: box {64, 128}
-  CUtensorMap tm_b;      // b [K, N]: box {64, 64}, 128B swizzle (MN-major B)
-  CUtensorMap tm_out;    // out [M, N]: box {64, 32}, 128B swizzle (store)
+  CUtensorMap tm_a;                    // a_gathered [M, K]: box {64, 128}, 128B swizzle
+  CUtensorMap tm_a_mk;                 // staging [K, M]: box {64, 64}, 128B swizzle
+  CUtensorMap tm_b;                    // b [K, N]: box {64, 64}, 128B swizzle (MN-major B)
+  CUtensorMap tm_out;                  // out [M, N]: box {64, 32}, 128B swizzle (store)
+  CUtensorMap tm_shard[kMaxShards];    // shard r [m_per_shard, K]: box {64, 128}
+  CUtensorMap tm_shard8[kMaxShards];   // shard r: box {64, 8} (row blocks straddling shards)
   const uint16_t* shards[kMaxShards];
   uint16_t* a_gathered;
   uint16_t* staging_mk;
   const float* bias;
-  uint64_t* flags;              // [num_mb * G]
-  unsigned long long* err;      // [2]: epoch of newest error, code << 32 | info
+  uint64_t* flags;          // [num_mb * G]
+  uint64_t* started;        // [num_tiles]: epoch once the tile's issuer began it
+  unsigned long long* err;  // [2]: epoch of newest error, code << 32 | info
   uint64_t* trace;
   int64_t trace_words;
   uint64_t epoch;
-  int64_t timeout_ns;           // one ready-flag wait
-  int64_t pipe_timeout_ns;      // one pipeline (mbarrier) wait
+  uint64_t fbase;           // epoch << kFlagShift
+  int64_t timeout_ns;       // one ready-flag wait
+  int64_t pipe_timeout_ns;  // one pipeline (mbarrier) wait
   int M, N, K, D, mps, rank;
   int num_mb, num_nb, num_kb, num_tiles;
-  int kpf, G;                   // k-blocks per flag, flags per row block
-  int mb_start;                 // first row block of the schedule (ring order)
-  int layout_m;                 // 1: A is read MN-major from the [K, M] staging
-  int fp16;                     // 1: fp16, 0: bf16
-  int inject_skip_flag;
+  int kpf, G;               // k-blocks per flag, flags per row block
+  int mb_start;             // first row block of the schedule (ring order)
+  int fp16;                 // 1: fp16, 0: bf16
+  int inject_skip_flag;     // this flag index is never published (fault injection)
 };
 
 struct GatherParams {
   const uint16_t* shards[kMaxShards];
   uint16_t* a_gathered;
-  int64_t vec_per_shard;  // 16-byte vectors per shard
+  uint16_t* staging_mk;     // [K, M] or null
+  int64_t vec_per_shard;    // 16-byte vectors per shard
+  int M, K, mps;
   uint64_t* trace;
   int64_t trace_words;
 };
@@ -135,11 +181,46 @@ __device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& mb,
   if (mb >= p.num_mb) mb -= p.num_mb;
 }
 
-// A row block is "local" when every row it holds lies in the local shard.
-__device__ __forceinline__ bool block_is_local(const GemmParams& p, int mb) {
-  int lo = mb * kBM;
-  int hi = min(lo + kBM, p.M);
-  return lo >= p.rank * p.mps && hi <= (p.rank + 1) * p.mps;
+__device__ __forceinline__ int my_tile_count(const GemmParams& p) {
+  return p.num_tiles > (int)blockIdx.x ? (p.num_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1
+                                       : 0;
+}
+
+// How a row block's A rows can be fetched.
+enum BlockKind : int { kLocal = 0, kDirect = 1, kRegFetch = 2 };
+
+// Local: every row lies in the local shard.  Direct: one shard holds every
+// row, or the block straddles shards at multiples of 8 rows (8-row TMA boxes).
+// Otherwise the register fetcher stages it.
+__device__ __forceinline__ int block_kind(const GemmParams& p, int mb) {
+  const int lo = mb * kBM;
+  const int hi = min(lo + kBM, p.M);
+  if (lo >= p.rank * p.mps && hi <= (p.rank + 1) * p.mps) return kLocal;
+  if (lo / p.mps == (hi - 1) / p.mps || (p.mps & 7) == 0) return kDirect;
+  return kRegFetch;
+}
+
+// First k-group of every tile in column block nb: the column blocks of a row
+// block start evenly spread over its k-groups.
+__device__ __forceinline__ int chunk_start(const GemmParams& p, int nb) {
+  return (int)(((int64_t)nb * p.G) / p.num_nb);
+}
+
+// The column block whose tiles start at (and so own) k-group g: the nb with
+// chunk_start(nb) <= g < chunk_start(nb + 1).
+__device__ __forceinline__ int owner_nb(const GemmParams& p, int g) {
+  return (int)(((int64_t)(g + 1) * p.num_nb + p.G - 1) / p.G) - 1;
+}
+
+// Schedule index of tile (mb, nb) (inverse of tile_coords).
+__device__ __forceinline__ int tile_index(const GemmParams& p, int mb, int nb) {
+  int pos = mb - p.mb_start;
+  if (pos < 0) pos += p.num_mb;
+  return pos * p.num_nb + nb;
+}
+
+__device__ __forceinline__ int chunk_boxes(const GemmParams& p, int g) {
+  return min(p.kpf, p.num_kb - g * p.kpf);
 }
 
 // Bounded mbarrier wait.  Returns false (after flagging the CTA abort word and
@@ -161,20 +242,26 @@ __device__ __forceinline__ bool wait_bar(const GemmParams& p, uint64_t* bar, uin
   }
 }
 
-// Bounded acquire-wait on a ready flag.  On expiry (or once another wait of
-// this call has expired) it records the error and returns false; the caller
-// then proceeds, so the pipeline always drains.
-__device__ __forceinline__ bool wait_ready(const GemmParams& p, int flag_idx) {
-  const uint64_t ready = 2 * p.epoch;
-  const uint64_t* f = p.flags + flag_idx;
-  if (ld_acquire_gpu(f) >= ready) return true;
+// Follower wait on a chunk: bounded acquire-polling until flag >= target.
+// When the flag is still untouched and the owner tile (owner_tile >= 0) has
+// not started, try to take the chunk over (atom.max to base); returns true if
+// this caller won it (it must then load, stage and publish the chunk).  On
+// expiry (or once another wait of this call has expired) it records the error
+// and returns false; the caller then proceeds, so the pipeline always drains.
+__device__ __forceinline__ bool wait_or_take(const GemmParams& p, int flag_idx, uint64_t target,
+                                             int owner_tile) {
+  uint64_t* f = p.flags + flag_idx;
   const uint64_t t0 = globaltimer_ns();
   uint32_t ns = 32;
-  for (uint32_t it = 1;; ++it) {
+  for (uint32_t it = 0;; ++it) {
+    const uint64_t v = ld_acquire_gpu(f);
+    if (v >= target) return false;
+    if (v < p.fbase && owner_tile >= 0 && ld_relaxed_gpu(p.started + owner_tile) != p.epoch &&
+        atom_max_relaxed_gpu(f, p.fbase) < p.fbase)
+      return true;
     __nanosleep(ns);
     if (ns < 256) ns <<= 1;
-    if (ld_acquire_gpu(f) >= ready) return true;
-    if ((it & 15u) == 0) {
+    if ((it & 15u) == 15u) {
       if (error_this_call(p)) return false;
       if (globaltimer_ns() - t0 > (uint64_t)p.timeout_ns || it > (1u << 26)) {
         record_error(p.err, p.epoch, kErrTimeout, (uint32_t)flag_idx & 0xFFFFFFu);
@@ -188,50 +275,61 @@ __device__ __forceinline__ uint32_t u4_get(const uint4& v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
-__device__ __forceinline__ const uint16_t* shard_row(const GemmParams& p, int grow) {
-  int s = grow / p.mps;
-  int lr = grow - s * p.mps;
-  return p.shards[s] + (int64_t)lr * p.K;
+// 8x8 transpose of 16-bit values held as 8 rows of 16 bytes: column c of the
+// input becomes vector c of the output (word w holds rows 2w, 2w+1).
+__device__ __forceinline__ uint4 transpose_col(const uint4 (&v)[8], int c) {
+  const uint32_t sel = (c & 1) ? 0x7632u : 0x5410u;
+  uint4 o;
+  o.x = __byte_perm(u4_get(v[0], c >> 1), u4_get(v[1], c >> 1), sel);
+  o.y = __byte_perm(u4_get(v[2], c >> 1), u4_get(v[3], c >> 1), sel);
+  o.z = __byte_perm(u4_get(v[4], c >> 1), u4_get(v[5], c >> 1), sel);
+  o.w = __byte_perm(u4_get(v[6], c >> 1), u4_get(v[7], c >> 1), sel);
+  return o;
 }
 
-// Copy one chunk (row block mb, k-group g) from the shards into a_gathered.
-__device__ __noinline__ void fetch_chunk_k(const GemmParams& p, int mb, int g, int lane) {
+__device__ __forceinline__ const uint16_t* shard_row(const uint16_t* const* shards, int mps, int K,
+                                                     int grow) {
+  int s = grow / mps;
+  int lr = grow - s * mps;
+  return shards[s] + (int64_t)lr * K;
+}
+
+// ------------------------------------------------------------------ register fetcher
+
+// Stage one chunk of a row block TMA cannot load from the shards (it straddles
+// shards at a row offset that is not a multiple of 8).  k-contiguous: copy into
+// a_gathered.  m-contiguous: also write it transposed into the [K, M] staging.
+__device__ __noinline__ void regfetch_chunk(const GemmParams& p, int mb, int g, int lane,
+                                            bool layout_m) {
   const int row0 = mb * kBM;
   const int rows = min(kBM, p.M - row0);
   const int c0 = g * p.kpf * kBK;
-  const int nv = min(p.kpf * kBK, p.K - c0) >> 3;  // 16-byte vectors per row
-  const int total = rows * nv;
-  constexpr int U = 8;
-  for (int base = 0; base < total; base += 32 * U) {
-    uint4 v[U];
-    int64_t dst[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int idx = base + u * 32 + lane;
-      dst[u] = -1;
-      if (idx < total) {
-        const int r = idx / nv;
-        const int cv = idx - r * nv;
-        v[u] = ld_stream_v4(shard_row(p, row0 + r) + c0 + cv * 8);
-        dst[u] = (int64_t)(row0 + r) * p.K + c0 + cv * 8;
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u)
-      if (dst[u] >= 0) st_v4(p.a_gathered + dst[u], v[u]);
-  }
-}
-
-// m-contiguous layout: the same chunk, written both to a_gathered ([M, K]) and
-// transposed into the [K, M] staging.  Each lane moves an 8x8 block: 8 row
-// loads of 16 bytes, an in-register transpose with byte permutes, 8 column
-// stores of 16 bytes.  Consecutive lanes take consecutive row groups so the
-// transposed stores are contiguous along M.
-__device__ __noinline__ void fetch_chunk_m(const GemmParams& p, int mb, int g, int lane) {
-  const int row0 = mb * kBM;
-  const int rows = min(kBM, p.M - row0);  // a multiple of 8 (M % 8 == 0)
-  const int c0 = g * p.kpf * kBK;
   const int cols = min(p.kpf * kBK, p.K - c0);
+  if (!layout_m) {
+    const int nv = cols >> 3;  // 16-byte vectors per row
+    const int total = rows * nv;
+    constexpr int U = 8;
+    for (int base = 0; base < total; base += 32 * U) {
+      uint4 v[U];
+      int64_t dst[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int idx = base + u * 32 + lane;
+        dst[u] = -1;
+        if (idx < total) {
+          const int r = idx / nv;
+          const int cv = idx - r * nv;
+          v[u] = ld_stream_v4(shard_row(p.shards, p.mps, p.K, row0 + r) + c0 + cv * 8);
+          dst[u] = (int64_t)(row0 + r) * p.K + c0 + cv * 8;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (dst[u] >= 0) st_v4(p.a_gathered + dst[u], v[u]);
+    }
+    return;
+  }
+  // rows is a multiple of 8 here (M % 8 == 0 for the m-contiguous layout).
   const int nrg = rows >> 3, ncg = cols >> 3;
   const int total = nrg * ncg;
   for (int idx = lane; idx < total; idx += 32) {
@@ -239,59 +337,43 @@ __device__ __noinline__ void fetch_chunk_m(const GemmParams& p, int mb, int g, i
     const int col = c0 + cg * 8;
     uint4 v[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = ld_stream_v4(shard_row(p, row0 + rg * 8 + i) + col);
+    for (int i = 0; i < 8; ++i)
+      v[i] = ld_stream_v4(shard_row(p.shards, p.mps, p.K, row0 + rg * 8 + i) + col);
 #pragma unroll
     for (int i = 0; i < 8; ++i) st_v4(p.a_gathered + (int64_t)(row0 + rg * 8 + i) * p.K + col, v[i]);
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint32_t sel = (c & 1) ? 0x7632u : 0x5410u;
-      uint4 o;
-      o.x = __byte_perm(u4_get(v[0], c >> 1), u4_get(v[1], c >> 1), sel);
-      o.y = __byte_perm(u4_get(v[2], c >> 1), u4_get(v[3], c >> 1), sel);
-      o.z = __byte_perm(u4_get(v[4], c >> 1), u4_get(v[5], c >> 1), sel);
-      o.w = __byte_perm(u4_get(v[6], c >> 1), u4_get(v[7], c >> 1), sel);
-      st_v4(p.staging_mk + (int64_t)(col + c) * p.M + row0 + rg * 8, o);
-    }
+    for (int c = 0; c < 8; ++c)
+      st_v4(p.staging_mk + (int64_t)(col + c) * p.M + row0 + rg * 8, transpose_col(v, c));
   }
 }
 
-// Fetcher warp: walk this CTA's tiles (non-local row blocks first, then the
-// local ones, which nobody waits for but a_gathered must still receive), claim
-// each still-untouched chunk, copy it, publish it.
-__device__ __forceinline__ void fetch_loop(const GemmParams& p, int lane) {
-  const uint64_t claimed = 2 * p.epoch - 1, ready = 2 * p.epoch;
-  for (int pass = 0; pass < 2; ++pass) {
-    int last_mb = -1;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
-      int mb, nb;
-      tile_coords(p, t, mb, nb);
-      if (mb == last_mb) continue;
-      last_mb = mb;
-      if (block_is_local(p, mb) != (pass == 1)) continue;
-      for (int g = 0; g < p.G; ++g) {
-        const int idx = mb * p.G + g;
-        uint64_t* f = p.flags + idx;
-        int won = 0;
-        if (lane == 0) {
-          const uint64_t v = ld_relaxed_gpu(f);
-          if (v < claimed)
-            won = atomicCAS(reinterpret_cast<unsigned long long*>(f), (unsigned long long)v,
-                            (unsigned long long)claimed) == v;
-        }
-        won = __shfl_sync(0xffffffffu, won, 0);
-        if (!won) continue;
-        const uint64_t t0 = p.trace ? globaltimer_ns() : 0;
-        if (p.layout_m)
-          fetch_chunk_m(p, mb, g, lane);
-        else
-          fetch_chunk_k(p, mb, g, lane);
-        __threadfence();
-        fence_proxy_async_global();
-        __syncwarp();
-        if (lane == 0) {
-          if (idx != p.inject_skip_flag) st_release_gpu(f, ready);
-          if (p.trace) trace_rec(p.trace, p.trace_words, 1, mb, g, t0, globaltimer_ns());
-        }
+__device__ __forceinline__ void regfetch_loop(const GemmParams& p, int lane, bool layout_m) {
+  int last_mb = -1;
+  for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+    int mb, nb;
+    tile_coords(p, t, mb, nb);
+    if (mb == last_mb || block_kind(p, mb) != kRegFetch) continue;
+    last_mb = mb;
+    for (int g = 0; g < p.G; ++g) {
+      const int idx = mb * p.G + g;
+      uint64_t* f = p.flags + idx;
+      int won = 0;
+      if (lane == 0) {
+        const uint64_t v = ld_relaxed_gpu(f);
+        if (v < p.fbase)
+          won = atomicCAS(reinterpret_cast<unsigned long long*>(f), (unsigned long long)v,
+                          (unsigned long long)p.fbase) == v;
+      }
+      won = __shfl_sync(0xffffffffu, won, 0);
+      if (!won) continue;
+      const uint64_t t0 = p.trace ? globaltimer_ns() : 0;
+      regfetch_chunk(p, mb, g, lane, layout_m);
+      __threadfence();
+      fence_proxy_async_global();
+      __syncwarp();
+      if (lane == 0) {
+        if (idx != p.inject_skip_flag) red_release_add_gpu(f, (uint64_t)chunk_boxes(p, g));
+        if (p.trace) trace_rec(p.trace, p.trace_words, kTraceRegFetch, mb, g, t0, globaltimer_ns());
       }
     }
   }
@@ -308,44 +390,49 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, int fp16) {
 
 // ------------------------------------------------------------------ the kernel
 
-template <bool kFused>
-__global__ void __launch_bounds__(kFused ? kFusedThreads : kGemmThreads, 1)
+template <int kMode>
+__global__ void __launch_bounds__(mode_threads(kMode), 1)
     agmm_gemm_kernel(const __grid_constant__ GemmParams p) {
+  constexpr bool kFused = mode_fused(kMode);
+  constexpr bool kLayoutM = mode_layout_m(kMode);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* epi_smem = smem + kStages * kStageBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kSmemData);
-  uint64_t* full = bars;                    // [kStages] TMA landed
-  uint64_t* empty = bars + kStages;         // [kStages] MMAs done reading
-  uint64_t* tmem_full = bars + 2 * kStages; // [2] accumulator ready
-  uint64_t* tmem_empty = tmem_full + 2;     // [2] accumulator drained
-  uint64_t* drain = tmem_empty + 2;         // [1] final MMA drain
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* full = bars;                     // [kStages] TMA landed
+  uint64_t* empty = bars + kStages;          // [kStages] every reader of the stage is done
+  uint64_t* tmem_full = bars + 2 * kStages;  // [2] accumulator ready
+  uint64_t* tmem_empty = tmem_full + 2;      // [2] accumulator drained
+  uint64_t* drain = tmem_empty + 2;          // [1] final MMA drain
+  uint32_t* info = reinterpret_cast<uint32_t*>(drain + 1);  // [kStages][4]
+  uint32_t* tprog = info + 4 * kStages;                      // [kTransposeWarps] slots done
+  uint32_t* tmem_slot = tprog + kTransposeWarps;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int my_tiles = my_tile_count(p);
+  const int my_stages = my_tiles * p.num_kb;
 
   if (threadIdx.x == 0) {
+    const uint32_t empty_count = 1 + (kFused ? 1 : 0) + (kMode == kFusedM ? 1 : 0);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], empty_count);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tmem_full[b], 1);
       mbar_init(&tmem_empty[b], 32 * kEpiWarps);
     }
     mbar_init(drain, 1);
+    for (int w = 0; w < kTransposeWarps; ++w) tprog[w] = 0;
     *abort_flag = 0;
     fence_mbarrier_init();
     prefetch_tensormap(&p.tm_a);
     prefetch_tensormap(&p.tm_b);
     prefetch_tensormap(&p.tm_out);
-    if (kFused) {
-      prefetch_tensormap(&p.tm_local);
-      if (p.layout_m) prefetch_tensormap(&p.tm_a_mk);
-    }
+    if (kLayoutM) prefetch_tensormap(&p.tm_a_mk);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -356,50 +443,117 @@ __global__ void __launch_bounds__(kFused ? kFusedThreads : kGemmThreads, 1)
   tcgen05_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
 
-  // Parity of the newest TMA load issued into each stage (drained on abort).
-  uint32_t issued_mask = 0, issued_parity = 0;
-  bool aborted = false;
-
   if (warp == 0) {
     // ---------------------------------------------------------- TMA issuer
     if (lane == 0) {
+      uint32_t issued_mask = 0, issued_parity = 0;
+      bool aborted = false;
       int stage = 0;
       uint32_t phase = 0;
-      for (int t = blockIdx.x; t < p.num_tiles && !aborted; t += gridDim.x) {
-        int mb, nb;
+      // Chunk cursor over this CTA's (tile, k-group) sequence.  Tile (mb, nb)
+      // visits its k-groups starting at chunk_start(nb).  A follower's flag is
+      // read one chunk ahead, so its latency overlaps the current chunk's loads.
+      int t = blockIdx.x, gi = 0, mb = 0, nb = 0, g = 0;
+      uint64_t cur_peek = 0;
+      if (t < p.num_tiles) {
         tile_coords(p, t, mb, nb);
-        const bool local = kFused && block_is_local(p, mb);
-        const bool a_mn = kFused && p.layout_m && !local;
-        int last_g = -1;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        g = chunk_start(p, nb);
+        if (kFused) cur_peek = ld_relaxed_gpu(p.flags + mb * p.G + g);
+      }
+      while (t < p.num_tiles && !aborted) {
+        if (kFused && gi == 0) st_relaxed_gpu(p.started + t, p.epoch);
+        const int flag_idx = mb * p.G + g;
+        const int nbox = chunk_boxes(p, g);
+        const int kind = kFused ? block_kind(p, mb) : kDirect;
+        const bool owner = kFused && owner_nb(p, g) == nb;
+        bool direct = false;  // A straight from a shard (else from the staging)
+        uint32_t bits = 0;
+        if (kFused) {
+          if (kind == kLocal) {
+            direct = true;
+            if (owner) bits = kInfoStage;  // the owner writes the local rows of a_gathered
+          } else if (kind == kDirect && owner) {
+            direct = true;
+            bits = kInfoStage | kInfoPublish;
+          } else {
+            const uint64_t target = p.fbase + (uint64_t)nbox;
+            if (cur_peek >= target) {
+              fence_acq_rel_gpu();  // the relaxed read saw it published: make it an acquire
+            } else {
+              const uint64_t t0 = p.trace ? globaltimer_ns() : 0;
+              const int owner_tile = kind == kDirect ? tile_index(p, mb, owner_nb(p, g)) : -1;
+              if (wait_or_take(p, flag_idx, target, owner_tile)) {
+                direct = true;
+                bits = kInfoStage | kInfoPublish;
+              }
+              if (p.trace) trace_rec(p.trace, p.trace_words, kTraceWait, mb, g, t0, globaltimer_ns());
+            }
+            if (!direct) fence_proxy_async_global();
+          }
+          if ((bits & kInfoStage) && p.trace) {
+            const uint64_t now = globaltimer_ns();
+            trace_rec(p.trace, p.trace_words, kTraceClaim, mb, g, now, now);
+          }
+        }
+        if (!direct && kLayoutM) bits |= kInfoAmn;
+
+        // next chunk in sequence, and a relaxed read of its flag
+        int nt = t, ngi = gi + 1, nmb = mb, nnb = nb, ng = 0;
+        if (ngi == p.G) {
+          ngi = 0;
+          nt += gridDim.x;
+          if (nt < p.num_tiles) tile_coords(p, nt, nmb, nnb);
+        }
+        uint64_t nxt_peek = 0;
+        if (nt < p.num_tiles) {
+          ng = chunk_start(p, nnb) + ngi;
+          if (ng >= p.G) ng -= p.G;
+          if (kFused) nxt_peek = ld_relaxed_gpu(p.flags + nmb * p.G + ng);
+        }
+
+        // single-shard or 8-row-group direct loads
+        int r0 = 0;
+        bool one_shard = true;
+        if (direct) {
+          const int lo = mb * kBM, hi = min(lo + kBM, p.M);
+          r0 = lo / p.mps;
+          one_shard = (hi - 1) / p.mps == r0;
+        }
+        for (int j = 0; j < nbox; ++j) {
+          const int kb = g * p.kpf + j;
           if (!wait_bar(p, &empty[stage], phase ^ 1u, abort_flag, kSiteEmpty)) {
             aborted = true;
             break;
           }
-          if (kFused && !local) {
-            const int g = kb / p.kpf;
-            if (g != last_g) {
-              const uint64_t t0 = p.trace ? globaltimer_ns() : 0;
-              wait_ready(p, mb * p.G + g);
-              fence_proxy_async_global();
-              if (p.trace) trace_rec(p.trace, p.trace_words, 2, mb, g, t0, globaltimer_ns());
-              last_g = g;
-            }
-          }
+          uint32_t* inf = info + 4 * stage;
+          inf[0] = bits | (j == nbox - 1 ? kInfoLast : 0u);
+          inf[1] = (uint32_t)mb;
+          inf[2] = (uint32_t)kb;
+          inf[3] = (uint32_t)flag_idx;
           uint8_t* a_dst = smem + stage * kStageBytes;
           uint8_t* b_dst = a_dst + kAStageBytes;
           mbar_arrive_expect_tx(&full[stage], kStageBytes);
-          if (local) {
-            tma_load_2d(a_dst, &p.tm_local, &full[stage], kb * kBK, mb * kBM - p.rank * p.mps);
-          } else if (a_mn) {
+          if (direct) {
+            if (one_shard) {
+              tma_load_2d(a_dst, &p.tm_shard[r0], &full[stage], kb * kBK, mb * kBM - r0 * p.mps);
+            } else {
+#pragma unroll 1
+              for (int q = 0; q < kBM / 8; ++q) {
+                const int row = mb * kBM + q * 8;
+                const int r = row < p.M ? row / p.mps : p.D - 1;  // past M: zero fill
+                tma_load_2d(a_dst + q * 1024, &p.tm_shard8[r], &full[stage], kb * kBK,
+                            row - r * p.mps);
+              }
+            }
+          } else if (kLayoutM) {
             tma_load_2d(a_dst, &p.tm_a_mk, &full[stage], mb * kBM, kb * kBK);
             tma_load_2d(a_dst + kMnChunkBytes, &p.tm_a_mk, &full[stage], mb * kBM + 64, kb * kBK);
           } else {
             tma_load_2d(a_dst, &p.tm_a, &full[stage], kb * kBK, mb * kBM);
           }
 #pragma unroll
-          for (int j = 0; j < kBN / 64; ++j)
-            tma_load_2d(b_dst + j * kMnChunkBytes, &p.tm_b, &full[stage], nb * kBN + j * 64,
+          for (int q = 0; q < kBN / 64; ++q)
+            tma_load_2d(b_dst + q * kMnChunkBytes, &p.tm_b, &full[stage], nb * kBN + q * 64,
                         kb * kBK);
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -408,6 +562,12 @@ __global__ void __launch_bounds__(kFused ? kFusedThreads : kGemmThreads, 1)
             phase ^= 1u;
           }
         }
+        t = nt;
+        gi = ngi;
+        g = ng;
+        mb = nmb;
+        nb = nnb;
+        cur_peek = nxt_peek;
       }
       if (aborted || *abort_flag) {
         // Let every issued load land before shared memory is released.
@@ -427,15 +587,10 @@ __global__ void __launch_bounds__(kFused ? kFusedThreads : kGemmThreads, 1)
       const uint32_t ab_bf16 = p.fp16 ? 0u : 1u;
       const uint32_t idesc_k = idesc_f16_f32(ab_bf16, 0, 1, kBM, kBN);
       const uint32_t idesc_mn = idesc_f16_f32(ab_bf16, 1, 1, kBM, kBN);
+      bool aborted = false;
       int stage = 0;
       uint32_t phase = 0;
-      int j = 0;
-      for (int t = blockIdx.x; t < p.num_tiles && !aborted; t += gridDim.x, ++j) {
-        int mb, nb;
-        tile_coords(p, t, mb, nb);
-        const bool local = kFused && block_is_local(p, mb);
-        const bool a_mn = kFused && p.layout_m && !local;
-        const uint32_t idesc = a_mn ? idesc_mn : idesc_k;
+      for (int j = 0; j < my_tiles && !aborted; ++j) {
         const int buf = j & 1;
         const uint32_t use = (uint32_t)(j >> 1);
         if (!wait_bar(p, &tmem_empty[buf], (use & 1u) ^ 1u, abort_flag, kSiteTmemEmpty)) {
@@ -450,6 +605,8 @@ __global__ void __launch_bounds__(kFused ? kFusedThreads : kGemmThreads, 1)
             break;
           }
           tcgen05_fence_after_sync();
+          const bool a_mn = (info[4 * stage] & kInfoAmn) != 0;
+          const uint32_t idesc = a_mn ? idesc_mn : idesc_k;
           const uint32_t a_addr = smem_u32(smem + stage * kStageBytes);
           const uint32_t b_addr = a_addr + kAStageBytes;
 #pragma unroll
@@ -483,11 +640,10 @@ __global__ void __launch_bounds__(kFused ? kFusedThreads : kGemmThreads, 1)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     uint8_t* my_bufs = epi_smem + (warp - 2) * kEpiBufs * kEpiBufBytes;
     const uint32_t my_bufs_u32 = smem_u32(my_bufs);
-    int j = 0;
     int chunk_count = 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++j) {
+    for (int j = 0; j < my_tiles; ++j) {
       int mb, nb;
-      tile_coords(p, t, mb, nb);
+      tile_coords(p, blockIdx.x + j * gridDim.x, mb, nb);
       const int buf = j & 1;
       const uint32_t use = (uint32_t)(j >> 1);
       // Every lane waits; the vote keeps the warp converged for tcgen05.ld.
@@ -535,20 +691,158 @@ __global__ void __launch_bounds__(kFused ? kFusedThreads : kGemmThreads, 1)
                        packed[4 * ch + 2], packed[4 * ch + 3]);
         fence_proxy_async_shared();
         __syncwarp();
-        if (lane == 0 && store) {
-          tma_store_2d(&p.tm_out, my_bufs + eb * kEpiBufBytes, n0, m0);
-        }
+        if (lane == 0 && store) tma_store_2d(&p.tm_out, my_bufs + eb * kEpiBufBytes, n0, m0);
         if (lane == 0) bulk_commit_group();
         ++chunk_count;
       }
       if (p.trace && lane == 0 && q == 0)
-        trace_rec(p.trace, p.trace_words, 3, mb, nb, t0, globaltimer_ns());
+        trace_rec(p.trace, p.trace_words, kTraceTile, mb, nb, t0, globaltimer_ns());
     }
     if (lane == 0) bulk_wait_group<0>();
     __syncwarp();
-  } else if (kFused) {
-    // ---------------------------------------------------------- fetchers
-    fetch_loop(p, lane);
+  } else if (kFused && warp == 2 + kEpiWarps) {
+    // ---------------------------------------------------------- stager
+    if (lane == 0) {
+      // k-contiguous: ring of flag indices, one per committed bulk group in
+      // commit order (-1: nothing to publish when that group completes).
+      // m-contiguous: chunks waiting for the transposers, as (flag index,
+      // sequence index of the chunk's last box).
+      int pend[kStagerLag + 1];
+      int npend = 0;
+      int tq_flag[kStages], tq_last[kStages];
+      int ntq = 0;
+      auto publish = [&](int idx) {
+        if (idx >= 0 && idx != p.inject_skip_flag)
+          st_release_gpu(p.flags + idx, p.fbase + (uint64_t)chunk_boxes(p, idx % p.G));
+      };
+      auto flush_groups = [&]() {
+        bulk_wait_group<0>();
+        fence_proxy_async_global();
+        for (int i = 0; i < npend; ++i) publish(pend[i]);
+        npend = 0;
+      };
+      // m-contiguous: box i is transposed once its warp (i % 4) has finished
+      // sequence slot i / 4; per-warp progress is in order, so checking the
+      // chunk's last box of each residue covers the whole chunk.
+      auto transposed = [&](int last, int nbox) -> bool {
+        for (int k = last; k > last - nbox && k > last - kTransposeWarps; --k)
+          if ((int)ld_acquire_cta_shared(smem_u32(tprog + (k % kTransposeWarps))) <=
+              k / kTransposeWarps)
+            return false;
+        return true;
+      };
+      auto drain_tq = [&](bool block) {
+        while (ntq > 0) {
+          const int nbox = chunk_boxes(p, tq_flag[0] % p.G);
+          if (!transposed(tq_last[0], nbox)) {
+            if (!block) return;
+            const uint64_t t0 = globaltimer_ns();
+            while (!transposed(tq_last[0], nbox)) {
+              if (*abort_flag || globaltimer_ns() - t0 > (uint64_t)p.pipe_timeout_ns) return;
+            }
+          }
+          fence_acq_rel_gpu();
+          publish(tq_flag[0]);
+          for (int k = 1; k < ntq; ++k) {
+            tq_flag[k - 1] = tq_flag[k];
+            tq_last[k - 1] = tq_last[k];
+          }
+          --ntq;
+        }
+      };
+      for (int i = 0; i < my_stages; ++i) {
+        const int s = i % kStages;
+        const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+        // Wait for the stage; publish what is pending while idle, so that no
+        // follower waits on a chunk this warp holds back.
+        bool ok = mbar_try_wait(&full[s], ph);
+        if (!ok) {
+          if (npend) flush_groups();
+          if (kLayoutM) drain_tq(true);
+          ok = wait_bar(p, &full[s], ph, abort_flag, kSiteStager);
+        }
+        if (!ok) break;
+        const uint32_t bits = info[4 * s];
+        const int flag_idx = (int)info[4 * s + 3];
+        const bool chunk_done = (bits & kInfoPublish) && (bits & kInfoLast);
+        if (bits & kInfoStage) {
+          tma_store_2d(&p.tm_a, smem + s * kStageBytes, (int)info[4 * s + 2] * kBK,
+                       (int)info[4 * s + 1] * kBM);
+          bulk_commit_group();
+          pend[npend++] = (!kLayoutM && chunk_done) ? flag_idx : -1;
+          bulk_wait_group_read<0>();
+        }
+        mbar_arrive(&empty[s]);
+        if (kLayoutM && chunk_done) {
+          if (ntq == kStages) drain_tq(true);
+          tq_flag[ntq] = flag_idx;
+          tq_last[ntq] = i;
+          ++ntq;
+        }
+        if (npend > kStagerLag) {
+          bulk_wait_group<kStagerLag>();
+          fence_proxy_async_global();
+          const int done = npend - kStagerLag;
+          for (int k = 0; k < done; ++k) publish(pend[k]);
+          for (int k = done; k < npend; ++k) pend[k - done] = pend[k];
+          npend = kStagerLag;
+        }
+        if (kLayoutM) drain_tq(false);
+      }
+      flush_groups();
+      if (kLayoutM) drain_tq(true);
+    }
+    __syncwarp();
+  } else if (kFused && warp == 3 + kEpiWarps) {
+    // ---------------------------------------------------------- register fetcher
+    regfetch_loop(p, lane, kLayoutM);
+    __syncwarp();
+  } else if (kMode == kFusedM) {
+    // ---------------------------------------------------------- transposers
+    // Warp w owns pipeline stage w.  For each box an owner loaded it reads the
+    // landed K-major (128-byte swizzled) tile in 8x8 blocks, transposes them in
+    // registers and writes [K, M] rows of the staging; then it reports its
+    // progress (sequence slots done) to the stager in shared memory.
+    const int w = warp - (4 + kEpiWarps);
+    const int s = w;
+    const uint32_t a_u32 = smem_u32(smem + s * kStageBytes);
+    for (int i = w; i < my_stages; i += kStages) {
+      const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+      const bool ok = wait_bar(p, &full[s], ph, abort_flag, kSiteTranspose);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      const uint32_t bits = info[4 * s];
+      const int mb = (int)info[4 * s + 1], kb = (int)info[4 * s + 2];
+      if (bits & kInfoPublish) {
+        // lane -> (row group rg, column group cg): a warp reads 4 rows x 8
+        // chunks per instruction, the conflict-free pattern for this swizzle.
+        const int cg = lane & 7;
+#pragma unroll 1
+        for (int b = 0; b < 4; ++b) {
+          const int rg = 4 * b + (lane >> 3);
+          uint4 v[8];
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            const int row = rg * 8 + r;
+            v[r] = ld_shared_v4(a_u32 + row * 128 + ((cg ^ (row & 7)) << 4));
+          }
+          const int m = mb * kBM + rg * 8;
+          const int k = kb * kBK + cg * 8;
+          if (m < p.M && k < p.K) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              st_v4(p.staging_mk + (int64_t)(k + c) * p.M + m, transpose_col(v, c));
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        __threadfence();
+        __syncwarp();
+      } else {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+      }
+      if (lane == 0) st_release_cta_shared(smem_u32(tprog + w), (uint32_t)(i / kStages + 1));
+    }
     __syncwarp();
   }
 
@@ -581,11 +875,40 @@ __global__ void __launch_bounds__(256) agmm_gather_kernel(const __grid_constant_
     for (int u = 0; u < U; ++u)
       if (i + u * stride < n) st_v4(dst + i + u * stride, v[u]);
   }
-  if (gp.trace && threadIdx.x == 0) {
-    __syncwarp(1u);
-    trace_rec(gp.trace, gp.trace_words, 4, blockIdx.x + blockIdx.y * gridDim.x, 0, t0,
+  if (gp.trace && threadIdx.x == 0)
+    trace_rec(gp.trace, gp.trace_words, kTraceGather, blockIdx.x + blockIdx.y * gridDim.x, 0, t0,
               globaltimer_ns());
+}
+
+// Barrier-path gather for the m-contiguous layout: a_gathered plus the [K, M]
+// staging.  Thread -> one 8x8 block (8 rows x 8 columns); a warp covers 16
+// consecutive row groups of two column groups so the transposed stores run
+// along M.
+__global__ void __launch_bounds__(256) agmm_gather_mk_kernel(const __grid_constant__ GatherParams gp) {
+  const uint64_t t0 = gp.trace ? globaltimer_ns() : 0;
+  const int nrg = gp.M >> 3, ncg = gp.K >> 3;
+  const int64_t row_blocks = (nrg + 15) / 16, col_pairs = (ncg + 1) / 2;
+  const int64_t total = row_blocks * col_pairs * 32;  // one thread per (16 x 2)-block slot
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += stride) {
+    const int64_t wi = idx >> 5;
+    const int lane = (int)(idx & 31);
+    const int64_t cp = wi / row_blocks;
+    const int rg = (int)((wi - cp * row_blocks) * 16 + (lane & 15));
+    const int cg = (int)(cp * 2 + (lane >> 4));
+    if (rg >= nrg || cg >= ncg) continue;
+    const int col = cg * 8;
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = ld_stream_v4(shard_row(gp.shards, gp.mps, gp.K, rg * 8 + i) + col);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) st_v4(gp.a_gathered + (int64_t)(rg * 8 + i) * gp.K + col, v[i]);
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      st_v4(gp.staging_mk + (int64_t)(col + c) * gp.M + rg * 8, transpose_col(v, c));
   }
+  if (gp.trace && threadIdx.x == 0)
+    trace_rec(gp.trace, gp.trace_words, kTraceGather, blockIdx.x, 0, t0, globaltimer_ns());
 }
 
 }  // namespace agmm

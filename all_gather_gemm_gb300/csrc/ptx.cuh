@@ -119,8 +119,49 @@ __device__ __forceinline__ uint64_t ld_relaxed_gpu(const uint64_t* p) {
   return v;
 }
 
+__device__ __forceinline__ void st_relaxed_gpu(uint64_t* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_release_cta_shared(uint32_t addr, uint32_t v) {
+  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_cta_shared(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void st_release_gpu(uint64_t* p, uint64_t v) {
   asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Relaxed atomic max; returns the old value.  Used to claim a chunk: raising
+// the flag to the call's base value succeeds for exactly one caller.
+__device__ __forceinline__ uint64_t atom_max_relaxed_gpu(uint64_t* p, uint64_t v) {
+  uint64_t old;
+  asm volatile("atom.relaxed.gpu.global.max.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v)
+               : "memory");
+  return old;
+}
+
+__device__ __forceinline__ void red_release_add_gpu(uint64_t* p, uint64_t v) {
+  asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Turns an earlier relaxed read of a flag into an acquire (fence pattern).
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
 }
 
 // 16-byte global load that bypasses L1 allocation (streamed once).

@@ -1,0 +1,384 @@
+"""Benchmark of the fused all-gather matmul on GB300.
+
+One step = one ag_matmul call over the whole workload: the fused persistent
+kernel gathers D row shards into a_gathered and computes out = a_gathered @ b.
+Default workload: M=16384 N=3584 K=8192 fp16 in 8 row shards of 2048x8192
+(the largest shape of the Iris HBM-buffer result tables), k-contiguous
+staging, local rank 0.  Inputs are synthetic and seeded (see
+all_gather_gemm_gb300/inputs.py).
+
+Reported (one JSON line on rank 0):
+  value        fused TFLOPS = 2*M*N*K / mean device time per step (CUDA events
+               around each call on its stream, L2 flushed between steps)
+  ms_per_step  that mean time; barrier_* keys give the gather-then-GEMM
+               baseline (ag_then_matmul) timed the same way, interleaved
+  roofline     achieved TFLOPS of the fused kernel against the measured bf16
+               tensor peak (fp16 runs at the same nominal rate)
+  e2e          the same metric through the public API from pinned host
+               buffers: H2D of the shards and b, the call, D2H of out
+  cpu_baseline the CPU oracle (as it stands) on a bounded row sample
+  clocks       nvidia-smi samples taken during the timed region
+
+--impl reference times the CPU oracle instead (the reference arm of this
+build: there is no installable reference implementation).
+Multi-GPU: replicas only -- under torchrun each rank runs the same problem on
+its own GPU; value = all ranks' FLOPs / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "ag_matmul TFLOPS & µs on 1 GB300 vs tensor peak; speedup over gather-then-GEMM"
+UNIT = "TFLOPS"
+L2_FLUSH_BYTES = 512 << 20
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCES = [os.path.join(ROOT, "all_gather_gemm_gb300", "csrc", f)
+                  for f in ("agmm.cu", "kernels.cuh", "ptx.cuh")]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), \
+            float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+def load_traffic(workload_name: str, layout: str):
+    """Per-launch DRAM bytes of the fused kernel from the committed ncu summary,
+    or None when the kernel sources changed since the capture."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    e = d.get(f"{workload_name}/{layout}")
+    if not e or e.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return int(e["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi samples during the timed region (SM clock, reasons)."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        smax = [num(r[2]) for r in rows if num(r[2]) is not None]
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+def headline_workload(name: str):
+    from all_gather_gemm_gb300 import inputs as inp
+    table = {"m16384_d8": inp.iris_m16384(), "m4096_d8_bias": inp.iris_m4096_bias(),
+             "m1024_d8": inp.iris_m1024(8), "m1024_d2": inp.iris_m1024(2),
+             "m1024_d4": inp.iris_m1024(4), "two_shard_256": inp.small_two_shard(),
+             "cube_4096": inp.cube(4096), "cube_2048": inp.cube(2048)}
+    return table[name]
+
+
+def cpu_baseline(w, rows: int, repeats: int = 1):
+    """The CPU oracle (gather + naive GEMM) on `rows` output rows."""
+    import numpy as np
+
+    import oracle
+    from all_gather_gemm_gb300 import inputs as inp
+    x = inp.make_inputs(w)
+    shard_bits = x.shard_bits()
+    b_bits = x.b_bits()
+    bias = x.bias_np()
+    rng = np.random.default_rng(0)
+    sel = np.sort(rng.choice(w.M, size=min(rows, w.M), replace=False)).astype(np.int64)
+    times, threads = [], 0
+    for _ in range(repeats):
+        t0 = time.perf_counter()
+        a = oracle.all_gather(shard_bits)
+        _, _, _, threads = oracle.gemm_rows(a, b_bits, bias, dtype=w.dtype, rows=sel,
+                                            want_abs=False)
+        times.append(time.perf_counter() - t0)
+    flops = 2.0 * len(sel) * w.N * w.K
+    return flops, times, threads, len(sel)
+
+
+def run_reference(args, w, rank, world):
+    """Reference arm: the CPU oracle as it stands, on bounded row samples."""
+    if rank != 0:
+        return
+    rows = args.reference_rows
+    for _ in range(args.warmup if args.warmup < 1 else 1):
+        cpu_baseline(w, min(rows, 16))
+    flops, times, threads, n = cpu_baseline(w, rows, repeats=args.steps)
+    t = sum(times) / len(times)
+    tflops = flops / t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tflops, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded)",
+        "config": {"workload": f"{w.name}: M={w.M} N={w.N} K={w.K} D={w.D} {w.dtype}",
+                   "sample": f"{n} of {w.M} output rows per step, all N columns"},
+        "cpu_baseline": {"value": tflops, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{n} of {w.M} output rows (gather + naive fp32 GEMM)"},
+        "e2e": {"value": tflops, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="m16384_d8")
+    ap.add_argument("--layout", default="k_contiguous", choices=["k_contiguous", "m_contiguous"])
+    ap.add_argument("--rank-local", type=int, default=0, help="local shard index")
+    ap.add_argument("--cpu-rows", type=int, default=1024, help="oracle rows timed for cpu_baseline")
+    ap.add_argument("--reference-rows", type=int, default=256)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    w = headline_workload(args.workload)
+
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    import all_gather_gemm_gb300 as agmm
+    from all_gather_gemm_gb300 import inputs as inp
+
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl")
+
+    def barrier_sync():
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    agmm.library()
+    x = inp.make_inputs(w)
+    shards = [s.cuda() for s in x.shards]
+    b = x.b.cuda()
+    bias = x.bias.cuda() if x.bias is not None else None
+    a_g = torch.empty((w.M, w.K), dtype=b.dtype, device="cuda")
+    out = torch.empty((w.M, w.N), dtype=b.dtype, device="cuda")
+    a_g2 = torch.empty_like(a_g)
+    out2 = torch.empty_like(out)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def fused():
+        agmm.ag_matmul(shards, b, bias, a_gathered=a_g, out=out, layout=args.layout,
+                       rank=args.rank_local, stream=stream)
+
+    def barrier():
+        agmm.ag_then_matmul(shards, b, bias, a_gathered=a_g2, out=out2, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        fused()
+        barrier()
+    code, info = agmm.device_error()
+    if code != 0:
+        raise SystemExit(f"device error {code} info {info:#x} during warm-up")
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    f_ev = [(ev(), ev()) for _ in range(args.steps)]
+    b_ev = [(ev(), ev()) for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank)
+    barrier_sync()
+    with sampler:
+        barrier_sync()
+        for i in range(args.steps):
+            flush.fill_(i)  # write 512 MB: evicts L2 (129 MB) between timed calls
+            f_ev[i][0].record(stream)
+            fused()
+            f_ev[i][1].record(stream)
+            flush.fill_(i + 1)
+            b_ev[i][0].record(stream)
+            barrier()
+            b_ev[i][1].record(stream)
+        barrier_sync()
+    clocks = sampler.summary()
+    code, info = agmm.device_error()
+    if code != 0:
+        raise SystemExit(f"device error {code} info {info:#x} in the timed region")
+    f_ms = [s.elapsed_time(e) for s, e in f_ev]
+    b_ms = [s.elapsed_time(e) for s, e in b_ev]
+    t_f = sum(f_ms) / len(f_ms)
+    t_b = sum(b_ms) / len(b_ms)
+    if world > 1:
+        tt = torch.tensor([t_f, t_b], device="cuda", dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_f, t_b = tt.tolist()
+
+    # ---------------- end to end through the public API from pinned host memory
+    e2e = None
+    if not args.no_e2e:
+        h_shards = [s.pin_memory() for s in x.shards]
+        h_b = x.b.pin_memory()
+        h_bias = x.bias.pin_memory() if x.bias is not None else None
+        h_out = torch.empty((w.M, w.N), dtype=b.dtype).pin_memory()
+        e_steps = max(3, min(args.steps, 10))
+        e_ev = [(ev(), ev()) for _ in range(e_steps)]
+        barrier_sync()
+        for i in range(e_steps):
+            e_ev[i][0].record(stream)
+            for d, h in zip(shards, h_shards):
+                d.copy_(h, non_blocking=True)
+            b.copy_(h_b, non_blocking=True)
+            if bias is not None:
+                bias.copy_(h_bias, non_blocking=True)
+            fused()
+            h_out.copy_(out, non_blocking=True)
+            e_ev[i][1].record(stream)
+        barrier_sync()
+        t_e = statistics.mean(s.elapsed_time(e) for s, e in e_ev)
+        if world > 1:
+            tt = torch.tensor([t_e], device="cuda", dtype=torch.float64)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            t_e = tt.item()
+        h2d = sum(s.numel() * 2 for s in x.shards) + x.b.numel() * 2 + (
+            x.bias.numel() * 4 if x.bias is not None else 0)
+        e2e = {"value": world * w.flops / (t_e * 1e-3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": w.M * w.N * 2,
+               "ms_per_step": t_e}
+
+    peak_burst, peak_sust, hbm, peak_src = load_peaks()
+    achieved = w.flops / (t_f * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_burst, "unit": "TFLOP/s",
+                "frac": achieved / peak_burst, "traffic": load_traffic(w.name, args.layout),
+                "peak_source": f"{peak_src} bf16 burst (fp16 tensor rate is nominally equal)",
+                "kernel": "agmm_gemm_kernel<true> (fused)"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        flops, times, threads, n = cpu_baseline(w, args.cpu_rows)
+        cpu = {"value": flops / times[0] / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"gather + naive fp32 GEMM on {n} of {w.M} output rows "
+                         f"({times[0]:.1f} s)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": world * w.flops / (t_f * 1e-3) / 1e12,
+            "unit": UNIT,
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": max(args.warmup, 3),
+            "ms_per_step": t_f,
+            "us_per_step": t_f * 1e3,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": w.dtype,
+            "data": "synthetic (seeded normal/uniform, shapes of the Iris result tables)",
+            "config": {"workload": f"{w.name}: M={w.M} N={w.N} K={w.K}, D={w.D} row shards of "
+                                   f"{w.m_per_shard}x{w.K}, {w.dtype}, {args.layout} staging, "
+                                   f"local rank {args.rank_local}",
+                       "l2": "flushed between timed calls (512 MB write)",
+                       "parallelism": "replicas" if world > 1 else "1 GPU"},
+            "barrier_us_per_step": t_b * 1e3,
+            "barrier_tflops": w.flops / (t_b * 1e-3) / 1e12,
+            "speedup_vs_barrier": t_b / t_f,
+            "fused_us_median": statistics.median(f_ms) * 1e3,
+            "barrier_us_median": statistics.median(b_ms) * 1e3,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "clocks": clocks,
+            "gpu_launches": args.steps * 3,
+            "gpu_launches_note": "per step: 1 fused kernel + 2 barrier-baseline kernels",
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -16,10 +16,13 @@
  * "New kernel": optional bias in the epilogue).
  *
  * ag_matmul runs the fused design of that Iris kernel (section "New kernel"
- * and its description): one persistent kernel in which producer warps copy A
- * tiles from the shards into an HBM staging buffer and publish per-tile ready
- * flags, while tensor-core consumer warps wait on those flags and compute each
+ * and its description): one persistent kernel in which A tiles are copied
+ * from the shards into an HBM staging buffer and per-tile ready flags are
+ * published, while tensor-core warps wait on those flags and compute each
  * output tile as soon as its A rows are staged -- no whole-gather barrier.
+ * Here the first CTA that needs a chunk of A loads it from its shard with TMA
+ * for its own MMA and stores that same shared-memory copy into the staging
+ * buffer; the other CTAs wait on the chunk's flag and read the staged copy.
  * Tiles that lie inside the local shard (option `rank`) are read straight from
  * that shard without waiting (the local-tile shortcut described in the Helion
  * PR).  ag_then_matmul is the barrier baseline of the Iris result tables
@@ -54,9 +57,9 @@
  * reports them.  No kernel of this library traps or faults on purpose: every
  * device-side wait is bounded by a time limit.
  *
- * Workspace: the fused path needs per-tile ready flags (8 bytes per
- * (128-row block, k-group)) and, for the m-contiguous layout, a [K, M]
- * staging buffer.  By default the library owns them (one set per device,
+ * Workspace: the fused path needs ready flags (8 bytes per (128-row block,
+ * k-group)) and one word per output tile (8 bytes per 128 x 256 tile); both
+ * paths need a [K, M] staging buffer for the m-contiguous layout.  By default the library owns them (one set per device,
  * grown on demand; growing synchronises the device).  Calls that use the
  * library workspace on the same device must be ordered (same stream, or
  * ordered by events); calls that may overlap on the GPU need separate
@@ -74,7 +77,7 @@
 extern "C" {
 #endif
 
-#define AG_MAX_SHARDS 64
+#define AG_MAX_SHARDS 16
 
 /* Return codes. */
 typedef enum ag_status {
@@ -102,9 +105,9 @@ typedef enum ag_layout { AG_LAYOUT_K_CONTIGUOUS = 0, AG_LAYOUT_M_CONTIGUOUS = 1 
 /* Options of the *_ex entry points.  Start from ag_options_default(). */
 typedef struct ag_options {
   int32_t dtype;            /* ag_dtype of a_shards, b, a_gathered, out (default bf16) */
-  int32_t layout;           /* ag_layout of the staged A (fused path only; default k-contiguous) */
+  int32_t layout;           /* ag_layout of the staged A (default k-contiguous) */
   int32_t rank;             /* the local shard, 0 <= rank < D (default 0) */
-  int32_t k_per_flag;       /* 64-column K blocks covered by one ready flag; 0 = 16 */
+  int32_t k_per_flag;       /* 64-column K blocks covered by one ready flag; 0 = 4 */
   int32_t num_sms;          /* cap on the persistent grid (CTAs); 0 = every SM */
   int32_t inject_skip_flag; /* fault injection: the producer never publishes this flag index
                                (-1 = off); the consumer wait then times out */
@@ -131,8 +134,10 @@ int ag_then_matmul(const void** a_shards, int D, int m_per_shard, int K, const v
                    const void* bias_or_null, void* a_gathered, void* out, cudaStream_t stream);
 
 /* As above with options (opt may be NULL for the defaults).  ag_then_matmul_ex
- * honours dtype, num_sms, timeout_ns and trace; it always gathers into the
- * [M, K] a_gathered and ignores layout, rank, k_per_flag and the workspace. */
+ * honours dtype, layout, num_sms, timeout_ns and trace: with the m-contiguous
+ * layout its gather kernel also writes the [K, M] staging (library-owned) and
+ * the GEMM reads A from there.  It ignores rank, k_per_flag, inject_skip_flag
+ * and the caller workspace. */
 int ag_matmul_ex(const void** a_shards, int D, int m_per_shard, int K, const void* b, int N,
                  const void* bias_or_null, void* a_gathered, void* out, cudaStream_t stream,
                  const ag_options* opt);
@@ -171,10 +176,12 @@ int ag_num_sms(void);
  * global nanosecond timer.  meta = role << 56 | cta << 40 | a << 20 | b with
  * the roles below.  Records beyond the capacity are dropped (the counter
  * still counts them). */
-#define AG_TRACE_FETCH 1u  /* producer staged chunk (a = 128-row block, b = k-group) */
-#define AG_TRACE_WAIT 2u   /* consumer waited for a ready flag (a = block, b = k-group) */
-#define AG_TRACE_TILE 3u   /* epilogue stored an output tile (a = row block, b = column block) */
-#define AG_TRACE_GATHER 4u /* barrier path: the gather kernel's CTA ran (a = CTA, b = 0) */
+#define AG_TRACE_CLAIM 1u    /* a CTA claimed a chunk and loads it from its shard
+                                (a = 128-row block, b = k-group; t_start = t_end) */
+#define AG_TRACE_WAIT 2u     /* a CTA waited for a chunk's ready flag (a = block, b = k-group) */
+#define AG_TRACE_TILE 3u     /* epilogue stored an output tile (a = row block, b = column block) */
+#define AG_TRACE_GATHER 4u   /* barrier path: a gather-kernel CTA ran (a = CTA, b = 0) */
+#define AG_TRACE_REGFETCH 5u /* a chunk TMA cannot address was copied by registers (a, b) */
 
 #ifdef __cplusplus
 }

@@ -41,7 +41,7 @@ def test_options_default_matches_header(lib):
     o = agmm.AgOptions()
     ctypes.memset(ctypes.byref(o), 0x5A, ctypes.sizeof(o))
     lib.ag_options_default(ctypes.byref(o))
-    assert (o.dtype, o.layout, o.rank, o.k_per_flag, o.num_sms) == (0, 0, 0, 16, 0)
+    assert (o.dtype, o.layout, o.rank, o.k_per_flag, o.num_sms) == (0, 0, 0, 4, 0)
     assert o.inject_skip_flag == -1 and o.timeout_ns == 2_000_000_000
     assert not o.trace and o.trace_words == 0 and not o.workspace and o.workspace_bytes == 0
     assert ctypes.sizeof(o) == 64
@@ -55,12 +55,17 @@ def test_status_strings(lib):
 
 
 def test_workspace_size(lib):
-    # 8 row blocks x ceil(128 k-blocks / 16) = 8 flags of 8 bytes, rounded to 1 KiB
-    assert agmm.workspace_size(8, 128, 8192, 3584) == 1024
-    # 128 row blocks x 8 flags x 8 bytes = 8 KiB, plus [K, M] staging for m-contiguous
-    assert agmm.workspace_size(8, 2048, 8192, 3584) == 8192
-    assert agmm.workspace_size(8, 2048, 8192, 3584, "m_contiguous") == 8192 + 16384 * 8192 * 2
-    assert agmm.workspace_size(8, 2048, 8192, 3584, k_per_flag=1) == 128 * 128 * 8
+    # flags: 8 row blocks x (128 k-blocks / 4 per flag) x 8 bytes = 2 KiB;
+    # started words: 8 x 14 tiles x 8 bytes = 896 B -> 1 KiB
+    assert agmm.workspace_size(8, 128, 8192, 3584) == 2048 + 1024
+    # 128 row blocks x 32 flags x 8 bytes = 32 KiB, 128 x 14 tiles x 8 B = 14 KiB,
+    # plus [K, M] staging for m-contiguous
+    assert agmm.workspace_size(8, 2048, 8192, 3584) == 32768 + 14336
+    assert agmm.workspace_size(8, 2048, 8192, 3584, "m_contiguous") == (
+        32768 + 14336 + 16384 * 8192 * 2)
+    assert agmm.workspace_size(8, 2048, 8192, 3584, k_per_flag=1) == 128 * 128 * 8 + 14336
+    assert agmm.workspace_size(8, 2048, 8192, 3584, k_per_flag=16) == 8192 + 14336
+    assert agmm.workspace_size(1, 1, 8, 8) == 2048  # one flag and one tile, 1 KiB each
     assert agmm.workspace_size(0, 1, 8, 8) == 0
     assert agmm.workspace_size(1, 1, 12, 8) == 0
 
@@ -108,12 +113,14 @@ def test_invalid_arguments_are_rejected_before_cuda(lib, fused):
     assert _call(lib, fused, opt=opts(layout=3)) == INVALID
     assert _call(lib, fused, opt=opts(timeout_ns=-5)) == INVALID
     assert _call(lib, fused, opt=opts(k_per_flag=-1)) == INVALID
-    D = 65
+    D = 17  # one more than AG_MAX_SHARDS
     assert _call(lib, fused, D=D, m=1, shards=[BASE + (r << 24) for r in range(D)]) == UNSUPPORTED
+    assert _call(lib, fused, opt=opts(k_per_flag=65537)) == INVALID
 
 
-def test_m_contiguous_needs_m_multiple_of_8(lib):
-    assert _call(lib, True, D=3, m=3, opt=opts(layout=1)) == UNSUPPORTED
+@pytest.mark.parametrize("fused", [True, False])
+def test_m_contiguous_needs_m_multiple_of_8(lib, fused):
+    assert _call(lib, fused, D=3, m=3, opt=opts(layout=1)) == UNSUPPORTED
 
 
 def test_valid_call_without_a_gpu_reports_cuda_not_a_crash(lib):

@@ -69,7 +69,7 @@ def check(oracle, x: inp.Inputs, a_dev, out_dev, rows=None, what=""):
 def run_both(x, layout="k_contiguous", rank=0, **kw):
     shards, b, bias = to_device(x)
     a_f, o_f = agmm.ag_matmul(shards, b, bias, layout=layout, rank=rank, **kw)
-    a_b, o_b = agmm.ag_then_matmul(shards, b, bias)
+    a_b, o_b = agmm.ag_then_matmul(shards, b, bias, layout=layout)
     torch.cuda.synchronize()
     code, info = agmm.device_error()
     assert code == 0, f"device error {code} info {info:#x}"
@@ -118,11 +118,14 @@ def test_iris_m16384_both_layouts(oracle_mod):
     a_k, o_k = agmm.ag_matmul(shards, b, layout="k_contiguous")
     a_m, o_m = agmm.ag_matmul(shards, b, layout="m_contiguous")
     a_b, o_b = agmm.ag_then_matmul(shards, b)
+    a_bm, o_bm = agmm.ag_then_matmul(shards, b, layout="m_contiguous")
     assert agmm.device_error() == (0, 0)
     check(oracle_mod, x, a_k, o_k, rows, what="k_contiguous")
     assert_bitwise(a_m, a_k, "a_gathered m vs k")
     assert_bitwise(o_m, o_k, "out m_contiguous vs k_contiguous")
     assert_bitwise(o_b, o_k, "out barrier vs fused")
+    assert_bitwise(a_bm, a_k, "a_gathered barrier m")
+    assert_bitwise(o_bm, o_k, "out barrier m_contiguous vs fused")
 
 
 def test_iris_m4096_bias_m_contiguous(oracle_mod):
@@ -158,11 +161,11 @@ def test_ragged_shapes(oracle_mod, D, m, K, N, dt):
         check(oracle_mod, x, a_b, o_b, what="barrier")
         assert_bitwise(o_f, o_b, "fused vs barrier")
         if w.M % 8 == 0:
-            shards, b, bias = to_device(x)
-            a_m, o_m = agmm.ag_matmul(shards, b, bias, layout="m_contiguous", rank=rank)
-            assert agmm.device_error() == (0, 0)
+            (a_m, o_m), (a_bm, o_bm) = run_both(x, layout="m_contiguous", rank=rank)
             assert_bitwise(a_m, a_f, "a_gathered m vs k")
             assert_bitwise(o_m, o_f, "m_contiguous vs k_contiguous")
+            assert_bitwise(a_bm, a_f, "barrier a_gathered m vs k")
+            assert_bitwise(o_bm, o_f, "barrier m_contiguous vs k_contiguous")
 
 
 @pytest.mark.parametrize("dt", ["bf16", "fp16"])
@@ -265,11 +268,12 @@ def test_host_pointer_is_rejected():
 # ---------------------------------------------------------------- failure detection
 
 def test_ready_flag_timeout_is_reported_and_context_survives(oracle_mod):
-    """Fault injection on the host side of the protocol: the producer never
-    publishes flag 0 (a row block of the non-local shard), so the consumer's
-    bounded wait runs out; the kernel records AG_ERR_TIMEOUT with the flag
-    index, finishes, and the next call on the same context is correct."""
-    w = inp.Workload("inject", D=2, m_per_shard=128, K=256, N=256, dtype="bf16")
+    """Fault injection: the CTA that stages chunk 0 (row block 0, which lies
+    in the non-local shard) never publishes its flag, so the other CTA that
+    needs that row block runs its bounded wait out; the kernel records
+    AG_ERR_TIMEOUT with the flag index, finishes, and the next call on the
+    same context is correct.  Two column blocks give row block 0 two readers."""
+    w = inp.Workload("inject", D=2, m_per_shard=128, K=256, N=512, dtype="bf16")
     x = inp.make_inputs(w)
     shards, b, _ = to_device(x)
     agmm.device_error()  # clear anything older
@@ -292,10 +296,12 @@ def test_trace_records_overlap_roles():
     n = int(t[0])
     rec = t[1:1 + 4 * min(n, 8192)].reshape(-1, 4)
     roles = set(int(r) >> 56 for r in rec[:, 2])
-    assert {1, 2, 3} <= roles
+    assert {1, 3} <= roles
     assert np.all(rec[:, 1] >= rec[:, 0])
     fetch = rec[(rec[:, 2] >> np.uint64(56)) == 1]
-    # every (row block, k-group) chunk is staged exactly once
-    num_mb, G = 2048 // 128, (2048 // 64 + 15) // 16
+    # every (row block, k-group) chunk is staged by its owner (or a follower
+    # that took it over) at least once
+    num_mb, G = 2048 // 128, 2048 // 64 // 4
     keys = ((fetch[:, 2] >> np.uint64(20)) & np.uint64(0xFFFFF)) * np.uint64(G) + (fetch[:, 2] & np.uint64(0xFFFFF))
-    assert sorted(keys.tolist()) == list(range(num_mb * G))
+    assert set(keys.tolist()) == set(range(num_mb * G))
+    assert len(keys) < 2 * num_mb * G
