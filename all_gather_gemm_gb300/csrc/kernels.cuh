@@ -102,7 +102,7 @@ constexpr uint32_t kSiteEmpty = 0xF00001, kSiteFull = 0xF00002, kSiteTmemEmpty =
 
 // Trace roles (see include/agmm.h).
 constexpr uint32_t kTraceClaim = 1, kTraceWait = 2, kTraceTile = 3, kTraceGather = 4,
-                   kTraceRegFetch = 5;
+                   kTraceRegFetch = 5, kTraceIssue = 6;
 
 struct GemmParams {
   CUtensorMap tm_a;                    // a_gathered [M, K]: box {64, 128}, 128B swizzle
@@ -203,13 +203,13 @@ __device__ __forceinline__ int block_kind(const GemmParams& p, int mb) {
 // First k-group of every tile in column block nb: the column blocks of a row
 // block start evenly spread over its k-groups.
 __device__ __forceinline__ int chunk_start(const GemmParams& p, int nb) {
-  return (int)(((int64_t)nb * p.G) / p.num_nb);
+  return (nb * p.G) / p.num_nb;  // nb * G < 2^31: num_mb * G and num_tiles are bounded
 }
 
 // The column block whose tiles start at (and so own) k-group g: the nb with
 // chunk_start(nb) <= g < chunk_start(nb + 1).
 __device__ __forceinline__ int owner_nb(const GemmParams& p, int g) {
-  return (int)(((int64_t)(g + 1) * p.num_nb + p.G - 1) / p.G) - 1;
+  return ((g + 1) * p.num_nb + p.G - 1) / p.G - 1;
 }
 
 // Schedule index of tile (mb, nb) (inverse of tile_coords).
@@ -221,6 +221,27 @@ __device__ __forceinline__ int tile_index(const GemmParams& p, int mb, int nb) {
 
 __device__ __forceinline__ int chunk_boxes(const GemmParams& p, int g) {
   return min(p.kpf, p.num_kb - g * p.kpf);
+}
+
+// Per-tile facts the TMA issuer needs for every chunk, computed once per tile.
+struct TileCtx {
+  int mb, nb;
+  int kind;        // BlockKind (kDirect for the barrier-path GEMM)
+  int r0;          // shard holding the block's first row
+  bool one_shard;  // every row of the block lies in shard r0
+  int ws, we;      // owned window of k-groups [ws, we); ws is also the k-loop start
+  __device__ __forceinline__ bool owns(int g) const { return g >= ws && g < we; }
+};
+
+template <bool kFused>
+__device__ __forceinline__ void tile_ctx(const GemmParams& p, int t, TileCtx& c) {
+  tile_coords(p, t, c.mb, c.nb);
+  c.ws = chunk_start(p, c.nb);
+  c.we = chunk_start(p, c.nb + 1);
+  c.kind = kFused ? block_kind(p, c.mb) : kDirect;
+  const int lo = c.mb * kBM, hi = min(lo + kBM, p.M);
+  c.r0 = lo / p.mps;
+  c.one_shard = (hi - 1) / p.mps == c.r0;
 }
 
 // Bounded mbarrier wait.  Returns false (after flagging the CTA abort word and
@@ -451,28 +472,36 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
       int stage = 0;
       uint32_t phase = 0;
       // Chunk cursor over this CTA's (tile, k-group) sequence.  Tile (mb, nb)
-      // visits its k-groups starting at chunk_start(nb).  A follower's flag is
-      // read one chunk ahead, so its latency overlaps the current chunk's loads.
-      int t = blockIdx.x, gi = 0, mb = 0, nb = 0, g = 0;
+      // visits its k-groups starting at chunk_start(nb) and owns the window
+      // [chunk_start(nb), chunk_start(nb + 1)).  Everything that needs a
+      // division is computed once per tile; a chunk costs a few adds.  A
+      // follower's flag is read one chunk ahead, so its latency overlaps the
+      // current chunk's loads.
+      TileCtx cur, nxt;
+      int t = blockIdx.x, gi = 0;
       uint64_t cur_peek = 0;
       if (t < p.num_tiles) {
-        tile_coords(p, t, mb, nb);
-        g = chunk_start(p, nb);
-        if (kFused) cur_peek = ld_relaxed_gpu(p.flags + mb * p.G + g);
+        tile_ctx<kFused>(p, t, cur);
+        if (cur.kind != kLocal && !cur.owns(cur.ws))
+          cur_peek = ld_relaxed_gpu(p.flags + cur.mb * p.G + cur.ws);
       }
+      const int last_nbox = chunk_boxes(p, p.G - 1);
       while (t < p.num_tiles && !aborted) {
+        const uint64_t t_chunk = p.trace ? globaltimer_ns() : 0;
         if (kFused && gi == 0) st_relaxed_gpu(p.started + t, p.epoch);
+        int g = cur.ws + gi;
+        if (g >= p.G) g -= p.G;
+        const int mb = cur.mb, nb = cur.nb;
         const int flag_idx = mb * p.G + g;
-        const int nbox = chunk_boxes(p, g);
-        const int kind = kFused ? block_kind(p, mb) : kDirect;
-        const bool owner = kFused && owner_nb(p, g) == nb;
+        const int nbox = g == p.G - 1 ? last_nbox : p.kpf;
+        const int kind = cur.kind;
         bool direct = false;  // A straight from a shard (else from the staging)
         uint32_t bits = 0;
         if (kFused) {
           if (kind == kLocal) {
             direct = true;
-            if (owner) bits = kInfoStage;  // the owner writes the local rows of a_gathered
-          } else if (kind == kDirect && owner) {
+            if (cur.owns(g)) bits = kInfoStage;  // the owner writes the local rows of a_gathered
+          } else if (kind == kDirect && cur.owns(g)) {
             direct = true;
             bits = kInfoStage | kInfoPublish;
           } else {
@@ -497,28 +526,29 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
         }
         if (!direct && kLayoutM) bits |= kInfoAmn;
 
-        // next chunk in sequence, and a relaxed read of its flag
-        int nt = t, ngi = gi + 1, nmb = mb, nnb = nb, ng = 0;
+        // Next chunk in sequence.  Only a follower chunk reads its flag; owner
+        // and local chunks never touch it, so the issuer never stalls on a
+        // load it does not need.
+        int nt = t, ngi = gi + 1;
+        bool new_tile = false;
         if (ngi == p.G) {
           ngi = 0;
           nt += gridDim.x;
-          if (nt < p.num_tiles) tile_coords(p, nt, nmb, nnb);
+          new_tile = true;
+          if (nt < p.num_tiles) tile_ctx<kFused>(p, nt, nxt);
         }
+        const TileCtx& nc = new_tile ? nxt : cur;
         uint64_t nxt_peek = 0;
-        if (nt < p.num_tiles) {
-          ng = chunk_start(p, nnb) + ngi;
+        bool nxt_follow = false;
+        if (kFused && nt < p.num_tiles) {
+          int ng = nc.ws + ngi;
           if (ng >= p.G) ng -= p.G;
-          if (kFused) nxt_peek = ld_relaxed_gpu(p.flags + nmb * p.G + ng);
+          nxt_follow = nc.kind != kLocal && !(nc.kind == kDirect && nc.owns(ng));
+          if (nxt_follow) nxt_peek = ld_relaxed_gpu(p.flags + nc.mb * p.G + ng);
         }
 
-        // single-shard or 8-row-group direct loads
-        int r0 = 0;
-        bool one_shard = true;
-        if (direct) {
-          const int lo = mb * kBM, hi = min(lo + kBM, p.M);
-          r0 = lo / p.mps;
-          one_shard = (hi - 1) / p.mps == r0;
-        }
+        const int r0 = cur.r0;
+        const bool one_shard = cur.one_shard;
         for (int j = 0; j < nbox; ++j) {
           const int kb = g * p.kpf + j;
           if (!wait_bar(p, &empty[stage], phase ^ 1u, abort_flag, kSiteEmpty)) {
@@ -562,12 +592,14 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
             phase ^= 1u;
           }
         }
+        if (p.trace)  // b: k-group | 1 << 16 if loaded from a shard | 2 << 16 if staged here
+          trace_rec(p.trace, p.trace_words, kTraceIssue, mb,
+                    (uint32_t)g | (direct ? 1u << 16 : 0u) | ((bits & kInfoStage) ? 2u << 16 : 0u),
+                    t_chunk, globaltimer_ns());
         t = nt;
         gi = ngi;
-        g = ng;
-        mb = nmb;
-        nb = nnb;
-        cur_peek = nxt_peek;
+        if (new_tile) cur = nxt;
+        if (nxt_follow) cur_peek = nxt_peek;
       }
       if (aborted || *abort_flag) {
         // Let every issued load land before shared memory is released.
