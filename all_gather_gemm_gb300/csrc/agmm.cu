@@ -24,7 +24,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int64_t kDefaultTimeoutNs = 2000000000LL;
-constexpr int kDefaultKPerFlag = 4;
+constexpr int kDefaultKPerFlag = 8;
 
 thread_local char t_cuda_msg[320] = "no CUDA error recorded on this thread";
 

@@ -90,8 +90,10 @@ constexpr uint32_t kInfoAmn = 4u;      // A box in shared memory is MN-major
 constexpr uint32_t kInfoLast = 8u;     // last box of its chunk
 
 constexpr int kNumBars = 2 * kStages + 4 + 1;
+constexpr int kStagerQ = kStagerLag + 1 + 2 * kStages;  // stager queues (ints)
 constexpr int kSmemData = kStages * kStageBytes + kEpiWarps * kEpiBufs * kEpiBufBytes;
-constexpr int kSmemBytes = 1024 + kSmemData + 8 * kNumBars + 16 * kStages + 4 * kStages + 64;
+constexpr int kSmemBytes =
+    1024 + kSmemData + 8 * kNumBars + 16 * kStages + 4 * kTransposeWarps + 4 * kStagerQ + 64;
 static_assert(kSmemBytes <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
 
 // Error code written to the device error word (matches ag_status).
@@ -204,6 +206,17 @@ __device__ __forceinline__ int block_kind(const GemmParams& p, int mb) {
 // block start evenly spread over its k-groups.
 __device__ __forceinline__ int chunk_start(const GemmParams& p, int nb) {
   return (nb * p.G) / p.num_nb;  // nb * G < 2^31: num_mb * G and num_tiles are bounded
+}
+
+// k-group visited at position i of a tile whose owned window is [ws, we): the
+// window first, then every other k-group in ascending order.  After the short
+// owner phase the tiles of a row block walk k in step again (they share A
+// k-slices in L2), and by then every window has been published.
+__device__ __forceinline__ int chunk_at(int i, int ws, int we) {
+  const int wlen = we - ws;
+  if (i < wlen) return ws + i;
+  const int j = i - wlen;
+  return j < ws ? j : j + wlen;
 }
 
 // The column block whose tiles start at (and so own) k-group g: the nb with
@@ -428,7 +441,8 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
   uint64_t* drain = tmem_empty + 2;          // [1] final MMA drain
   uint32_t* info = reinterpret_cast<uint32_t*>(drain + 1);  // [kStages][4]
   uint32_t* tprog = info + 4 * kStages;                      // [kTransposeWarps] slots done
-  uint32_t* tmem_slot = tprog + kTransposeWarps;
+  int* stager_q = reinterpret_cast<int*>(tprog + kTransposeWarps);  // [kStagerQ]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stager_q + kStagerQ);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -472,8 +486,8 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
       int stage = 0;
       uint32_t phase = 0;
       // Chunk cursor over this CTA's (tile, k-group) sequence.  Tile (mb, nb)
-      // visits its k-groups starting at chunk_start(nb) and owns the window
-      // [chunk_start(nb), chunk_start(nb + 1)).  Everything that needs a
+      // owns the window [chunk_start(nb), chunk_start(nb + 1)) and visits it
+      // first (chunk_at).  Everything that needs a
       // division is computed once per tile; a chunk costs a few adds.  A
       // follower's flag is read one chunk ahead, so its latency overlaps the
       // current chunk's loads.
@@ -482,15 +496,15 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
       uint64_t cur_peek = 0;
       if (t < p.num_tiles) {
         tile_ctx<kFused>(p, t, cur);
-        if (cur.kind != kLocal && !cur.owns(cur.ws))
-          cur_peek = ld_relaxed_gpu(p.flags + cur.mb * p.G + cur.ws);
+        const int g0 = chunk_at(0, cur.ws, cur.we);
+        if (cur.kind != kLocal && !cur.owns(g0))
+          cur_peek = ld_relaxed_gpu(p.flags + cur.mb * p.G + g0);
       }
       const int last_nbox = chunk_boxes(p, p.G - 1);
       while (t < p.num_tiles && !aborted) {
         const uint64_t t_chunk = p.trace ? globaltimer_ns() : 0;
         if (kFused && gi == 0) st_relaxed_gpu(p.started + t, p.epoch);
-        int g = cur.ws + gi;
-        if (g >= p.G) g -= p.G;
+        const int g = chunk_at(gi, cur.ws, cur.we);
         const int mb = cur.mb, nb = cur.nb;
         const int flag_idx = mb * p.G + g;
         const int nbox = g == p.G - 1 ? last_nbox : p.kpf;
@@ -507,7 +521,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
           } else {
             const uint64_t target = p.fbase + (uint64_t)nbox;
             if (cur_peek >= target) {
-              fence_acq_rel_gpu();  // the relaxed read saw it published: make it an acquire
+              fence_acquire_gpu();  // the relaxed read saw it published: make it an acquire
             } else {
               const uint64_t t0 = p.trace ? globaltimer_ns() : 0;
               const int owner_tile = kind == kDirect ? tile_index(p, mb, owner_nb(p, g)) : -1;
@@ -537,14 +551,17 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
           new_tile = true;
           if (nt < p.num_tiles) tile_ctx<kFused>(p, nt, nxt);
         }
-        const TileCtx& nc = new_tile ? nxt : cur;
+        // (scalar selects, not a reference: the cursor must stay in registers)
+        const int n_mb = new_tile ? nxt.mb : cur.mb;
+        const int n_kind = new_tile ? nxt.kind : cur.kind;
+        const int n_ws = new_tile ? nxt.ws : cur.ws;
+        const int n_we = new_tile ? nxt.we : cur.we;
         uint64_t nxt_peek = 0;
         bool nxt_follow = false;
         if (kFused && nt < p.num_tiles) {
-          int ng = nc.ws + ngi;
-          if (ng >= p.G) ng -= p.G;
-          nxt_follow = nc.kind != kLocal && !(nc.kind == kDirect && nc.owns(ng));
-          if (nxt_follow) nxt_peek = ld_relaxed_gpu(p.flags + nc.mb * p.G + ng);
+          const int ng = chunk_at(ngi, n_ws, n_we);
+          nxt_follow = n_kind != kLocal && !(n_kind == kDirect && ng >= n_ws && ng < n_we);
+          if (nxt_follow) nxt_peek = ld_relaxed_gpu(p.flags + n_mb * p.G + ng);
         }
 
         const int r0 = cur.r0;
@@ -739,9 +756,12 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
       // commit order (-1: nothing to publish when that group completes).
       // m-contiguous: chunks waiting for the transposers, as (flag index,
       // sequence index of the chunk's last box).
-      int pend[kStagerLag + 1];
-      int npend = 0;
-      int tq_flag[kStages], tq_last[kStages];
+      // (kept in shared memory: a dynamically indexed local array would live
+      // in local memory, which misses to L2 when shared memory takes the L1)
+      int* pend = stager_q;                        // [kStagerLag + 1]
+      int* tq_flag = stager_q + kStagerLag + 1;    // [kStages]
+      int* tq_last = tq_flag + kStages;            // [kStages]
+      int npend = 0, nreal = 0;  // entries, and entries with a flag to publish
       int ntq = 0;
       auto publish = [&](int idx) {
         if (idx >= 0 && idx != p.inject_skip_flag)
@@ -751,7 +771,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
         bulk_wait_group<0>();
         fence_proxy_async_global();
         for (int i = 0; i < npend; ++i) publish(pend[i]);
-        npend = 0;
+        npend = nreal = 0;
       };
       // m-contiguous: box i is transposed once its warp (i % 4) has finished
       // sequence slot i / 4; per-warp progress is in order, so checking the
@@ -773,7 +793,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
               if (*abort_flag || globaltimer_ns() - t0 > (uint64_t)p.pipe_timeout_ns) return;
             }
           }
-          fence_acq_rel_gpu();
+          fence_acquire_gpu();
           publish(tq_flag[0]);
           for (int k = 1; k < ntq; ++k) {
             tq_flag[k - 1] = tq_flag[k];
@@ -789,7 +809,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
         // follower waits on a chunk this warp holds back.
         bool ok = mbar_try_wait(&full[s], ph);
         if (!ok) {
-          if (npend) flush_groups();
+          if (nreal) flush_groups();
           if (kLayoutM) drain_tq(true);
           ok = wait_bar(p, &full[s], ph, abort_flag, kSiteStager);
         }
@@ -801,7 +821,9 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
           tma_store_2d(&p.tm_a, smem + s * kStageBytes, (int)info[4 * s + 2] * kBK,
                        (int)info[4 * s + 1] * kBM);
           bulk_commit_group();
-          pend[npend++] = (!kLayoutM && chunk_done) ? flag_idx : -1;
+          pend[npend] = (!kLayoutM && chunk_done) ? flag_idx : -1;
+          nreal += pend[npend] >= 0;
+          ++npend;
           bulk_wait_group_read<0>();
         }
         mbar_arrive(&empty[s]);
@@ -815,7 +837,10 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
           bulk_wait_group<kStagerLag>();
           fence_proxy_async_global();
           const int done = npend - kStagerLag;
-          for (int k = 0; k < done; ++k) publish(pend[k]);
+          for (int k = 0; k < done; ++k) {
+            nreal -= pend[k] >= 0;
+            publish(pend[k]);
+          }
           for (int k = done; k < npend; ++k) pend[k - done] = pend[k];
           npend = kStagerLag;
         }

@@ -151,8 +151,9 @@ __device__ __forceinline__ void red_release_add_gpu(uint64_t* p, uint64_t v) {
 }
 
 // Turns an earlier relaxed read of a flag into an acquire (fence pattern).
-__device__ __forceinline__ void fence_acq_rel_gpu() {
-  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+// The acquire-only fence does not wait for this thread's earlier stores.
+__device__ __forceinline__ void fence_acquire_gpu() {
+  asm volatile("fence.acquire.gpu;" ::: "memory");
 }
 
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {

@@ -210,7 +210,7 @@ def main():
     ap.add_argument("--workload", default="m16384_d8")
     ap.add_argument("--layout", default="k_contiguous", choices=["k_contiguous", "m_contiguous"])
     ap.add_argument("--rank-local", type=int, default=0, help="local shard index")
-    ap.add_argument("--cpu-rows", type=int, default=1024, help="oracle rows timed for cpu_baseline")
+    ap.add_argument("--cpu-rows", type=int, default=16384, help="oracle rows timed for cpu_baseline")
     ap.add_argument("--reference-rows", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

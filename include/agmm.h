@@ -107,7 +107,7 @@ typedef struct ag_options {
   int32_t dtype;            /* ag_dtype of a_shards, b, a_gathered, out (default bf16) */
   int32_t layout;           /* ag_layout of the staged A (default k-contiguous) */
   int32_t rank;             /* the local shard, 0 <= rank < D (default 0) */
-  int32_t k_per_flag;       /* 64-column K blocks covered by one ready flag; 0 = 4 */
+  int32_t k_per_flag;       /* 64-column K blocks covered by one ready flag; 0 = 8 */
   int32_t num_sms;          /* cap on the persistent grid (CTAs); 0 = every SM */
   int32_t inject_skip_flag; /* fault injection: the producer never publishes this flag index
                                (-1 = off); the consumer wait then times out */

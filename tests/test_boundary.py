@@ -41,7 +41,7 @@ def test_options_default_matches_header(lib):
     o = agmm.AgOptions()
     ctypes.memset(ctypes.byref(o), 0x5A, ctypes.sizeof(o))
     lib.ag_options_default(ctypes.byref(o))
-    assert (o.dtype, o.layout, o.rank, o.k_per_flag, o.num_sms) == (0, 0, 0, 4, 0)
+    assert (o.dtype, o.layout, o.rank, o.k_per_flag, o.num_sms) == (0, 0, 0, 8, 0)
     assert o.inject_skip_flag == -1 and o.timeout_ns == 2_000_000_000
     assert not o.trace and o.trace_words == 0 and not o.workspace and o.workspace_bytes == 0
     assert ctypes.sizeof(o) == 64
@@ -55,14 +55,14 @@ def test_status_strings(lib):
 
 
 def test_workspace_size(lib):
-    # flags: 8 row blocks x (128 k-blocks / 4 per flag) x 8 bytes = 2 KiB;
+    # flags: 8 row blocks x (128 k-blocks / 8 per flag) x 8 bytes = 1 KiB;
     # started words: 8 x 14 tiles x 8 bytes = 896 B -> 1 KiB
-    assert agmm.workspace_size(8, 128, 8192, 3584) == 2048 + 1024
-    # 128 row blocks x 32 flags x 8 bytes = 32 KiB, 128 x 14 tiles x 8 B = 14 KiB,
+    assert agmm.workspace_size(8, 128, 8192, 3584) == 1024 + 1024
+    # 128 row blocks x 16 flags x 8 bytes = 16 KiB, 128 x 14 tiles x 8 B = 14 KiB,
     # plus [K, M] staging for m-contiguous
-    assert agmm.workspace_size(8, 2048, 8192, 3584) == 32768 + 14336
+    assert agmm.workspace_size(8, 2048, 8192, 3584) == 16384 + 14336
     assert agmm.workspace_size(8, 2048, 8192, 3584, "m_contiguous") == (
-        32768 + 14336 + 16384 * 8192 * 2)
+        16384 + 14336 + 16384 * 8192 * 2)
     assert agmm.workspace_size(8, 2048, 8192, 3584, k_per_flag=1) == 128 * 128 * 8 + 14336
     assert agmm.workspace_size(8, 2048, 8192, 3584, k_per_flag=16) == 8192 + 14336
     assert agmm.workspace_size(1, 1, 8, 8) == 2048  # one flag and one tile, 1 KiB each
