@@ -26,12 +26,12 @@ __all__ = [
 ]
 
 STATUS = {0: "AG_OK", 1: "AG_ERR_INVALID_ARG", 2: "AG_ERR_UNSUPPORTED", 3: "AG_ERR_CUDA",
-          4: "AG_ERR_TIMEOUT", 5: "AG_ERR_WORKSPACE"}
+          4: "AG_ERR_TIMEOUT", 5: "AG_ERR_WORKSPACE", 6: "AG_ERR_TOO_LARGE"}
 LAYOUTS = {"k_contiguous": 0, "m_contiguous": 1}
 DTYPES = {"bf16": 0, "fp16": 1}
 EXPORTS = ("ag_options_default", "ag_matmul", "ag_then_matmul", "ag_matmul_ex",
            "ag_then_matmul_ex", "ag_workspace_size", "ag_get_device_error",
-           "ag_release_workspace", "ag_status_string", "ag_num_sms")
+           "ag_release_workspace", "ag_status_string", "ag_num_sms", "ag_matmul_noalloc")
 
 
 class AgmmError(RuntimeError):
@@ -92,6 +92,8 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.ag_status_string.restype = ctypes.c_char_p
     lib.ag_num_sms.argtypes = []
     lib.ag_num_sms.restype = i32
+    lib.ag_matmul_noalloc.argtypes = core + [ctypes.POINTER(AgOptions)]
+    lib.ag_matmul_noalloc.restype = i32
     _lib = lib
     return lib
 

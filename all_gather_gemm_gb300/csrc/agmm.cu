@@ -384,6 +384,154 @@ int run(bool fused, const void** a_shards, int D, int m_per_shard, int K, const 
 
 }  // namespace
 
+// ---------------------------------------------------------------------------
+// ag_matmul_noalloc: the fused kernel with its scratch in a fixed device array
+// (for callers that cannot allocate device memory; see include/agmm.h).
+
+namespace {
+
+constexpr size_t kNoAllocErrBytes = 256;  // error word at the front, 256-byte aligned rest
+
+// Scratch of ag_matmul_noalloc: [error word | ready flags | per-tile words].
+// Zero at module load; every call of every stream on this device shares it.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[AG_NOALLOC_SCRATCH_BYTES];
+
+struct NoAllocState {
+  bool init = false;
+  bool supported = false;
+  int sms = 0;
+  uint8_t* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+  uint64_t reported_epoch = 0;
+};
+NoAllocState g_noalloc[kMaxDevices];
+
+// Once per device, with that device current: check the device, set the fused
+// kernel's shared-memory limit and look up the array's device address (the
+// host-side name of a __device__ array is only a stand-in, never a device
+// pointer).  Allocates nothing.
+int noalloc_setup(NoAllocState& ns, int dev) {
+  if (ns.init) return ns.supported ? AG_OK : AG_ERR_UNSUPPORTED;
+  int major = 0, sms = 0;
+  AG_CK(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev));
+  AG_CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, agmm_gemm_kernel<kFusedK>) != cudaSuccess || major != 10) {
+    cudaGetLastError();
+    ns.init = true;
+    ns.supported = false;
+    return AG_ERR_UNSUPPORTED;
+  }
+  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kFusedK>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
+  void* ptr = nullptr;
+  AG_CK(cudaGetSymbolAddress(&ptr, g_noalloc_scratch));
+  if (!ptr || !aligned(ptr, 256)) {
+    snprintf(t_cuda_msg, sizeof t_cuda_msg, "scratch array has no usable device address");
+    return AG_ERR_CUDA;
+  }
+  ns.sms = sms;
+  ns.scratch = static_cast<uint8_t*>(ptr);
+  ns.init = true;
+  ns.supported = true;
+  return AG_OK;
+}
+
+// Newest unreported error recorded by ag_matmul_noalloc on `dev` (code 0 if
+// none).  The caller holds g_mu and has synchronised the stream.
+int noalloc_take_error(int dev, int* code, int* info) {
+  NoAllocState& ns = g_noalloc[dev];
+  if (!ns.scratch) return AG_OK;
+  unsigned long long host[2];
+  AG_CK(cudaMemcpy(host, ns.scratch, sizeof host, cudaMemcpyDeviceToHost));
+  if (host[0] > ns.reported_epoch) {
+    ns.reported_epoch = host[0];
+    if (code) *code = (int)(host[1] >> 32);
+    if (info) *info = (int)(host[1] & 0xFFFFFFFFull);
+  }
+  return AG_OK;
+}
+
+int run_noalloc(const void** a_shards, int D, int m_per_shard, int K, const void* b, int N,
+                const void* bias, void* a_gathered, void* out, cudaStream_t stream,
+                const ag_options* opt_in) {
+  ag_options o;
+  ag_options_default(&o);
+  if (opt_in) o = *opt_in;
+  if (o.workspace) return AG_ERR_INVALID_ARG;  // the scratch is fixed
+  if (o.layout != AG_LAYOUT_K_CONTIGUOUS) return AG_ERR_UNSUPPORTED;
+  Shape s;
+  int st = validate(a_shards, D, m_per_shard, K, b, N, bias, a_gathered, out, o, true, &s);
+  if (st != AG_OK) return st;
+  if (kNoAllocErrBytes + flags_bytes(s) > (size_t)AG_NOALLOC_SCRATCH_BYTES) return AG_ERR_TOO_LARGE;
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  AG_CK(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices) return AG_ERR_UNSUPPORTED;
+  NoAllocState& ns = g_noalloc[dev];
+  if ((st = noalloc_setup(ns, dev)) != AG_OK) return st;
+  for (int r = 0; r < D; ++r)
+    if ((st = check_device_ptr(a_shards[r], dev)) != AG_OK) return st;
+  if ((st = check_device_ptr(b, dev)) != AG_OK || (st = check_device_ptr(a_gathered, dev)) != AG_OK ||
+      (st = check_device_ptr(out, dev)) != AG_OK)
+    return st;
+  if (bias && (st = check_device_ptr(bias, dev)) != AG_OK) return st;
+  if (o.trace && (st = check_device_ptr(o.trace, dev)) != AG_OK) return st;
+
+  GemmParams p;
+  memset(&p, 0, sizeof p);
+  if ((st = make_map(&p.tm_a, a_gathered, (uint64_t)K, (uint64_t)s.M, kBK, kBM)) != AG_OK) return st;
+  if ((st = make_map(&p.tm_b, b, (uint64_t)N, (uint64_t)K, 64, kBK)) != AG_OK) return st;
+  if ((st = make_map(&p.tm_out, out, (uint64_t)N, (uint64_t)s.M, kEpiCols, kEpiRows)) != AG_OK)
+    return st;
+  const bool straddle8 = D > 1 && (m_per_shard % kBM) != 0 && (m_per_shard % 8) == 0;
+  for (int r = 0; r < D; ++r) {
+    if ((st = make_map(&p.tm_shard[r], a_shards[r], (uint64_t)K, (uint64_t)m_per_shard, kBK,
+                       kBM)) != AG_OK)
+      return st;
+    if (straddle8 && (st = make_map(&p.tm_shard8[r], a_shards[r], (uint64_t)K,
+                                    (uint64_t)m_per_shard, kBK, 8)) != AG_OK)
+      return st;
+  }
+  const uint64_t epoch = g_epoch.fetch_add(1) + 1;
+  const int64_t timeout = o.timeout_ns ? o.timeout_ns : kDefaultTimeoutNs;
+  uint64_t* flags = reinterpret_cast<uint64_t*>(ns.scratch + kNoAllocErrBytes);
+  for (int r = 0; r < D; ++r) p.shards[r] = static_cast<const uint16_t*>(a_shards[r]);
+  p.a_gathered = static_cast<uint16_t*>(a_gathered);
+  p.staging_mk = nullptr;
+  p.bias = static_cast<const float*>(bias);
+  p.flags = flags;
+  p.started = flags + flags_region(s) / 8;
+  p.err = reinterpret_cast<unsigned long long*>(ns.scratch);
+  p.trace = o.trace;
+  p.trace_words = o.trace_words;
+  p.epoch = epoch;
+  p.fbase = epoch << kFlagShift;
+  p.timeout_ns = timeout;
+  p.pipe_timeout_ns = 4 * timeout + 2000000000LL;
+  p.M = (int)s.M;
+  p.N = N;
+  p.K = K;
+  p.D = D;
+  p.mps = m_per_shard;
+  p.rank = o.rank;
+  p.num_mb = s.num_mb;
+  p.num_nb = s.num_nb;
+  p.num_kb = s.num_kb;
+  p.num_tiles = s.num_mb * s.num_nb;
+  p.kpf = s.kpf;
+  p.G = s.G;
+  p.mb_start = (int)(((int64_t)o.rank * m_per_shard) / kBM);
+  p.fp16 = o.dtype == AG_DTYPE_FP16 ? 1 : 0;
+  p.inject_skip_flag = o.inject_skip_flag;
+  const int cap = o.num_sms ? std::min(o.num_sms, ns.sms) : ns.sms;
+  const int grid = std::max(1, std::min(cap, p.num_tiles));
+  return launch(agmm_gemm_kernel<kFusedK>, grid, mode_threads(kFusedK), stream, p,
+                "fused kernel (no-alloc)");
+}
+
+}  // namespace
+
 extern "C" {
 
 void ag_options_default(ag_options* opt) {
@@ -450,7 +598,8 @@ int ag_get_device_error(cudaStream_t stream, int* code, int* info) {
   AG_CK(cudaGetDevice(&dev));
   AG_CK(cudaStreamSynchronize(stream));
   std::lock_guard<std::mutex> lock(g_mu);
-  if (dev < 0 || dev >= kMaxDevices || !g_dev[dev].err) return AG_OK;
+  if (dev < 0 || dev >= kMaxDevices) return AG_OK;
+  if (!g_dev[dev].err) return noalloc_take_error(dev, code, info);
   DevState& ds = g_dev[dev];
   unsigned long long host[2];
   AG_CK(cudaMemcpy(host, ds.err, sizeof host, cudaMemcpyDeviceToHost));
@@ -458,8 +607,9 @@ int ag_get_device_error(cudaStream_t stream, int* code, int* info) {
     ds.reported_epoch = host[0];
     if (code) *code = (int)(host[1] >> 32);
     if (info) *info = (int)(host[1] & 0xFFFFFFFFull);
+    return AG_OK;
   }
-  return AG_OK;
+  return noalloc_take_error(dev, code, info);
 }
 
 int ag_release_workspace(void) {
@@ -486,8 +636,16 @@ const char* ag_status_string(int status) {
     case AG_ERR_CUDA: return t_cuda_msg;
     case AG_ERR_TIMEOUT: return "device-side wait timed out";
     case AG_ERR_WORKSPACE: return "caller workspace too small";
+    case AG_ERR_TOO_LARGE: return "problem needs more than the fixed no-alloc scratch";
     default: return "unknown status";
   }
+}
+
+int ag_matmul_noalloc(const void** a_shards, int D, int m_per_shard, int K, const void* b, int N,
+                      const void* bias_or_null, void* a_gathered, void* out,
+                      cudaStream_t stream, const ag_options* opt) {
+  return run_noalloc(a_shards, D, m_per_shard, K, b, N, bias_or_null, a_gathered, out, stream,
+                     opt);
 }
 
 int ag_num_sms(void) {

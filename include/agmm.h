@@ -86,7 +86,8 @@ typedef enum ag_status {
   AG_ERR_UNSUPPORTED = 2, /* valid request this build cannot run (device, dtype/layout combo, D > AG_MAX_SHARDS) */
   AG_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed; see ag_status_string */
   AG_ERR_TIMEOUT = 4,     /* device-side: a bounded wait ran out (reported by ag_get_device_error) */
-  AG_ERR_WORKSPACE = 5    /* caller workspace smaller than ag_workspace_size() */
+  AG_ERR_WORKSPACE = 5,   /* caller workspace smaller than ag_workspace_size() */
+  AG_ERR_TOO_LARGE = 6    /* problem needs more than ag_matmul_noalloc's fixed scratch */
 } ag_status;
 
 typedef enum ag_dtype { AG_DTYPE_BF16 = 0, AG_DTYPE_FP16 = 1 } ag_dtype;
@@ -169,6 +170,53 @@ const char* ag_status_string(int status);
 /* Number of SMs the persistent kernels size their grid by on the current
  * device (0 if no device). */
 int ag_num_sms(void);
+
+/* Size of the fixed device scratch that ag_matmul_noalloc uses (see below). */
+#define AG_NOALLOC_SCRATCH_BYTES (256 * 1024)
+
+/* ag_matmul_noalloc -- the fused all-gather matmul for callers that cannot
+ * allocate device memory.  (No counterpart on the pages: this is a library
+ * convenience, not part of the method.)
+ *
+ * Who needs it: code that must not call cudaMalloc/cudaFree (or any routine
+ * that may allocate, torch's caching allocator included) when it runs --
+ * e.g. a host framework that plans and owns every device allocation up
+ * front, or a latency-critical loop where an allocation's implicit device
+ * synchronisation is not acceptable.  ag_matmul may allocate: its first call
+ * on a device creates the error word and the flag workspace, and a larger
+ * problem later grows the workspace.
+ *
+ * What it does: exactly what ag_matmul_ex does for the k-contiguous layout
+ * (same kernel, same results bit for bit), but the kernel's scratch -- its
+ * error word, the ready flags and the per-tile words -- lives in one
+ * file-scope device array of AG_NOALLOC_SCRATCH_BYTES bytes inside this
+ * library.  Every GPU that loads the library holds that array until the
+ * process exits.  The caller still passes (and owns) every input and output.
+ *
+ * Limits and errors: ag_options.layout must be AG_LAYOUT_K_CONTIGUOUS
+ * (m-contiguous staging needs K * M * 2 bytes; AG_ERR_UNSUPPORTED otherwise)
+ * and ag_options.workspace must be NULL (AG_ERR_INVALID_ARG).  A problem whose
+ * scratch -- 256 bytes plus ag_workspace_size() for the k-contiguous layout --
+ * exceeds AG_NOALLOC_SCRATCH_BYTES is rejected with AG_ERR_TOO_LARGE before
+ * anything is enqueued.  With the default k_per_flag of 8 that admits, for
+ * example, M = 16384, N = 3584, K = 8192 (about 30 KB of scratch).  All other
+ * arguments and errors are as for ag_matmul_ex; device-side timeouts are
+ * reported by ag_get_device_error.
+ *
+ * Sharing: every call on a device uses the same array, which keeps the last
+ * call's contents.  Nothing in it needs clearing between calls: flags and
+ * per-tile words carry the call's epoch, so values left by earlier calls
+ * read as untouched.  Calls whose kernels may overlap on the GPU (different
+ * streams without ordering) race on the array and give wrong results; order
+ * them on one stream or with events.
+ *
+ * Set-up: the first call on each device (with that device current) looks up
+ * the array's device address once and sets the kernel's shared-memory limit;
+ * make that first call before any stream capture begins.  The call itself
+ * performs no device allocation or free. */
+int ag_matmul_noalloc(const void** a_shards, int D, int m_per_shard, int K, const void* b, int N,
+                      const void* bias_or_null, void* a_gathered, void* out,
+                      cudaStream_t stream, const ag_options* opt);
 
 /* Timeline records.  When ag_options.trace is set, word 0 of the buffer is an
  * atomic record counter (the caller zeroes it) and record i occupies words
