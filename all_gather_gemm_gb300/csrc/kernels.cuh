@@ -130,6 +130,8 @@ struct GemmParams {
   int num_mb, num_nb, num_kb, num_tiles;
   int kpf, G;               // k-blocks per flag, flags per row block
   int mb_start;             // first row block of the schedule (ring order)
+  int ng;                   // column blocks per schedule pass
+  int w0;                   // column blocks of the first pass (they own the chunks)
   int fp16;                 // 1: fp16, 0: bf16
   int inject_skip_flag;     // this flag index is never published (fault injection)
 };
@@ -172,13 +174,21 @@ __device__ __forceinline__ void trace_rec(uint64_t* tr, int64_t words, uint32_t 
   tr[w + 3] = 0;
 }
 
-// Persistent schedule: tile t -> (row block, column block).  Row blocks are
-// visited in ring order starting at mb_start (the local shard's first block
-// for the fused kernel), all column blocks of one row block consecutively, so
-// concurrently running CTAs share A rows in L2 and sweep b.
+// Persistent schedule: tile t -> (row block, column block).  Column blocks
+// are taken in groups of ng: a pass sweeps every row block over one group, so
+// only that group's columns of b need to stay in L2 during the pass (A is read
+// once per group).  Within a pass, row blocks are visited in ring order
+// starting at mb_start (the local shard's first block for the fused kernel),
+// the group's column blocks of one row block consecutively, so concurrently
+// running CTAs share A rows in L2.
 __device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& mb, int& nb) {
-  int pos = t / p.num_nb;
-  nb = t - pos * p.num_nb;
+  const int per_pass = p.num_mb * p.ng;
+  const int gq = t / per_pass;
+  const int g0 = gq * p.ng;
+  const int width = min(p.ng, p.num_nb - g0);
+  const int r = t - gq * per_pass;
+  const int pos = r / width;
+  nb = g0 + (r - pos * width);
   mb = p.mb_start + pos;
   if (mb >= p.num_mb) mb -= p.num_mb;
 }
@@ -205,7 +215,13 @@ __device__ __forceinline__ int block_kind(const GemmParams& p, int mb) {
 // First k-group of every tile in column block nb: the column blocks of a row
 // block start evenly spread over its k-groups.
 __device__ __forceinline__ int chunk_start(const GemmParams& p, int nb) {
-  return (nb * p.G) / p.num_nb;  // nb * G < 2^31: num_mb * G and num_tiles are bounded
+  // nb * G < 2^31: num_mb * G and num_tiles are bounded
+  return nb < p.w0 ? (nb * p.G) / p.w0 : 0;
+}
+
+// End of the window owned by column block nb (empty outside the first group).
+__device__ __forceinline__ int chunk_end(const GemmParams& p, int nb) {
+  return nb < p.w0 ? ((nb + 1) * p.G) / p.w0 : 0;
 }
 
 // k-group visited at position i of a tile whose owned window is [ws, we): the
@@ -219,17 +235,20 @@ __device__ __forceinline__ int chunk_at(int i, int ws, int we) {
   return j < ws ? j : j + wlen;
 }
 
-// The column block whose tiles start at (and so own) k-group g: the nb with
-// chunk_start(nb) <= g < chunk_start(nb + 1).
+// The column block whose tiles own k-group g: the nb < w0 with
+// chunk_start(nb) <= g < chunk_end(nb).
 __device__ __forceinline__ int owner_nb(const GemmParams& p, int g) {
-  return ((g + 1) * p.num_nb + p.G - 1) / p.G - 1;
+  return ((g + 1) * p.w0 + p.G - 1) / p.G - 1;
 }
 
 // Schedule index of tile (mb, nb) (inverse of tile_coords).
 __device__ __forceinline__ int tile_index(const GemmParams& p, int mb, int nb) {
   int pos = mb - p.mb_start;
   if (pos < 0) pos += p.num_mb;
-  return pos * p.num_nb + nb;
+  const int gq = nb / p.ng;
+  const int g0 = gq * p.ng;
+  const int width = min(p.ng, p.num_nb - g0);
+  return gq * p.num_mb * p.ng + pos * width + (nb - g0);
 }
 
 __device__ __forceinline__ int chunk_boxes(const GemmParams& p, int g) {
@@ -250,7 +269,7 @@ template <bool kFused>
 __device__ __forceinline__ void tile_ctx(const GemmParams& p, int t, TileCtx& c) {
   tile_coords(p, t, c.mb, c.nb);
   c.ws = chunk_start(p, c.nb);
-  c.we = chunk_start(p, c.nb + 1);
+  c.we = chunk_end(p, c.nb);
   c.kind = kFused ? block_kind(p, c.mb) : kDirect;
   const int lo = c.mb * kBM, hi = min(lo + kBM, p.M);
   c.r0 = lo / p.mps;

@@ -204,7 +204,7 @@ def run_reference(args, w, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="m16384_d8")
@@ -258,7 +258,8 @@ def main():
                        rank=args.rank_local, stream=stream)
 
     def barrier():
-        agmm.ag_then_matmul(shards, b, bias, a_gathered=a_g2, out=out2, stream=stream)
+        agmm.ag_then_matmul(shards, b, bias, a_gathered=a_g2, out=out2, stream=stream,
+                            layout=args.layout)
 
     for _ in range(max(args.warmup, 3)):
         fused()
@@ -338,10 +339,11 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        flops, times, threads, n = cpu_baseline(w, args.cpu_rows)
-        cpu = {"value": flops / times[0] / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": f"gather + naive fp32 GEMM on {n} of {w.M} output rows "
-                         f"({times[0]:.1f} s)"}
+        flops, times, threads, n = cpu_baseline(w, args.cpu_rows, repeats=2)
+        t_cpu = sum(times) / len(times)
+        cpu = {"value": flops / t_cpu / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"gather + naive fp32 GEMM on {n} of {w.M} output rows, mean of "
+                         f"{len(times)} runs ({sum(times):.1f} s of CPU work)"}
 
     if rank == 0:
         line = {
