@@ -105,10 +105,17 @@ def _status_text(status: int) -> str:
         return "?"
 
 
+_DEFAULT_OPTIONS = None
+
+
 def default_options() -> AgOptions:
-    o = AgOptions()
-    library().ag_options_default(ctypes.byref(o))
-    return o
+    """A fresh ag_options filled by ag_options_default (the C side's defaults)."""
+    global _DEFAULT_OPTIONS
+    if _DEFAULT_OPTIONS is None:
+        o = AgOptions()
+        library().ag_options_default(ctypes.byref(o))
+        _DEFAULT_OPTIONS = bytes(o)
+    return AgOptions.from_buffer_copy(_DEFAULT_OPTIONS)
 
 
 def _stream_handle(stream):
@@ -185,7 +192,7 @@ def _call(fused, shards, b, bias, a_gathered, out, stream, layout, rank, k_per_f
 
 
 def ag_matmul(shards, b, bias=None, *, a_gathered=None, out=None, stream=None,
-              layout: str = "k_contiguous", rank: int = 0, k_per_flag: int = 8,
+              layout: str = "k_contiguous", rank: int = 0, k_per_flag: int = 0,
               num_sms: int = 0, timeout_ns: int = 0, inject_skip_flag: int = -1, trace=None,
               workspace=None):
     """Fused all-gather matmul (one persistent kernel).  Returns (a_gathered, out)."""
@@ -194,7 +201,7 @@ def ag_matmul(shards, b, bias=None, *, a_gathered=None, out=None, stream=None,
 
 
 def ag_then_matmul(shards, b, bias=None, *, a_gathered=None, out=None, stream=None,
-                   layout: str = "k_contiguous", k_per_flag: int = 8, num_sms: int = 0,
+                   layout: str = "k_contiguous", k_per_flag: int = 0, num_sms: int = 0,
                    timeout_ns: int = 0, trace=None):
     """Barrier baseline: gather kernel, then GEMM kernel.  Returns (a_gathered, out)."""
     return _call(False, shards, b, bias, a_gathered, out, stream, layout, 0, k_per_flag,
@@ -211,7 +218,7 @@ def device_error(stream=None):
     return code.value, info.value
 
 
-def workspace_size(D, m_per_shard, K, N, layout: str = "k_contiguous", k_per_flag: int = 8) -> int:
+def workspace_size(D, m_per_shard, K, N, layout: str = "k_contiguous", k_per_flag: int = 0) -> int:
     o = default_options()
     o.layout = LAYOUTS[layout]
     o.k_per_flag = k_per_flag

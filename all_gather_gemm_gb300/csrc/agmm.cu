@@ -12,6 +12,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <unordered_map>
 
 #include "agmm.h"
 #include "kernels.cuh"
@@ -24,7 +25,16 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int64_t kDefaultTimeoutNs = 2000000000LL;
-constexpr int kDefaultKPerFlag = 8;
+constexpr int kMaxAutoKPerFlag = 8;
+
+// Default flag granularity: at most 8 k-blocks per flag, but at least as many
+// flags per row block as there are column blocks, so that every column
+// block's tiles own a chunk to start on and none waits out another tile's
+// whole k-loop (with fewer flags than column blocks, several tiles start on
+// the same chunk and all but its owner wait for it).
+int auto_k_per_flag(int num_kb, int num_nb) {
+  return std::max(1, std::min(kMaxAutoKPerFlag, num_kb / std::max(1, num_nb)));
+}
 
 thread_local char t_cuda_msg[320] = "no CUDA error recorded on this thread";
 
@@ -131,7 +141,7 @@ int validate(const void** a_shards, int D, int m_per_shard, int K, const void* b
   sh->num_mb = (int)((M + kBM - 1) / kBM);
   sh->num_nb = (N + kBN - 1) / kBN;
   sh->num_kb = (K + kBK - 1) / kBK;
-  sh->kpf = o.k_per_flag ? o.k_per_flag : kDefaultKPerFlag;
+  sh->kpf = o.k_per_flag ? o.k_per_flag : auto_k_per_flag(sh->num_kb, sh->num_nb);
   sh->G = (sh->num_kb + sh->kpf - 1) / sh->kpf;
   if ((int64_t)sh->num_mb * sh->num_nb > INT32_MAX || (int64_t)sh->num_mb * sh->G > 0xFFFFFF)
     return AG_ERR_UNSUPPORTED;
@@ -237,8 +247,41 @@ int launch(Kernel k, int grid, int threads, cudaStream_t stream, const GemmParam
   return e == cudaSuccess ? AG_OK : cuda_fail(e, what);
 }
 
+// Encoded tensor maps, keyed by everything that goes into one (the address,
+// the 2-D extent, the box).  Callers usually pass the same buffers call after
+// call, and encoding is host work that would otherwise sit in front of every
+// launch.  A map holds only an address and a shape, so a cached entry stays
+// valid for any buffer later allocated at that address with that shape.
+// Guarded by g_mu (make_map runs under it); cleared when it grows large.
+struct MapKey {
+  uintptr_t base;
+  uint64_t inner, outer;
+  uint32_t box_inner, box_outer;
+  bool operator==(const MapKey& o) const {
+    return base == o.base && inner == o.inner && outer == o.outer && box_inner == o.box_inner &&
+           box_outer == o.box_outer;
+  }
+};
+struct MapKeyHash {
+  size_t operator()(const MapKey& k) const {
+    uint64_t h = k.base * 0x9E3779B97F4A7C15ull;
+    h ^= (k.inner + 0x632BE59BD9B4E019ull + (h << 6) + (h >> 2));
+    h ^= (k.outer + 0x94D049BB133111EBull + (h << 6) + (h >> 2));
+    h ^= ((uint64_t)k.box_inner << 32 | k.box_outer) + (h << 6) + (h >> 2);
+    return (size_t)h;
+  }
+};
+constexpr size_t kMapCacheMax = 1024;
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
+
 int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
              uint32_t box_outer) {
+  const MapKey key{reinterpret_cast<uintptr_t>(base), inner, outer, box_inner, box_outer};
+  auto hit = g_maps.find(key);
+  if (hit != g_maps.end()) {
+    *m = hit->second;
+    return AG_OK;
+  }
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (!enc) {
     snprintf(t_cuda_msg, sizeof t_cuda_msg, "cuTensorMapEncodeTiled entry point unavailable");
@@ -255,6 +298,8 @@ int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, u
     snprintf(t_cuda_msg, sizeof t_cuda_msg, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
     return AG_ERR_CUDA;
   }
+  if (g_maps.size() >= kMapCacheMax) g_maps.clear();
+  g_maps.emplace(key, *m);
   return AG_OK;
 }
 
@@ -556,7 +601,7 @@ void ag_options_default(ag_options* opt) {
   opt->dtype = AG_DTYPE_BF16;
   opt->layout = AG_LAYOUT_K_CONTIGUOUS;
   opt->rank = 0;
-  opt->k_per_flag = kDefaultKPerFlag;
+  opt->k_per_flag = 0;  // automatic
   opt->num_sms = 0;
   opt->inject_skip_flag = -1;
   opt->timeout_ns = kDefaultTimeoutNs;
@@ -602,7 +647,7 @@ size_t ag_workspace_size(int D, int m_per_shard, int K, int N, const ag_options*
   s.num_mb = (int)((M + kBM - 1) / kBM);
   s.num_nb = (N + kBN - 1) / kBN;
   s.num_kb = (K + kBK - 1) / kBK;
-  s.kpf = o.k_per_flag ? o.k_per_flag : kDefaultKPerFlag;
+  s.kpf = o.k_per_flag ? o.k_per_flag : auto_k_per_flag(s.num_kb, s.num_nb);
   s.G = (s.num_kb + s.kpf - 1) / s.kpf;
   return flags_bytes(s) + (o.layout == AG_LAYOUT_M_CONTIGUOUS ? (size_t)K * M * 2 : 0);
 }

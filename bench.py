@@ -201,6 +201,64 @@ def run_reference(args, w, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_sweep(args):
+    """Fused vs barrier device time (and host time per call) on the workloads of
+    the parity configs: the two-shard case, the cube sweep, M=1024 at D=2/4/8,
+    M=16384 (both layouts) and M=4096 with bias (m-contiguous)."""
+    import torch
+
+    import all_gather_gemm_gb300 as agmm
+    from all_gather_gemm_gb300 import inputs as inp
+
+    cases = [(inp.small_two_shard(), "k_contiguous")]
+    cases += [(w, "k_contiguous") for w in inp.cube_sweep()]
+    cases += [(inp.iris_m1024(d), "k_contiguous") for d in (2, 4, 8)]
+    cases += [(inp.iris_m16384(), "k_contiguous"), (inp.iris_m16384(), "m_contiguous"),
+              (inp.iris_m4096_bias(), "m_contiguous")]
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
+    steps = max(args.steps // 5, 5)
+    for w, layout in cases:
+        x = inp.make_inputs(w)
+        shards = [s.cuda() for s in x.shards]
+        b = x.b.cuda()
+        bias = x.bias.cuda() if x.bias is not None else None
+        a_g = torch.empty((w.M, w.K), dtype=b.dtype, device="cuda")
+        out = torch.empty((w.M, w.N), dtype=b.dtype, device="cuda")
+        calls = {
+            "fused": lambda: agmm.ag_matmul(shards, b, bias, a_gathered=a_g, out=out,
+                                            layout=layout),
+            "barrier": lambda: agmm.ag_then_matmul(shards, b, bias, a_gathered=a_g, out=out,
+                                                   layout=layout)}
+        for fn in calls.values():
+            for _ in range(3):
+                fn()
+        dev = {k: [] for k in calls}
+        host = {k: [] for k in calls}
+        for i in range(steps):
+            for k, fn in calls.items():
+                # as in the bench line: the flush kernel runs while the host prepares
+                # the call, so the events time the device work, not host overhead
+                flush.fill_(i)
+                s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                s.record()
+                t0 = time.perf_counter()
+                fn()
+                host[k].append((time.perf_counter() - t0) * 1e6)
+                e.record()
+                torch.cuda.synchronize()
+                dev[k].append(s.elapsed_time(e) * 1e3)
+        code, info = agmm.device_error()
+        f_us = statistics.median(dev["fused"])
+        b_us = statistics.median(dev["barrier"])
+        print(json.dumps({"workload": w.name, "layout": layout, "M": w.M, "N": w.N, "K": w.K,
+                          "D": w.D, "dtype": w.dtype, "fused_us": f_us, "barrier_us": b_us,
+                          "speedup_vs_barrier": b_us / f_us,
+                          "fused_tflops": w.flops / (f_us * 1e-6) / 1e12,
+                          "host_us_fused": statistics.median(host["fused"]),
+                          "host_us_barrier": statistics.median(host["barrier"]),
+                          "device_error": code}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -214,6 +272,9 @@ def main():
     ap.add_argument("--reference-rows", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="instead of the bench line: fused vs barrier on every workload of the "
+                         "parity configs, one JSON line each")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -221,6 +282,9 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     w = headline_workload(args.workload)
 
+    if args.sweep:
+        run_sweep(args)
+        return
     if args.impl == "reference":
         run_reference(args, w, rank, world)
         return

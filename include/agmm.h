@@ -108,7 +108,8 @@ typedef struct ag_options {
   int32_t dtype;            /* ag_dtype of a_shards, b, a_gathered, out (default bf16) */
   int32_t layout;           /* ag_layout of the staged A (default k-contiguous) */
   int32_t rank;             /* the local shard, 0 <= rank < D (default 0) */
-  int32_t k_per_flag;       /* 64-column K blocks covered by one ready flag; 0 = 8 */
+  int32_t k_per_flag;       /* 64-column K blocks covered by one ready flag; 0 = automatic:
+                               min(8, max(1, K-blocks / column blocks)) (default) */
   int32_t num_sms;          /* cap on the persistent grid (CTAs); 0 = every SM */
   int32_t inject_skip_flag; /* fault injection: the producer never publishes this flag index
                                (-1 = off); the consumer wait then times out */
@@ -198,7 +199,7 @@ int ag_num_sms(void);
  * and ag_options.workspace must be NULL (AG_ERR_INVALID_ARG).  A problem whose
  * scratch -- 256 bytes plus ag_workspace_size() for the k-contiguous layout --
  * exceeds AG_NOALLOC_SCRATCH_BYTES is rejected with AG_ERR_TOO_LARGE before
- * anything is enqueued.  With the default k_per_flag of 8 that admits, for
+ * anything is enqueued.  With the automatic k_per_flag that admits, for
  * example, M = 16384, N = 3584, K = 8192 (about 30 KB of scratch).  All other
  * arguments and errors are as for ag_matmul_ex; device-side timeouts are
  * reported by ag_get_device_error.

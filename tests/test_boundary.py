@@ -41,7 +41,7 @@ def test_options_default_matches_header(lib):
     o = agmm.AgOptions()
     ctypes.memset(ctypes.byref(o), 0x5A, ctypes.sizeof(o))
     lib.ag_options_default(ctypes.byref(o))
-    assert (o.dtype, o.layout, o.rank, o.k_per_flag, o.num_sms) == (0, 0, 0, 8, 0)
+    assert (o.dtype, o.layout, o.rank, o.k_per_flag, o.num_sms) == (0, 0, 0, 0, 0)
     assert o.inject_skip_flag == -1 and o.timeout_ns == 2_000_000_000
     assert not o.trace and o.trace_words == 0 and not o.workspace and o.workspace_bytes == 0
     assert ctypes.sizeof(o) == 64
@@ -66,6 +66,10 @@ def test_workspace_size(lib):
     assert agmm.workspace_size(8, 2048, 8192, 3584, k_per_flag=1) == 128 * 128 * 8 + 14336
     assert agmm.workspace_size(8, 2048, 8192, 3584, k_per_flag=16) == 8192 + 14336
     assert agmm.workspace_size(1, 1, 8, 8) == 2048  # one flag and one tile, 1 KiB each
+    # automatic granularity: K=384 has 6 k-blocks and N=384 two column blocks,
+    # so 3 k-blocks per flag -> 2 flags per row block (3 row blocks): 48 B -> 1 KiB
+    assert agmm.workspace_size(8, 48, 384, 384) == 1024 + 1024
+    assert agmm.workspace_size(8, 48, 384, 384, k_per_flag=8) == 1024 + 1024
     assert agmm.workspace_size(0, 1, 8, 8) == 0
     assert agmm.workspace_size(1, 1, 12, 8) == 0
 

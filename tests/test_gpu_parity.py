@@ -301,7 +301,7 @@ def test_trace_records_overlap_roles():
     fetch = rec[(rec[:, 2] >> np.uint64(56)) == 1]
     # every (row block, k-group) chunk is staged by its owner (or a follower
     # that took it over) at least once
-    num_mb, G = 2048 // 128, 2048 // 64 // 8
+    num_mb, G = 2048 // 128, 2048 // 64 // 4  # automatic k_per_flag: 32 k-blocks / 8 column blocks
     keys = ((fetch[:, 2] >> np.uint64(20)) & np.uint64(0xFFFFF)) * np.uint64(G) + (fetch[:, 2] & np.uint64(0xFFFFF))
     assert set(keys.tolist()) == set(range(num_mb * G))
     assert len(keys) < 2 * num_mb * G
