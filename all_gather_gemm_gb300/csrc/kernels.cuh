@@ -603,12 +603,18 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
             if (one_shard) {
               tma_load_2d(a_dst, &p.tm_shard[r0], &full[stage], kb * kBK, mb * kBM - r0 * p.mps);
             } else {
+              // Walk the 8-row groups across shard boundaries (m_per_shard is a
+              // multiple of 8 here) without a division per group.  Past the
+              // last shard the row stays out of range: TMA zero-fills it.
+              int r = r0, lr = mb * kBM - r0 * p.mps;
 #pragma unroll 1
               for (int q = 0; q < kBM / 8; ++q) {
-                const int row = mb * kBM + q * 8;
-                const int r = row < p.M ? row / p.mps : p.D - 1;  // past M: zero fill
-                tma_load_2d(a_dst + q * 1024, &p.tm_shard8[r], &full[stage], kb * kBK,
-                            row - r * p.mps);
+                tma_load_2d(a_dst + q * 1024, &p.tm_shard8[r], &full[stage], kb * kBK, lr);
+                lr += 8;
+                if (lr >= p.mps && r < p.D - 1) {
+                  lr -= p.mps;
+                  ++r;
+                }
               }
             }
           } else if (kLayoutM) {

@@ -99,16 +99,18 @@ def main(argv=None) -> int:
 
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--workload", default="m16384_d8",
-                    choices=["m16384_d8", "m4096_d8_bias", "m1024_d8", "cube_4096", "cube_2048"])
+                    help="m16384_d8, m4096_d8_bias, m1024_d8 or cube_<n> (n a multiple of 8)")
     ap.add_argument("--layout", default="k_contiguous", choices=list(agmm.LAYOUTS))
-    ap.add_argument("--k-per-flag", type=int, default=8)
+    ap.add_argument("--k-per-flag", type=int, default=0, help="0: the library's automatic choice")
     ap.add_argument("--records", type=int, default=1 << 18)
     ap.add_argument("--json", default=None, help="write a Chrome trace of the fused call here")
     args = ap.parse_args(argv)
     table = {"m16384_d8": inp.iris_m16384, "m4096_d8_bias": inp.iris_m4096_bias,
-             "m1024_d8": lambda: inp.iris_m1024(8), "cube_4096": lambda: inp.cube(4096),
-             "cube_2048": lambda: inp.cube(2048)}
-    w = table[args.workload]()
+             "m1024_d8": lambda: inp.iris_m1024(8)}
+    if args.workload.startswith("cube_"):
+        w = inp.cube(int(args.workload[5:]))
+    else:
+        w = table[args.workload]()
     x = inp.make_inputs(w)
     shards = [s.cuda() for s in x.shards]
     b = x.b.cuda()
