@@ -18,15 +18,16 @@
 //               accumulate) into one of two TMEM accumulators.
 //   warps 2-5   epilogue: tcgen05.ld, + fp32 bias, round to 16 bits,
 //               128-byte-swizzled shared memory, TMA store of the out tile.
-//   warp 6      stager (fused only): TMA-stores each landed box an owner
-//               loaded into a_gathered (the k-contiguous staging buffer) and,
-//               once every box of the chunk is written, publishes the chunk.
+//   warp 6      stager (fused only): publishes a chunk once every box of it
+//               has been written to the staging buffer.
 //   warp 7      register fetcher (fused only): copies chunks that TMA cannot
 //               load from a single shard (a row block straddling shards whose
 //               row count is not a multiple of 8) and publishes them.
-//   warps 8-11  transposers (fused, m-contiguous staging only): write each
-//               owner-loaded box transposed into the [K, M] staging, which is
-//               what followers read; the stager publishes once they are done.
+//   warps 8-11  copiers (fused only), one per pipeline stage: read each box an
+//               owner loaded from shared memory, free the stage, and write the
+//               box into a_gathered (the k-contiguous staging) -- and, for the
+//               m-contiguous layout, transposed into the [K, M] staging, which
+//               is what followers then read.
 //
 // Each staged box is therefore read from its shard once, by the CTA that also
 // multiplies it ("fetch once, write through"), and no atomic sits on the
@@ -67,10 +68,9 @@ constexpr int kEpiCols = 64;                           // columns per store box 
 constexpr int kEpiBufBytes = kEpiRows * kEpiCols * 2;  // 4 KB
 constexpr int kEpiBufs = 2;
 constexpr int kTmemCols = 2 * kBN;
-constexpr int kTransposeWarps = 4;  // one per pipeline stage
+constexpr int kCopyWarps = 4;  // fused kernel: one copier warp per pipeline stage
 constexpr int kMaxShards = 16;
 constexpr int kFlagShift = 20;      // flag base = epoch << 20; boxes per chunk < 2^20
-constexpr int kStagerLag = 4;       // bulk groups the stager may leave in flight
 
 // Kernel variants: barrier-path GEMM (A from a_gathered or the [K, M] staging)
 // and the fused kernel, each for both staging layouts.
@@ -79,7 +79,7 @@ enum Mode : int { kGemmK = 0, kGemmM = 1, kFusedK = 2, kFusedM = 3 };
 __host__ __device__ constexpr bool mode_fused(int m) { return m >= kFusedK; }
 __host__ __device__ constexpr bool mode_layout_m(int m) { return m == kGemmM || m == kFusedM; }
 __host__ __device__ constexpr int mode_threads(int m) {
-  return 32 * (2 + kEpiWarps + (mode_fused(m) ? 2 : 0) + (m == kFusedM ? kTransposeWarps : 0));
+  return 32 * (2 + kEpiWarps + (mode_fused(m) ? 2 + kCopyWarps : 0));
 }
 
 // Per-stage record written by the TMA issuer before it arms the stage's full
@@ -90,17 +90,18 @@ constexpr uint32_t kInfoAmn = 4u;      // A box in shared memory is MN-major
 constexpr uint32_t kInfoLast = 8u;     // last box of its chunk
 
 constexpr int kNumBars = 2 * kStages + 4 + 1;
-constexpr int kStagerQ = kStagerLag + 1 + 2 * kStages;  // stager queues (ints)
+constexpr int kStagerQ = 2 * kStages;  // stager queue (ints)
+static_assert(kCopyWarps == kStages, "copier warp w owns pipeline stage w");
 constexpr int kSmemData = kStages * kStageBytes + kEpiWarps * kEpiBufs * kEpiBufBytes;
 constexpr int kSmemBytes =
-    1024 + kSmemData + 8 * kNumBars + 16 * kStages + 4 * kTransposeWarps + 4 * kStagerQ + 64;
+    1024 + kSmemData + 8 * kNumBars + 16 * kStages + 4 * kCopyWarps + 4 * kStagerQ + 64;
 static_assert(kSmemBytes <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
 
 // Error code written to the device error word (matches ag_status).
 constexpr uint32_t kErrTimeout = 4;
 // Sites reported with a pipeline timeout (ready-flag timeouts report the flag index).
 constexpr uint32_t kSiteEmpty = 0xF00001, kSiteFull = 0xF00002, kSiteTmemEmpty = 0xF00003,
-                   kSiteTmemFull = 0xF00004, kSiteStager = 0xF00005, kSiteTranspose = 0xF00006;
+                   kSiteTmemFull = 0xF00004, kSiteStager = 0xF00005, kSiteCopy = 0xF00006;
 
 // Trace roles (see include/agmm.h).
 constexpr uint32_t kTraceClaim = 1, kTraceWait = 2, kTraceTile = 3, kTraceGather = 4,
@@ -459,8 +460,8 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
   uint64_t* tmem_empty = tmem_full + 2;      // [2] accumulator drained
   uint64_t* drain = tmem_empty + 2;          // [1] final MMA drain
   uint32_t* info = reinterpret_cast<uint32_t*>(drain + 1);  // [kStages][4]
-  uint32_t* tprog = info + 4 * kStages;                      // [kTransposeWarps] slots done
-  int* stager_q = reinterpret_cast<int*>(tprog + kTransposeWarps);  // [kStagerQ]
+  uint32_t* tprog = info + 4 * kStages;                      // [kCopyWarps] slots done
+  int* stager_q = reinterpret_cast<int*>(tprog + kCopyWarps);  // [kStagerQ]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stager_q + kStagerQ);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -470,7 +471,8 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
   const int my_stages = my_tiles * p.num_kb;
 
   if (threadIdx.x == 0) {
-    const uint32_t empty_count = 1 + (kFused ? 1 : 0) + (kMode == kFusedM ? 1 : 0);
+    // MMA commit; fused: + stager (reads the stage record) + the stage's copier
+    const uint32_t empty_count = kFused ? 3 : 1;
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], empty_count);
@@ -480,7 +482,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
       mbar_init(&tmem_empty[b], 32 * kEpiWarps);
     }
     mbar_init(drain, 1);
-    for (int w = 0; w < kTransposeWarps; ++w) tprog[w] = 0;
+    for (int w = 0; w < kCopyWarps; ++w) tprog[w] = 0;
     *abort_flag = 0;
     fence_mbarrier_init();
     prefetch_tensormap(&p.tm_a);
@@ -776,45 +778,38 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
     __syncwarp();
   } else if (kFused && warp == 2 + kEpiWarps) {
     // ---------------------------------------------------------- stager
+    // Publishes staged chunks.  The copier warps write each owner box into
+    // a_gathered (and the [K, M] staging); once every box of a chunk is
+    // written, this warp releases the chunk's flag.  It reads each stage's
+    // record, so it takes part in the stage's empty barrier.
     if (lane == 0) {
-      // k-contiguous: ring of flag indices, one per committed bulk group in
-      // commit order (-1: nothing to publish when that group completes).
-      // m-contiguous: chunks waiting for the transposers, as (flag index,
-      // sequence index of the chunk's last box).
-      // (kept in shared memory: a dynamically indexed local array would live
-      // in local memory, which misses to L2 when shared memory takes the L1)
-      int* pend = stager_q;                        // [kStagerLag + 1]
-      int* tq_flag = stager_q + kStagerLag + 1;    // [kStages]
-      int* tq_last = tq_flag + kStages;            // [kStages]
-      int npend = 0, nreal = 0;  // entries, and entries with a flag to publish
+      // Chunks waiting for the copiers: (flag index, sequence index of the
+      // chunk's last box).  Kept in shared memory: a dynamically indexed local
+      // array would live in local memory, which misses to L2 when shared
+      // memory takes the L1.
+      int* tq_flag = stager_q;            // [kStages]
+      int* tq_last = stager_q + kStages;  // [kStages]
       int ntq = 0;
       auto publish = [&](int idx) {
-        if (idx >= 0 && idx != p.inject_skip_flag)
+        if (idx != p.inject_skip_flag)
           st_release_gpu(p.flags + idx, p.fbase + (uint64_t)chunk_boxes(p, idx % p.G));
       };
-      auto flush_groups = [&]() {
-        bulk_wait_group<0>();
-        fence_proxy_async_global();
-        for (int i = 0; i < npend; ++i) publish(pend[i]);
-        npend = nreal = 0;
-      };
-      // m-contiguous: box i is transposed once its warp (i % 4) has finished
-      // sequence slot i / 4; per-warp progress is in order, so checking the
-      // chunk's last box of each residue covers the whole chunk.
-      auto transposed = [&](int last, int nbox) -> bool {
-        for (int k = last; k > last - nbox && k > last - kTransposeWarps; --k)
-          if ((int)ld_acquire_cta_shared(smem_u32(tprog + (k % kTransposeWarps))) <=
-              k / kTransposeWarps)
+      // Box i is written once its copier (warp i % 4) has finished sequence
+      // slot i / 4; per-warp progress is in order, so checking the chunk's
+      // last box of each residue covers the whole chunk.
+      auto copied = [&](int last, int nbox) -> bool {
+        for (int k = last; k > last - nbox && k > last - kCopyWarps; --k)
+          if ((int)ld_acquire_cta_shared(smem_u32(tprog + (k % kCopyWarps))) <= k / kCopyWarps)
             return false;
         return true;
       };
-      auto drain_tq = [&](bool block) {
+      auto drain = [&](bool block) {
         while (ntq > 0) {
           const int nbox = chunk_boxes(p, tq_flag[0] % p.G);
-          if (!transposed(tq_last[0], nbox)) {
+          if (!copied(tq_last[0], nbox)) {
             if (!block) return;
             const uint64_t t0 = globaltimer_ns();
-            while (!transposed(tq_last[0], nbox)) {
+            while (!copied(tq_last[0], nbox)) {
               if (*abort_flag || globaltimer_ns() - t0 > (uint64_t)p.pipe_timeout_ns) return;
             }
           }
@@ -827,92 +822,99 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
           --ntq;
         }
       };
-      for (int i = 0; i < my_stages; ++i) {
+      bool aborted = false;
+      for (int i = 0; i < my_stages && !aborted; ++i) {
         const int s = i % kStages;
         const uint32_t ph = (uint32_t)(i / kStages) & 1u;
-        // Wait for the stage; publish what is pending while idle, so that no
-        // follower waits on a chunk this warp holds back.
-        bool ok = mbar_try_wait(&full[s], ph);
-        if (!ok) {
-          if (nreal) flush_groups();
-          if (kLayoutM) drain_tq(true);
-          ok = wait_bar(p, &full[s], ph, abort_flag, kSiteStager);
+        // While the stage is not there yet, keep publishing what the copiers
+        // finish, so that no follower waits on a chunk this warp holds back.
+        if (!mbar_try_wait(&full[s], ph)) {
+          const uint64_t t0 = globaltimer_ns();
+          for (uint32_t it = 1;; ++it) {
+            if (ntq) drain(false);
+            if (mbar_try_wait(&full[s], ph)) break;
+            if ((it & 63u) == 0 && (*abort_flag || globaltimer_ns() - t0 > (uint64_t)p.pipe_timeout_ns)) {
+              if (!*abort_flag) {
+                *abort_flag = 1;
+                record_error(p.err, p.epoch, kErrTimeout, kSiteStager);
+              }
+              aborted = true;
+              break;
+            }
+          }
+          if (aborted) break;
         }
-        if (!ok) break;
         const uint32_t bits = info[4 * s];
         const int flag_idx = (int)info[4 * s + 3];
-        const bool chunk_done = (bits & kInfoPublish) && (bits & kInfoLast);
-        if (bits & kInfoStage) {
-          tma_store_2d(&p.tm_a, smem + s * kStageBytes, (int)info[4 * s + 2] * kBK,
-                       (int)info[4 * s + 1] * kBM);
-          bulk_commit_group();
-          pend[npend] = (!kLayoutM && chunk_done) ? flag_idx : -1;
-          nreal += pend[npend] >= 0;
-          ++npend;
-          bulk_wait_group_read<0>();
-        }
         mbar_arrive(&empty[s]);
-        if (kLayoutM && chunk_done) {
-          if (ntq == kStages) drain_tq(true);
+        if ((bits & kInfoPublish) && (bits & kInfoLast)) {
+          if (ntq == kStages) drain(true);
           tq_flag[ntq] = flag_idx;
           tq_last[ntq] = i;
           ++ntq;
         }
-        if (npend > kStagerLag) {
-          bulk_wait_group<kStagerLag>();
-          fence_proxy_async_global();
-          const int done = npend - kStagerLag;
-          for (int k = 0; k < done; ++k) {
-            nreal -= pend[k] >= 0;
-            publish(pend[k]);
-          }
-          for (int k = done; k < npend; ++k) pend[k - done] = pend[k];
-          npend = kStagerLag;
-        }
-        if (kLayoutM) drain_tq(false);
+        if (ntq) drain(false);
       }
-      flush_groups();
-      if (kLayoutM) drain_tq(true);
+      drain(true);
     }
     __syncwarp();
   } else if (kFused && warp == 3 + kEpiWarps) {
     // ---------------------------------------------------------- register fetcher
     regfetch_loop(p, lane, kLayoutM);
     __syncwarp();
-  } else if (kMode == kFusedM) {
-    // ---------------------------------------------------------- transposers
-    // Warp w owns pipeline stage w.  For each box an owner loaded it reads the
-    // landed K-major (128-byte swizzled) tile in 8x8 blocks, transposes them in
-    // registers and writes [K, M] rows of the staging; then it reports its
-    // progress (sequence slots done) to the stager in shared memory.
+  } else if (kFused) {
+    // ---------------------------------------------------------- copiers
+    // Warp w owns pipeline stage w.  For each box its owner had staged it
+    // reads the landed K-major (128-byte swizzled) tile, releases the stage as
+    // soon as the reads are done, and writes the rows into a_gathered with
+    // 16-byte stores; for the m-contiguous layout it also writes the box
+    // transposed into the [K, M] staging (8x8 register transposes), which is
+    // what followers read.  Then it reports progress to the stager.
     const int w = warp - (4 + kEpiWarps);
     const int s = w;
     const uint32_t a_u32 = smem_u32(smem + s * kStageBytes);
+    const int ch = lane & 7;  // 16-byte chunk of a 128-byte row: 4 rows x 8 chunks per access
     for (int i = w; i < my_stages; i += kStages) {
       const uint32_t ph = (uint32_t)(i / kStages) & 1u;
-      const bool ok = wait_bar(p, &full[s], ph, abort_flag, kSiteTranspose);
+      const bool ok = wait_bar(p, &full[s], ph, abort_flag, kSiteCopy);
       if (!__all_sync(0xffffffffu, ok)) break;
       const uint32_t bits = info[4 * s];
       const int mb = (int)info[4 * s + 1], kb = (int)info[4 * s + 2];
-      if (bits & kInfoPublish) {
-        // lane -> (row group rg, column group cg): a warp reads 4 rows x 8
-        // chunks per instruction, the conflict-free pattern for this swizzle.
-        const int cg = lane & 7;
+      if (bits & kInfoStage) {
+        const int k = kb * kBK + ch * 8;
+        const bool k_ok = k < p.K;
 #pragma unroll 1
-        for (int b = 0; b < 4; ++b) {
-          const int rg = 4 * b + (lane >> 3);
+        for (int it0 = 0; it0 < kBM / 4; it0 += 8) {
           uint4 v[8];
 #pragma unroll
-          for (int r = 0; r < 8; ++r) {
-            const int row = rg * 8 + r;
-            v[r] = ld_shared_v4(a_u32 + row * 128 + ((cg ^ (row & 7)) << 4));
+          for (int u = 0; u < 8; ++u) {
+            const int row = (it0 + u) * 4 + (lane >> 3);
+            v[u] = ld_shared_v4(a_u32 + row * 128 + ((ch ^ (row & 7)) << 4));
           }
-          const int m = mb * kBM + rg * 8;
-          const int k = kb * kBK + cg * 8;
-          if (m < p.M && k < p.K) {
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-              st_v4(p.staging_mk + (int64_t)(k + c) * p.M + m, transpose_col(v, c));
+          for (int u = 0; u < 8; ++u) {
+            const int m = mb * kBM + (it0 + u) * 4 + (lane >> 3);
+            if (k_ok && m < p.M) st_v4(p.a_gathered + (int64_t)m * p.K + k, v[u]);
+          }
+        }
+        if (kLayoutM && (bits & kInfoPublish)) {
+          // lane -> (row group rg, column group cg): a warp reads 4 rows x 8
+          // chunks per instruction, the conflict-free pattern for this swizzle.
+#pragma unroll 1
+          for (int b = 0; b < 4; ++b) {
+            const int rg = 4 * b + (lane >> 3);
+            uint4 v[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+              const int row = rg * 8 + r;
+              v[r] = ld_shared_v4(a_u32 + row * 128 + ((ch ^ (row & 7)) << 4));
+            }
+            const int m = mb * kBM + rg * 8;
+            if (m < p.M && k_ok) {
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                st_v4(p.staging_mk + (int64_t)(k + c) * p.M + m, transpose_col(v, c));
+            }
           }
         }
         __syncwarp();
