@@ -18,16 +18,19 @@
 //               accumulate) into one of two TMEM accumulators.
 //   warps 2-5   epilogue: tcgen05.ld, + fp32 bias, round to 16 bits,
 //               128-byte-swizzled shared memory, TMA store of the out tile.
-//   warp 6      stager (fused only): publishes a chunk once every box of it
-//               has been written to the staging buffer.
-//   warp 7      register fetcher (fused only): copies chunks that TMA cannot
+//   warp 6      register fetcher (fused only): copies chunks that TMA cannot
 //               load from a single shard (a row block straddling shards whose
 //               row count is not a multiple of 8) and publishes them.
-//   warps 8-11  copiers (fused only), one per pipeline stage: read each box an
-//               owner loaded from shared memory, free the stage, and write the
-//               box into a_gathered (the k-contiguous staging) -- and, for the
-//               m-contiguous layout, transposed into the [K, M] staging, which
-//               is what followers then read.
+//   warps 7-10  copiers (fused only), one per pipeline stage.  The issuer
+//               hands a copier only the boxes it stages (a pair of mbarriers
+//               per stage, so the MMA's own pipeline is the plain GEMM's for
+//               every other box).  The copier reads the landed box from shared
+//               memory, frees the stage, and writes the box into a_gathered
+//               (the k-contiguous staging) -- and, for the m-contiguous
+//               layout, transposed into the [K, M] staging, which is what
+//               followers then read.  The copier that writes the last box of
+//               a chunk publishes the chunk once the other copiers' boxes of
+//               it are written.
 //
 // Each staged box is therefore read from its shard once, by the CTA that also
 // multiplies it ("fetch once, write through"), and no atomic sits on the
@@ -79,29 +82,36 @@ enum Mode : int { kGemmK = 0, kGemmM = 1, kFusedK = 2, kFusedM = 3 };
 __host__ __device__ constexpr bool mode_fused(int m) { return m >= kFusedK; }
 __host__ __device__ constexpr bool mode_layout_m(int m) { return m == kGemmM || m == kFusedM; }
 __host__ __device__ constexpr int mode_threads(int m) {
-  return 32 * (2 + kEpiWarps + (mode_fused(m) ? 2 + kCopyWarps : 0));
+  return 32 * (2 + kEpiWarps + (mode_fused(m) ? 1 + kCopyWarps : 0));
 }
 
-// Per-stage record written by the TMA issuer before it arms the stage's full
-// barrier (so readers that waited on that barrier see it).
+// Per-stage record written by the TMA issuer: word 0 = the box's bits, read
+// by the MMA warp once the stage is full; words 1-6 = the copier's record
+// {bits, mb, kb, flag index, sequence index, boxes in the chunk}, written
+// before a staged box is handed to the stage's copier and kept until the
+// copier frees the stage.  The two never share a word, so the end record
+// (kInfoEnd in word 1) cannot race with the MMA warp.
+constexpr int kInfoWords = 8;
 constexpr uint32_t kInfoStage = 1u;    // A box is to be stored into a_gathered
 constexpr uint32_t kInfoPublish = 2u;  // ... and its chunk published once staged
 constexpr uint32_t kInfoAmn = 4u;      // A box in shared memory is MN-major
 constexpr uint32_t kInfoLast = 8u;     // last box of its chunk
+constexpr uint32_t kInfoPhase = 16u;   // parity of the full-barrier phase of this fill
+constexpr uint32_t kInfoEnd = 32u;     // hand-off only: the issuer is done, the copier leaves
 
-constexpr int kNumBars = 2 * kStages + 4 + 1;
-constexpr int kStagerQ = 2 * kStages;  // stager queue (ints)
+// full, empty [kStages]; tmem_full, tmem_empty [2]; drain; cready [kStages]
+constexpr int kNumBars = 3 * kStages + 4 + 1;
 static_assert(kCopyWarps == kStages, "copier warp w owns pipeline stage w");
 constexpr int kSmemData = kStages * kStageBytes + kEpiWarps * kEpiBufs * kEpiBufBytes;
 constexpr int kSmemBytes =
-    1024 + kSmemData + 8 * kNumBars + 16 * kStages + 4 * kCopyWarps + 4 * kStagerQ + 64;
+    1024 + kSmemData + 8 * kNumBars + 4 * kInfoWords * kStages + 4 * kCopyWarps + 64;
 static_assert(kSmemBytes <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
 
 // Error code written to the device error word (matches ag_status).
 constexpr uint32_t kErrTimeout = 4;
 // Sites reported with a pipeline timeout (ready-flag timeouts report the flag index).
 constexpr uint32_t kSiteEmpty = 0xF00001, kSiteFull = 0xF00002, kSiteTmemEmpty = 0xF00003,
-                   kSiteTmemFull = 0xF00004, kSiteStager = 0xF00005, kSiteCopy = 0xF00006;
+                   kSiteTmemFull = 0xF00004, kSiteStreamEnd = 0xF00005, kSiteCopy = 0xF00006;
 
 // Trace roles (see include/agmm.h).
 constexpr uint32_t kTraceClaim = 1, kTraceWait = 2, kTraceTile = 3, kTraceGather = 4,
@@ -296,6 +306,61 @@ __device__ __forceinline__ bool wait_bar(const GemmParams& p, uint64_t* bar, uin
   }
 }
 
+// Copier side of the hand-off: waits for the n-th record the issuer hands
+// to this stage's copier (phase n of `bar`).  False on abort or timeout.  A
+// copier may idle for as long as its CTA has nothing to stage, so the time
+// limit restarts whenever the issuer makes progress (`iseq`).
+__device__ __forceinline__ bool wait_handoff(const GemmParams& p, uint64_t* bar, uint32_t n,
+                                             volatile uint32_t* iseq, volatile int* abort_flag) {
+  const uint32_t parity = n & 1u;
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = globaltimer_ns();
+  uint32_t seen = *iseq;
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort_flag) return false;
+      const uint32_t now_seq = *iseq;
+      const uint64_t now = globaltimer_ns();
+      if (now_seq != seen) {
+        seen = now_seq;
+        t0 = now;
+      } else if (now - t0 > (uint64_t)p.pipe_timeout_ns) {
+        *abort_flag = 1;
+        record_error(p.err, p.epoch, kErrTimeout, kSiteCopy);
+        return false;
+      }
+    }
+  }
+}
+
+// Publication check by the copier of a chunk's last box (sequence index
+// `seq`): the chunk's boxes are seq - nbox + 1 .. seq, box i sits in stage
+// i % kStages, and each copier writes its boxes in order and then advances
+// tprog to (index + 1) with a CTA-scope release.  So the chunk is written once
+// the latest of its boxes in every other stage is.  Bounded; false on abort
+// or timeout (the chunk then stays unpublished and its followers report it).
+__device__ __forceinline__ bool chunk_written(const GemmParams& p, const uint32_t* tprog, int seq,
+                                              int nbox, volatile int* abort_flag) {
+  const int others = min(nbox, kCopyWarps) - 1;
+  const uint64_t t0 = globaltimer_ns();
+  for (int q = 1; q <= others; ++q) {
+    const int i = seq - q;
+    const uint32_t slot = smem_u32(tprog + (i % kCopyWarps));
+    for (uint32_t it = 0; ld_acquire_cta_shared(slot) <= (uint32_t)i; ++it) {
+      if ((it & 63u) == 63u &&
+          (*abort_flag || globaltimer_ns() - t0 > (uint64_t)p.pipe_timeout_ns)) {
+        if (!*abort_flag) {
+          *abort_flag = 1;
+          record_error(p.err, p.epoch, kErrTimeout, kSiteCopy);
+        }
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
 // Follower wait on a chunk: bounded acquire-polling until flag >= target.
 // When the flag is still untouched and the owner tile (owner_tile >= 0) has
 // not started, try to take the chunk over (atom.max to base); returns true if
@@ -459,23 +524,25 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
   uint64_t* tmem_full = bars + 2 * kStages;  // [2] accumulator ready
   uint64_t* tmem_empty = tmem_full + 2;      // [2] accumulator drained
   uint64_t* drain = tmem_empty + 2;          // [1] final MMA drain
-  uint32_t* info = reinterpret_cast<uint32_t*>(drain + 1);  // [kStages][4]
-  uint32_t* tprog = info + 4 * kStages;                      // [kCopyWarps] slots done
-  int* stager_q = reinterpret_cast<int*>(tprog + kCopyWarps);  // [kStagerQ]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stager_q + kStagerQ);
+  uint64_t* cready = drain + 1;              // [kStages] fused: a staged box handed to the copier
+  uint32_t* info = reinterpret_cast<uint32_t*>(cready + kStages);  // [kStages][kInfoWords]
+  uint32_t* tprog = info + kInfoWords * kStages;  // [kCopyWarps] sequence index + 1 of the last box written
+  volatile uint32_t* iseq = tprog + kCopyWarps;   // issuer progress (chunks), a liveness signal
+  uint32_t* tmem_slot = tprog + kCopyWarps + 1;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int my_tiles = my_tile_count(p);
-  const int my_stages = my_tiles * p.num_kb;
 
   if (threadIdx.x == 0) {
-    // MMA commit; fused: + stager (reads the stage record) + the stage's copier
-    const uint32_t empty_count = kFused ? 3 : 1;
+    // empty: the MMA commit, and (fused) the stage's copier for a staged box
+    // or the issuer itself, at fill time, for any other box -- so the issuer
+    // waits on one barrier per box either way.
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], empty_count);
+      mbar_init(&empty[s], kFused ? 2 : 1);
+      mbar_init(&cready[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tmem_full[b], 1);
@@ -483,6 +550,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
     }
     mbar_init(drain, 1);
     for (int w = 0; w < kCopyWarps; ++w) tprog[w] = 0;
+    *iseq = 0;
     *abort_flag = 0;
     fence_mbarrier_init();
     prefetch_tensormap(&p.tm_a);
@@ -504,7 +572,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
     if (lane == 0) {
       uint32_t issued_mask = 0, issued_parity = 0;
       bool aborted = false;
-      int stage = 0;
+      int stage = 0, seq = 0;
       uint32_t phase = 0;
       // Chunk cursor over this CTA's (tile, k-group) sequence.  Tile (mb, nb)
       // owns the window [chunk_start(nb), chunk_start(nb + 1)) and visits it
@@ -593,11 +661,23 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
             aborted = true;
             break;
           }
-          uint32_t* inf = info + 4 * stage;
-          inf[0] = bits | (j == nbox - 1 ? kInfoLast : 0u);
-          inf[1] = (uint32_t)mb;
-          inf[2] = (uint32_t)kb;
-          inf[3] = (uint32_t)flag_idx;
+          uint32_t* inf = info + kInfoWords * stage;
+          const uint32_t box_bits = bits | (j == nbox - 1 ? kInfoLast : 0u);
+          inf[0] = box_bits;
+          if (kFused) {
+            if (bits & kInfoStage) {
+              // Hand the box to the stage's copier (the arrive releases the record).
+              inf[1] = box_bits | (phase ? kInfoPhase : 0u);
+              inf[2] = (uint32_t)mb;
+              inf[3] = (uint32_t)kb;
+              inf[4] = (uint32_t)flag_idx;
+              inf[5] = (uint32_t)seq;
+              inf[6] = (uint32_t)nbox;
+              mbar_arrive(&cready[stage]);
+            } else {
+              mbar_arrive(&empty[stage]);  // no copier reads this box
+            }
+          }
           uint8_t* a_dst = smem + stage * kStageBytes;
           uint8_t* b_dst = a_dst + kAStageBytes;
           mbar_arrive_expect_tx(&full[stage], kStageBytes);
@@ -631,6 +711,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
                         kb * kBK);
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          ++seq;
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
@@ -644,6 +725,19 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
         gi = ngi;
         if (new_tile) cur = nxt;
         if (nxt_follow) cur_peek = nxt_peek;
+        if (kFused) *iseq = (uint32_t)seq;
+      }
+      if (kFused) {
+        // End of stream for every copier: once the stage's last fill is done
+        // with (so a copier record in it is no longer read), hand the copier an
+        // end record.
+        for (int s = 0; s < kStages; ++s) {
+          if (((issued_mask >> s) & 1u) &&
+              !wait_bar(p, &empty[s], (issued_parity >> s) & 1u, abort_flag, kSiteStreamEnd))
+            break;  // abort flag set: the copiers leave on it
+          info[kInfoWords * s + 1] = kInfoEnd;
+          mbar_arrive(&cready[s]);
+        }
       }
       if (aborted || *abort_flag) {
         // Let every issued load land before shared memory is released.
@@ -681,7 +775,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
             break;
           }
           tcgen05_fence_after_sync();
-          const bool a_mn = (info[4 * stage] & kInfoAmn) != 0;
+          const bool a_mn = (info[kInfoWords * stage] & kInfoAmn) != 0;
           const uint32_t idesc = a_mn ? idesc_mn : idesc_k;
           const uint32_t a_addr = smem_u32(smem + stage * kStageBytes);
           const uint32_t b_addr = a_addr + kAStageBytes;
@@ -777,110 +871,34 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
     if (lane == 0) bulk_wait_group<0>();
     __syncwarp();
   } else if (kFused && warp == 2 + kEpiWarps) {
-    // ---------------------------------------------------------- stager
-    // Publishes staged chunks.  The copier warps write each owner box into
-    // a_gathered (and the [K, M] staging); once every box of a chunk is
-    // written, this warp releases the chunk's flag.  It reads each stage's
-    // record, so it takes part in the stage's empty barrier.
-    if (lane == 0) {
-      // Chunks waiting for the copiers: (flag index, sequence index of the
-      // chunk's last box).  Kept in shared memory: a dynamically indexed local
-      // array would live in local memory, which misses to L2 when shared
-      // memory takes the L1.
-      int* tq_flag = stager_q;            // [kStages]
-      int* tq_last = stager_q + kStages;  // [kStages]
-      int ntq = 0;
-      auto publish = [&](int idx) {
-        if (idx != p.inject_skip_flag)
-          st_release_gpu(p.flags + idx, p.fbase + (uint64_t)chunk_boxes(p, idx % p.G));
-      };
-      // Box i is written once its copier (warp i % 4) has finished sequence
-      // slot i / 4; per-warp progress is in order, so checking the chunk's
-      // last box of each residue covers the whole chunk.
-      auto copied = [&](int last, int nbox) -> bool {
-        for (int k = last; k > last - nbox && k > last - kCopyWarps; --k)
-          if ((int)ld_acquire_cta_shared(smem_u32(tprog + (k % kCopyWarps))) <= k / kCopyWarps)
-            return false;
-        return true;
-      };
-      auto drain = [&](bool block) {
-        while (ntq > 0) {
-          const int nbox = chunk_boxes(p, tq_flag[0] % p.G);
-          if (!copied(tq_last[0], nbox)) {
-            if (!block) return;
-            const uint64_t t0 = globaltimer_ns();
-            while (!copied(tq_last[0], nbox)) {
-              if (*abort_flag || globaltimer_ns() - t0 > (uint64_t)p.pipe_timeout_ns) return;
-            }
-          }
-          fence_acquire_gpu();
-          publish(tq_flag[0]);
-          for (int k = 1; k < ntq; ++k) {
-            tq_flag[k - 1] = tq_flag[k];
-            tq_last[k - 1] = tq_last[k];
-          }
-          --ntq;
-        }
-      };
-      bool aborted = false;
-      for (int i = 0; i < my_stages && !aborted; ++i) {
-        const int s = i % kStages;
-        const uint32_t ph = (uint32_t)(i / kStages) & 1u;
-        // While the stage is not there yet, keep publishing what the copiers
-        // finish, so that no follower waits on a chunk this warp holds back.
-        if (!mbar_try_wait(&full[s], ph)) {
-          const uint64_t t0 = globaltimer_ns();
-          for (uint32_t it = 1;; ++it) {
-            if (ntq) drain(false);
-            if (mbar_try_wait(&full[s], ph)) break;
-            if ((it & 63u) == 0 && (*abort_flag || globaltimer_ns() - t0 > (uint64_t)p.pipe_timeout_ns)) {
-              if (!*abort_flag) {
-                *abort_flag = 1;
-                record_error(p.err, p.epoch, kErrTimeout, kSiteStager);
-              }
-              aborted = true;
-              break;
-            }
-          }
-          if (aborted) break;
-        }
-        const uint32_t bits = info[4 * s];
-        const int flag_idx = (int)info[4 * s + 3];
-        mbar_arrive(&empty[s]);
-        if ((bits & kInfoPublish) && (bits & kInfoLast)) {
-          if (ntq == kStages) drain(true);
-          tq_flag[ntq] = flag_idx;
-          tq_last[ntq] = i;
-          ++ntq;
-        }
-        if (ntq) drain(false);
-      }
-      drain(true);
-    }
-    __syncwarp();
-  } else if (kFused && warp == 3 + kEpiWarps) {
     // ---------------------------------------------------------- register fetcher
     regfetch_loop(p, lane, kLayoutM);
     __syncwarp();
   } else if (kFused) {
     // ---------------------------------------------------------- copiers
-    // Warp w owns pipeline stage w.  For each box its owner had staged it
-    // reads the landed K-major (128-byte swizzled) tile, releases the stage as
-    // soon as the reads are done, and writes the rows into a_gathered with
-    // 16-byte stores; for the m-contiguous layout it also writes the box
-    // transposed into the [K, M] staging (8x8 register transposes), which is
-    // what followers read.  Then it reports progress to the stager.
-    const int w = warp - (4 + kEpiWarps);
+    // Warp w owns pipeline stage w and takes, in order, the boxes the issuer
+    // stages there.  For each it waits for the box to land, reads the K-major
+    // (128-byte swizzled) tile, frees the stage and writes the rows into
+    // a_gathered with 16-byte stores; for the m-contiguous layout it also
+    // writes a published box transposed into the [K, M] staging (8x8 register
+    // transposes), which is what followers read.  The copier of a chunk's last
+    // box publishes the chunk once the other copiers' boxes of it are written.
+    const int w = warp - (3 + kEpiWarps);
     const int s = w;
     const uint32_t a_u32 = smem_u32(smem + s * kStageBytes);
     const int ch = lane & 7;  // 16-byte chunk of a 128-byte row: 4 rows x 8 chunks per access
-    for (int i = w; i < my_stages; i += kStages) {
-      const uint32_t ph = (uint32_t)(i / kStages) & 1u;
-      const bool ok = wait_bar(p, &full[s], ph, abort_flag, kSiteCopy);
+    for (uint32_t n = 0;; ++n) {
+      const bool got = wait_handoff(p, &cready[s], n, iseq, abort_flag);
+      if (!__all_sync(0xffffffffu, got)) break;
+      // The record stays until this warp frees the stage (its empty arrive).
+      const uint32_t* inf = info + kInfoWords * s + 1;
+      const uint32_t bits = inf[0];
+      if (bits & kInfoEnd) break;
+      const int mb = (int)inf[1], kb = (int)inf[2], flag_idx = (int)inf[3];
+      const int seq = (int)inf[4], nbox = (int)inf[5];
+      const bool ok = wait_bar(p, &full[s], (bits & kInfoPhase) ? 1u : 0u, abort_flag, kSiteCopy);
       if (!__all_sync(0xffffffffu, ok)) break;
-      const uint32_t bits = info[4 * s];
-      const int mb = (int)info[4 * s + 1], kb = (int)info[4 * s + 2];
-      if (bits & kInfoStage) {
+      {
         const int k = kb * kBK + ch * 8;
         const bool k_ok = k < p.K;
 #pragma unroll 1
@@ -917,15 +935,16 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
             }
           }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-        __threadfence();
-        __syncwarp();
-      } else {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
       }
-      if (lane == 0) st_release_cta_shared(smem_u32(tprog + w), (uint32_t)(i / kStages + 1));
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&empty[s]);
+        st_release_cta_shared(smem_u32(tprog + w), (uint32_t)seq + 1u);
+        if ((bits & kInfoPublish) && (bits & kInfoLast) &&
+            chunk_written(p, tprog, seq, nbox, abort_flag) && flag_idx != p.inject_skip_flag)
+          st_release_gpu(p.flags + flag_idx, p.fbase + (uint64_t)nbox);
+      }
+      __syncwarp();
     }
     __syncwarp();
   }
