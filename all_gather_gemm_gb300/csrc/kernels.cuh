@@ -21,16 +21,16 @@
 //   warp 6      register fetcher (fused only): copies chunks that TMA cannot
 //               load from a single shard (a row block straddling shards whose
 //               row count is not a multiple of 8) and publishes them.
-//   warps 7-10  copiers (fused only), one per pipeline stage.  The issuer
-//               hands a copier only the boxes it stages (a pair of mbarriers
-//               per stage, so the MMA's own pipeline is the plain GEMM's for
-//               every other box).  The copier reads the landed box from shared
-//               memory, frees the stage, and writes the box into a_gathered
-//               (the k-contiguous staging) -- and, for the m-contiguous
-//               layout, transposed into the [K, M] staging, which is what
-//               followers then read.  The copier that writes the last box of
-//               a chunk publishes the chunk once the other copiers' boxes of
-//               it are written.
+//   warps 7-10  copiers (fused only), off the MMA pipeline.  When the issuer
+//               starts a chunk it stages, it hands the chunk's record to the
+//               copiers through a ring in shared memory; they copy the chunk's
+//               boxes (spread over the four warps) from its shard into
+//               a_gathered (the k-contiguous staging) -- and, for the
+//               m-contiguous layout, transposed into the [K, M] staging, which
+//               is what followers then read -- with 16-byte global loads and
+//               stores, and the last of them to finish publishes the chunk.
+//               The issuer loads the same boxes into the pipeline for its own
+//               MMAs as usual, so the pipeline is the plain GEMM's.
 //
 // Each staged box is therefore read from its shard once, by the CTA that also
 // multiplies it ("fetch once, write through"), and no atomic sits on the
@@ -71,7 +71,7 @@ constexpr int kEpiCols = 64;                           // columns per store box 
 constexpr int kEpiBufBytes = kEpiRows * kEpiCols * 2;  // 4 KB
 constexpr int kEpiBufs = 2;
 constexpr int kTmemCols = 2 * kBN;
-constexpr int kCopyWarps = 4;  // fused kernel: one copier warp per pipeline stage
+constexpr int kCopyWarps = 4;  // fused kernel: warps copying staged chunks
 constexpr int kMaxShards = 16;
 constexpr int kFlagShift = 20;      // flag base = epoch << 20; boxes per chunk < 2^20
 
@@ -85,33 +85,30 @@ __host__ __device__ constexpr int mode_threads(int m) {
   return 32 * (2 + kEpiWarps + (mode_fused(m) ? 1 + kCopyWarps : 0));
 }
 
-// Per-stage record written by the TMA issuer: word 0 = the box's bits, read
-// by the MMA warp once the stage is full; words 1-6 = the copier's record
-// {bits, mb, kb, flag index, sequence index, boxes in the chunk}, written
-// before a staged box is handed to the stage's copier and kept until the
-// copier frees the stage.  The two never share a word, so the end record
-// (kInfoEnd in word 1) cannot race with the MMA warp.
-constexpr int kInfoWords = 8;
-constexpr uint32_t kInfoStage = 1u;    // A box is to be stored into a_gathered
-constexpr uint32_t kInfoPublish = 2u;  // ... and its chunk published once staged
-constexpr uint32_t kInfoAmn = 4u;      // A box in shared memory is MN-major
-constexpr uint32_t kInfoLast = 8u;     // last box of its chunk
-constexpr uint32_t kInfoPhase = 16u;   // parity of the full-barrier phase of this fill
-constexpr uint32_t kInfoEnd = 32u;     // hand-off only: the issuer is done, the copier leaves
+// Bits of a stage's record (read by the MMA warp once the stage is full) and
+// of a chunk record handed to the copiers.
+constexpr uint32_t kInfoStage = 1u;    // chunk: to be written into a_gathered
+constexpr uint32_t kInfoPublish = 2u;  // chunk: ... and published once written
+constexpr uint32_t kInfoAmn = 4u;      // stage: the A box in shared memory is MN-major
+constexpr uint32_t kInfoEnd = 8u;      // chunk record: the issuer is done, the copiers leave
 
-// full, empty [kStages]; tmem_full, tmem_empty [2]; drain; cready [kStages]
-constexpr int kNumBars = 3 * kStages + 4 + 1;
-static_assert(kCopyWarps == kStages, "copier warp w owns pipeline stage w");
+// Chunk records handed from the issuer to the copiers:
+// {bits, mb, first k-block, boxes, flag index, box sequence index, done count, -}.
+constexpr int kRing = 8;
+constexpr int kRingWords = 8;
+
+// full, empty [kStages]; tmem_full, tmem_empty [2]; drain; rfull, rfree [kRing]
+constexpr int kNumBars = 2 * kStages + 4 + 1 + 2 * kRing;
 constexpr int kSmemData = kStages * kStageBytes + kEpiWarps * kEpiBufs * kEpiBufBytes;
 constexpr int kSmemBytes =
-    1024 + kSmemData + 8 * kNumBars + 4 * kInfoWords * kStages + 4 * kCopyWarps + 64;
+    1024 + kSmemData + 8 * kNumBars + 4 * kStages + 4 * kRing * kRingWords + 16 + 64;
 static_assert(kSmemBytes <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
 
 // Error code written to the device error word (matches ag_status).
 constexpr uint32_t kErrTimeout = 4;
 // Sites reported with a pipeline timeout (ready-flag timeouts report the flag index).
 constexpr uint32_t kSiteEmpty = 0xF00001, kSiteFull = 0xF00002, kSiteTmemEmpty = 0xF00003,
-                   kSiteTmemFull = 0xF00004, kSiteStreamEnd = 0xF00005, kSiteCopy = 0xF00006;
+                   kSiteTmemFull = 0xF00004, kSiteRing = 0xF00005, kSiteCopy = 0xF00006;
 
 // Trace roles (see include/agmm.h).
 constexpr uint32_t kTraceClaim = 1, kTraceWait = 2, kTraceTile = 3, kTraceGather = 4,
@@ -306,10 +303,10 @@ __device__ __forceinline__ bool wait_bar(const GemmParams& p, uint64_t* bar, uin
   }
 }
 
-// Copier side of the hand-off: waits for the n-th record the issuer hands
-// to this stage's copier (phase n of `bar`).  False on abort or timeout.  A
-// copier may idle for as long as its CTA has nothing to stage, so the time
-// limit restarts whenever the issuer makes progress (`iseq`).
+// Copier side of the hand-off: waits for phase `n` of a ring slot's `rfull`
+// barrier (the issuer's n-th record in that slot).  False on abort or
+// timeout.  Copiers may idle for as long as their CTA has nothing to stage,
+// so the time limit restarts whenever the issuer makes progress (`iseq`).
 __device__ __forceinline__ bool wait_handoff(const GemmParams& p, uint64_t* bar, uint32_t n,
                                              volatile uint32_t* iseq, volatile int* abort_flag) {
   const uint32_t parity = n & 1u;
@@ -332,33 +329,6 @@ __device__ __forceinline__ bool wait_handoff(const GemmParams& p, uint64_t* bar,
       }
     }
   }
-}
-
-// Publication check by the copier of a chunk's last box (sequence index
-// `seq`): the chunk's boxes are seq - nbox + 1 .. seq, box i sits in stage
-// i % kStages, and each copier writes its boxes in order and then advances
-// tprog to (index + 1) with a CTA-scope release.  So the chunk is written once
-// the latest of its boxes in every other stage is.  Bounded; false on abort
-// or timeout (the chunk then stays unpublished and its followers report it).
-__device__ __forceinline__ bool chunk_written(const GemmParams& p, const uint32_t* tprog, int seq,
-                                              int nbox, volatile int* abort_flag) {
-  const int others = min(nbox, kCopyWarps) - 1;
-  const uint64_t t0 = globaltimer_ns();
-  for (int q = 1; q <= others; ++q) {
-    const int i = seq - q;
-    const uint32_t slot = smem_u32(tprog + (i % kCopyWarps));
-    for (uint32_t it = 0; ld_acquire_cta_shared(slot) <= (uint32_t)i; ++it) {
-      if ((it & 63u) == 63u &&
-          (*abort_flag || globaltimer_ns() - t0 > (uint64_t)p.pipe_timeout_ns)) {
-        if (!*abort_flag) {
-          *abort_flag = 1;
-          record_error(p.err, p.epoch, kErrTimeout, kSiteCopy);
-        }
-        return false;
-      }
-    }
-  }
-  return true;
 }
 
 // Follower wait on a chunk: bounded acquire-polling until flag >= target.
@@ -524,11 +494,12 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
   uint64_t* tmem_full = bars + 2 * kStages;  // [2] accumulator ready
   uint64_t* tmem_empty = tmem_full + 2;      // [2] accumulator drained
   uint64_t* drain = tmem_empty + 2;          // [1] final MMA drain
-  uint64_t* cready = drain + 1;              // [kStages] fused: a staged box handed to the copier
-  uint32_t* info = reinterpret_cast<uint32_t*>(cready + kStages);  // [kStages][kInfoWords]
-  uint32_t* tprog = info + kInfoWords * kStages;  // [kCopyWarps] sequence index + 1 of the last box written
-  volatile uint32_t* iseq = tprog + kCopyWarps;   // issuer progress (chunks), a liveness signal
-  uint32_t* tmem_slot = tprog + kCopyWarps + 1;
+  uint64_t* rfull = drain + 1;               // [kRing] fused: chunk record written
+  uint64_t* rfree = rfull + kRing;           // [kRing] fused: every copier is done with it
+  uint32_t* info = reinterpret_cast<uint32_t*>(rfree + kRing);  // [kStages] stage bits
+  uint32_t* ring = info + kStages;                // [kRing][kRingWords] chunk records
+  volatile uint32_t* iseq = ring + kRing * kRingWords;  // issuer progress (chunks), a liveness signal
+  uint32_t* tmem_slot = ring + kRing * kRingWords + 1;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -536,20 +507,19 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
   const int my_tiles = my_tile_count(p);
 
   if (threadIdx.x == 0) {
-    // empty: the MMA commit, and (fused) the stage's copier for a staged box
-    // or the issuer itself, at fill time, for any other box -- so the issuer
-    // waits on one barrier per box either way.
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kFused ? 2 : 1);
-      mbar_init(&cready[s], 1);
+      mbar_init(&empty[s], 1);  // the MMA commit
+    }
+    for (int r = 0; r < kRing; ++r) {
+      mbar_init(&rfull[r], 1);
+      mbar_init(&rfree[r], kCopyWarps);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tmem_full[b], 1);
       mbar_init(&tmem_empty[b], 32 * kEpiWarps);
     }
     mbar_init(drain, 1);
-    for (int w = 0; w < kCopyWarps; ++w) tprog[w] = 0;
     *iseq = 0;
     *abort_flag = 0;
     fence_mbarrier_init();
@@ -574,6 +544,8 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
       bool aborted = false;
       int stage = 0, seq = 0;
       uint32_t phase = 0;
+      int rslot = 0;        // fused: next ring slot for a chunk record
+      uint32_t rphase = 0;  // ... and the parity of its use
       // Chunk cursor over this CTA's (tile, k-group) sequence.  Tile (mb, nb)
       // owns the window [chunk_start(nb), chunk_start(nb + 1)) and visits it
       // first (chunk_at).  Everything that needs a
@@ -627,6 +599,26 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
             trace_rec(p.trace, p.trace_words, kTraceClaim, mb, g, now, now);
           }
         }
+        if (kFused && (bits & kInfoStage)) {
+          // Hand the chunk to the copiers (the arrive releases the record).
+          if (!wait_bar(p, &rfree[rslot], rphase ^ 1u, abort_flag, kSiteRing)) {
+            aborted = true;
+            break;
+          }
+          uint32_t* rec = ring + rslot * kRingWords;
+          rec[0] = bits;
+          rec[1] = (uint32_t)mb;
+          rec[2] = (uint32_t)(g * p.kpf);
+          rec[3] = (uint32_t)nbox;
+          rec[4] = (uint32_t)flag_idx;
+          rec[5] = (uint32_t)seq;
+          rec[6] = 0u;
+          mbar_arrive(&rfull[rslot]);
+          if (++rslot == kRing) {
+            rslot = 0;
+            rphase ^= 1u;
+          }
+        }
         if (!direct && kLayoutM) bits |= kInfoAmn;
 
         // Next chunk in sequence.  Only a follower chunk reads its flag; owner
@@ -661,23 +653,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
             aborted = true;
             break;
           }
-          uint32_t* inf = info + kInfoWords * stage;
-          const uint32_t box_bits = bits | (j == nbox - 1 ? kInfoLast : 0u);
-          inf[0] = box_bits;
-          if (kFused) {
-            if (bits & kInfoStage) {
-              // Hand the box to the stage's copier (the arrive releases the record).
-              inf[1] = box_bits | (phase ? kInfoPhase : 0u);
-              inf[2] = (uint32_t)mb;
-              inf[3] = (uint32_t)kb;
-              inf[4] = (uint32_t)flag_idx;
-              inf[5] = (uint32_t)seq;
-              inf[6] = (uint32_t)nbox;
-              mbar_arrive(&cready[stage]);
-            } else {
-              mbar_arrive(&empty[stage]);  // no copier reads this box
-            }
-          }
+          info[stage] = bits;
           uint8_t* a_dst = smem + stage * kStageBytes;
           uint8_t* b_dst = a_dst + kAStageBytes;
           mbar_arrive_expect_tx(&full[stage], kStageBytes);
@@ -727,17 +703,11 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
         if (nxt_follow) cur_peek = nxt_peek;
         if (kFused) *iseq = (uint32_t)seq;
       }
-      if (kFused) {
-        // End of stream for every copier: once the stage's last fill is done
-        // with (so a copier record in it is no longer read), hand the copier an
-        // end record.
-        for (int s = 0; s < kStages; ++s) {
-          if (((issued_mask >> s) & 1u) &&
-              !wait_bar(p, &empty[s], (issued_parity >> s) & 1u, abort_flag, kSiteStreamEnd))
-            break;  // abort flag set: the copiers leave on it
-          info[kInfoWords * s + 1] = kInfoEnd;
-          mbar_arrive(&cready[s]);
-        }
+      if (kFused && wait_bar(p, &rfree[rslot], rphase ^ 1u, abort_flag, kSiteRing)) {
+        // End of stream (if the slot does not free, the abort flag is set and
+        // the copiers leave on it).
+        ring[rslot * kRingWords] = kInfoEnd;
+        mbar_arrive(&rfull[rslot]);
       }
       if (aborted || *abort_flag) {
         // Let every issued load land before shared memory is released.
@@ -775,7 +745,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
             break;
           }
           tcgen05_fence_after_sync();
-          const bool a_mn = (info[kInfoWords * stage] & kInfoAmn) != 0;
+          const bool a_mn = (info[stage] & kInfoAmn) != 0;
           const uint32_t idesc = a_mn ? idesc_mn : idesc_k;
           const uint32_t a_addr = smem_u32(smem + stage * kStageBytes);
           const uint32_t b_addr = a_addr + kAStageBytes;
@@ -876,73 +846,72 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
     __syncwarp();
   } else if (kFused) {
     // ---------------------------------------------------------- copiers
-    // Warp w owns pipeline stage w and takes, in order, the boxes the issuer
-    // stages there.  For each it waits for the box to land, reads the K-major
-    // (128-byte swizzled) tile, frees the stage and writes the rows into
-    // a_gathered with 16-byte stores; for the m-contiguous layout it also
-    // writes a published box transposed into the [K, M] staging (8x8 register
-    // transposes), which is what followers read.  The copier of a chunk's last
-    // box publishes the chunk once the other copiers' boxes of it are written.
+    // Take the issuer's chunk records in order.  Box j of a chunk whose first
+    // box has sequence index q goes to warp (q + j) % kCopyWarps, so the
+    // boxes of consecutive chunks spread evenly over the warps.  A box is
+    // copied in 8-row groups: lane = (row group, 16-byte column chunk), 8 rows
+    // of 16 bytes per lane, two groups (16 loads) in flight; for the
+    // m-contiguous layout a published box is also written transposed (8x8
+    // register transposes) into the [K, M] staging.  Each warp that copied
+    // boxes of a chunk then adds one to the record's done count (acq_rel, CTA
+    // scope); the one that completes it publishes the chunk (release, GPU
+    // scope), so the flag follows every copier's writes.
     const int w = warp - (3 + kEpiWarps);
-    const int s = w;
-    const uint32_t a_u32 = smem_u32(smem + s * kStageBytes);
-    const int ch = lane & 7;  // 16-byte chunk of a 128-byte row: 4 rows x 8 chunks per access
+    const int ch = lane & 7;  // 16-byte column chunk of a 128-byte box row
     for (uint32_t n = 0;; ++n) {
-      const bool got = wait_handoff(p, &cready[s], n, iseq, abort_flag);
+      const int slot = (int)(n % kRing);
+      const bool got = wait_handoff(p, &rfull[slot], n / kRing, iseq, abort_flag);
       if (!__all_sync(0xffffffffu, got)) break;
-      // The record stays until this warp frees the stage (its empty arrive).
-      const uint32_t* inf = info + kInfoWords * s + 1;
-      const uint32_t bits = inf[0];
+      uint32_t* rec = ring + slot * kRingWords;
+      const uint32_t bits = rec[0];
       if (bits & kInfoEnd) break;
-      const int mb = (int)inf[1], kb = (int)inf[2], flag_idx = (int)inf[3];
-      const int seq = (int)inf[4], nbox = (int)inf[5];
-      const bool ok = wait_bar(p, &full[s], (bits & kInfoPhase) ? 1u : 0u, abort_flag, kSiteCopy);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      {
-        const int k = kb * kBK + ch * 8;
-        const bool k_ok = k < p.K;
+      const int mb = (int)rec[1], kb0 = (int)rec[2], nbox = (int)rec[3], flag_idx = (int)rec[4];
+      const int q = (int)rec[5];
+      const int j0 = (w - q % kCopyWarps + kCopyWarps) % kCopyWarps;
+      const bool publish_m = kLayoutM && (bits & kInfoPublish);
+      const int row0 = mb * kBM;
+      for (int j = j0; j < nbox; j += kCopyWarps) {
+        const int k = (kb0 + j) * kBK + ch * 8;
+        if (k >= p.K) continue;  // K % 8 == 0: a column chunk is all in or all out
 #pragma unroll 1
-        for (int it0 = 0; it0 < kBM / 4; it0 += 8) {
-          uint4 v[8];
+        for (int b = 0; b < 4; b += 2) {
+          uint4 v[2][8];
+          int m[2];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int row = (it0 + u) * 4 + (lane >> 3);
-            v[u] = ld_shared_v4(a_u32 + row * 128 + ((ch ^ (row & 7)) << 4));
-          }
+          for (int h = 0; h < 2; ++h) {
+            // Row group rg = 8 consecutive rows; with m_per_shard % 8 == 0 (or
+            // a row block inside one shard) the group is inside one shard.
+            m[h] = row0 + (4 * (b + h) + (lane >> 3)) * 8;
+            const int nrow = min(8, p.M - m[h]);
+            if (nrow > 0) {
+              const uint16_t* src = shard_row(p.shards, p.mps, p.K, m[h]) + k;
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int m = mb * kBM + (it0 + u) * 4 + (lane >> 3);
-            if (k_ok && m < p.M) st_v4(p.a_gathered + (int64_t)m * p.K + k, v[u]);
-          }
-        }
-        if (kLayoutM && (bits & kInfoPublish)) {
-          // lane -> (row group rg, column group cg): a warp reads 4 rows x 8
-          // chunks per instruction, the conflict-free pattern for this swizzle.
-#pragma unroll 1
-          for (int b = 0; b < 4; ++b) {
-            const int rg = 4 * b + (lane >> 3);
-            uint4 v[8];
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-              const int row = rg * 8 + r;
-              v[r] = ld_shared_v4(a_u32 + row * 128 + ((ch ^ (row & 7)) << 4));
+              for (int r = 0; r < 8; ++r)
+                if (r < nrow) v[h][r] = ld_stream_v4(src + (int64_t)r * p.K);
             }
-            const int m = mb * kBM + rg * 8;
-            if (m < p.M && k_ok) {
+          }
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int nrow = min(8, p.M - m[h]);
+#pragma unroll
+            for (int r = 0; r < 8; ++r)
+              if (r < nrow) st_v4(p.a_gathered + (int64_t)(m[h] + r) * p.K + k, v[h][r]);
+            if (publish_m && nrow == 8) {  // M % 8 == 0 for this layout
 #pragma unroll
               for (int c = 0; c < 8; ++c)
-                st_v4(p.staging_mk + (int64_t)(k + c) * p.M + m, transpose_col(v, c));
+                st_v4(p.staging_mk + (int64_t)(k + c) * p.M + m[h], transpose_col(v[h], c));
             }
           }
         }
       }
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&empty[s]);
-        st_release_cta_shared(smem_u32(tprog + w), (uint32_t)seq + 1u);
-        if ((bits & kInfoPublish) && (bits & kInfoLast) &&
-            chunk_written(p, tprog, seq, nbox, abort_flag) && flag_idx != p.inject_skip_flag)
-          st_release_gpu(p.flags + flag_idx, p.fbase + (uint64_t)nbox);
+        if ((bits & kInfoPublish) && j0 < nbox) {
+          const uint32_t done = atom_add_acq_rel_cta_shared(smem_u32(rec + 6), 1u) + 1u;
+          if (done == (uint32_t)min(nbox, kCopyWarps) && flag_idx != p.inject_skip_flag)
+            st_release_gpu(p.flags + flag_idx, p.fbase + (uint64_t)nbox);
+        }
+        mbar_arrive(&rfree[slot]);
       }
       __syncwarp();
     }

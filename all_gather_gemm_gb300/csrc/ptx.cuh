@@ -146,6 +146,16 @@ __device__ __forceinline__ uint64_t atom_max_relaxed_gpu(uint64_t* p, uint64_t v
   return old;
 }
 
+// Returns the old value; acquire+release at CTA scope (shared memory).
+__device__ __forceinline__ uint32_t atom_add_acq_rel_cta_shared(uint32_t addr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;"
+               : "=r"(old)
+               : "r"(addr), "r"(v)
+               : "memory");
+  return old;
+}
+
 __device__ __forceinline__ void red_release_add_gpu(uint64_t* p, uint64_t v) {
   asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
