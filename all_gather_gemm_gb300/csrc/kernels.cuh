@@ -303,6 +303,21 @@ __device__ __forceinline__ bool wait_bar(const GemmParams& p, uint64_t* bar, uin
   }
 }
 
+// Issuer side of the hand-off: writes a chunk record into a ring slot and
+// arrives on the slot's rfull barrier (the arrive releases the record).
+__device__ __forceinline__ void hand_chunk(uint32_t* rec, uint64_t* rfull_bar, uint32_t bits,
+                                           int mb, int g, int nbox, int flag_idx, int seq,
+                                           const GemmParams& p) {
+  rec[0] = bits;
+  rec[1] = (uint32_t)mb;
+  rec[2] = (uint32_t)(g * p.kpf);
+  rec[3] = (uint32_t)nbox;
+  rec[4] = (uint32_t)flag_idx;
+  rec[5] = (uint32_t)seq;
+  rec[6] = 0u;  // done count
+  mbar_arrive(rfull_bar);
+}
+
 // Copier side of the hand-off: waits for phase `n` of a ring slot's `rfull`
 // barrier (the issuer's n-th record in that slot).  False on abort or
 // timeout.  Copiers may idle for as long as their CTA has nothing to stage,
@@ -341,15 +356,24 @@ __device__ __forceinline__ bool wait_or_take(const GemmParams& p, int flag_idx, 
                                              int owner_tile) {
   uint64_t* f = p.flags + flag_idx;
   const uint64_t t0 = globaltimer_ns();
-  uint32_t ns = 32;
+  // Once the owner tile is seen started it stays started for this call, so
+  // its word is no longer read; while it is read, both loads are in flight at
+  // once.  Polls are relaxed: one acquire fence follows the poll that sees
+  // the chunk published.
+  bool owner_started = owner_tile < 0;
   for (uint32_t it = 0;; ++it) {
-    const uint64_t v = ld_acquire_gpu(f);
-    if (v >= target) return false;
-    if (v < p.fbase && owner_tile >= 0 && ld_relaxed_gpu(p.started + owner_tile) != p.epoch &&
-        atom_max_relaxed_gpu(f, p.fbase) < p.fbase)
+    const uint64_t v = ld_relaxed_gpu(f);
+    const uint64_t st = owner_started ? p.epoch : ld_relaxed_gpu(p.started + owner_tile);
+    if (v >= target) {
+      fence_acquire_gpu();
+      return false;
+    }
+    if (st == p.epoch) {
+      owner_started = true;
+    } else if (v < p.fbase && atom_max_relaxed_gpu(f, p.fbase) < p.fbase) {
       return true;
-    __nanosleep(ns);
-    if (ns < 256) ns <<= 1;
+    }
+    __nanosleep(64);
     if ((it & 15u) == 15u) {
       if (error_this_call(p)) return false;
       if (globaltimer_ns() - t0 > (uint64_t)p.timeout_ns || it > (1u << 26)) {
@@ -552,14 +576,26 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
       // division is computed once per tile; a chunk costs a few adds.  A
       // follower's flag is read one chunk ahead, so its latency overlaps the
       // current chunk's loads.
+      //
+      // Staging ahead (fused): while it works on a tile, the issuer hands the
+      // window of its next tile (nxt) to the copiers, one chunk per chunk it
+      // issues and only when a ring slot is free at once, so that tile's
+      // followers in other CTAs find those chunks published early.  `pre`
+      // counts the chunks of nxt handed so far (window order), `cur_pre`
+      // those of the current tile, which it then loads without staging.  The
+      // next tile is marked started only once its whole window is handed:
+      // until then a follower may still take its chunks over, as for any
+      // tile that has not started.
       TileCtx cur, nxt;
       int t = blockIdx.x, gi = 0;
+      int pre = 0, cur_pre = 0;
       uint64_t cur_peek = 0;
       if (t < p.num_tiles) {
         tile_ctx<kFused>(p, t, cur);
         const int g0 = chunk_at(0, cur.ws, cur.we);
         if (cur.kind != kLocal && !cur.owns(g0))
           cur_peek = ld_relaxed_gpu(p.flags + cur.mb * p.G + g0);
+        if (t + (int)gridDim.x < p.num_tiles) tile_ctx<kFused>(p, t + gridDim.x, nxt);
       }
       const int last_nbox = chunk_boxes(p, p.G - 1);
       while (t < p.num_tiles && !aborted) {
@@ -573,12 +609,14 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
         bool direct = false;  // A straight from a shard (else from the staging)
         uint32_t bits = 0;
         if (kFused) {
+          const bool staged_ahead = cur.owns(g) && g - cur.ws < cur_pre;
           if (kind == kLocal) {
             direct = true;
-            if (cur.owns(g)) bits = kInfoStage;  // the owner writes the local rows of a_gathered
+            // the owner writes the local rows of a_gathered
+            if (cur.owns(g) && !staged_ahead) bits = kInfoStage;
           } else if (kind == kDirect && cur.owns(g)) {
             direct = true;
-            bits = kInfoStage | kInfoPublish;
+            if (!staged_ahead) bits = kInfoStage | kInfoPublish;
           } else {
             const uint64_t target = p.fbase + (uint64_t)nbox;
             if (cur_peek >= target) {
@@ -600,20 +638,12 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
           }
         }
         if (kFused && (bits & kInfoStage)) {
-          // Hand the chunk to the copiers (the arrive releases the record).
+          // Hand the chunk to the copiers.
           if (!wait_bar(p, &rfree[rslot], rphase ^ 1u, abort_flag, kSiteRing)) {
             aborted = true;
             break;
           }
-          uint32_t* rec = ring + rslot * kRingWords;
-          rec[0] = bits;
-          rec[1] = (uint32_t)mb;
-          rec[2] = (uint32_t)(g * p.kpf);
-          rec[3] = (uint32_t)nbox;
-          rec[4] = (uint32_t)flag_idx;
-          rec[5] = (uint32_t)seq;
-          rec[6] = 0u;
-          mbar_arrive(&rfull[rslot]);
+          hand_chunk(ring + rslot * kRingWords, &rfull[rslot], bits, mb, g, nbox, flag_idx, seq, p);
           if (++rslot == kRing) {
             rslot = 0;
             rphase ^= 1u;
@@ -630,7 +660,6 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
           ngi = 0;
           nt += gridDim.x;
           new_tile = true;
-          if (nt < p.num_tiles) tile_ctx<kFused>(p, nt, nxt);
         }
         // (scalar selects, not a reference: the cursor must stay in registers)
         const int n_mb = new_tile ? nxt.mb : cur.mb;
@@ -697,9 +726,32 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
           trace_rec(p.trace, p.trace_words, kTraceIssue, mb,
                     (uint32_t)g | (direct ? 1u << 16 : 0u) | ((bits & kInfoStage) ? 2u << 16 : 0u),
                     t_chunk, globaltimer_ns());
+        if (kFused && !aborted && !new_tile && t + (int)gridDim.x < p.num_tiles &&
+            nxt.kind != kRegFetch && pre < nxt.we - nxt.ws &&
+            mbar_test_wait(&rfree[rslot], rphase ^ 1u)) {
+          // Stage ahead: one chunk of the next tile's window.
+          const int pg = nxt.ws + pre;
+          hand_chunk(ring + rslot * kRingWords, &rfull[rslot],
+                     kInfoStage | (nxt.kind == kDirect ? kInfoPublish : 0u), nxt.mb, pg,
+                     chunk_boxes(p, pg), nxt.mb * p.G + pg, seq, p);
+          if (p.trace) {
+            const uint64_t now = globaltimer_ns();
+            trace_rec(p.trace, p.trace_words, kTraceClaim, nxt.mb, pg, now, now);
+          }
+          if (++rslot == kRing) {
+            rslot = 0;
+            rphase ^= 1u;
+          }
+          if (++pre == nxt.we - nxt.ws) st_relaxed_gpu(p.started + t + gridDim.x, p.epoch);
+        }
         t = nt;
         gi = ngi;
-        if (new_tile) cur = nxt;
+        if (new_tile) {
+          cur = nxt;
+          cur_pre = pre;
+          pre = 0;
+          if (t + (int)gridDim.x < p.num_tiles) tile_ctx<kFused>(p, t + gridDim.x, nxt);
+        }
         if (nxt_follow) cur_peek = nxt_peek;
         if (kFused) *iseq = (uint32_t)seq;
       }
