@@ -609,14 +609,17 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
         bool direct = false;  // A straight from a shard (else from the staging)
         uint32_t bits = 0;
         if (kFused) {
+          // A window chunk staged ahead is read like a follower's: from the
+          // staging its copiers wrote a tile ago (still in L2), not again from
+          // the shard.
           const bool staged_ahead = cur.owns(g) && g - cur.ws < cur_pre;
           if (kind == kLocal) {
             direct = true;
             // the owner writes the local rows of a_gathered
             if (cur.owns(g) && !staged_ahead) bits = kInfoStage;
-          } else if (kind == kDirect && cur.owns(g)) {
+          } else if (kind == kDirect && cur.owns(g) && !staged_ahead) {
             direct = true;
-            if (!staged_ahead) bits = kInfoStage | kInfoPublish;
+            bits = kInfoStage | kInfoPublish;
           } else {
             const uint64_t target = p.fbase + (uint64_t)nbox;
             if (cur_peek >= target) {
@@ -666,11 +669,14 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
         const int n_kind = new_tile ? nxt.kind : cur.kind;
         const int n_ws = new_tile ? nxt.ws : cur.ws;
         const int n_we = new_tile ? nxt.we : cur.we;
+        // (staging ahead does not run on a tile's last chunk, so pre is final here)
+        const int n_pre = new_tile ? pre : cur_pre;
         uint64_t nxt_peek = 0;
         bool nxt_follow = false;
         if (kFused && nt < p.num_tiles) {
           const int ng = chunk_at(ngi, n_ws, n_we);
-          nxt_follow = n_kind != kLocal && !(n_kind == kDirect && ng >= n_ws && ng < n_we);
+          nxt_follow = n_kind != kLocal &&
+                       !(n_kind == kDirect && ng >= n_ws && ng < n_we && ng - n_ws >= n_pre);
           if (nxt_follow) nxt_peek = ld_relaxed_gpu(p.flags + n_mb * p.G + ng);
         }
 
