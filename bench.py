@@ -399,7 +399,7 @@ def main():
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_burst, "unit": "TFLOP/s",
                 "frac": achieved / peak_burst, "traffic": load_traffic(w.name, args.layout),
                 "peak_source": f"{peak_src} bf16 burst (fp16 tensor rate is nominally equal)",
-                "kernel": "agmm_gemm_kernel<true> (fused)"}
+                "kernel": ("agmm_gemm_kernel<3> (fused, m-contiguous)" if args.layout == "m_contiguous" else "agmm_gemm_kernel<2> (fused, k-contiguous)")}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
