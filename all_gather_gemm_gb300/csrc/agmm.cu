@@ -69,6 +69,7 @@ struct DevState {
   bool init = false;
   bool supported = false;
   int sms = 0;
+  int pair_clusters = 0;  // CTA pairs of the pair kernels that fit on the GPU at once
   unsigned long long* err = nullptr;  // [2] device error word
   uint64_t* flags = nullptr;
   size_t flags_cap = 0;  // words
@@ -192,20 +193,44 @@ int device_init(DevState& ds, int dev) {
   ds.sms = sms;
   // The kernels are built for sm_103a only; a missing image is "unsupported".
   cudaFuncAttributes fa;
-  if (cudaFuncGetAttributes(&fa, agmm_gemm_kernel<kFusedK>) != cudaSuccess || major != 10) {
+  if (cudaFuncGetAttributes(&fa, agmm_gemm_kernel<kFusedK, false>) != cudaSuccess || major != 10) {
     cudaGetLastError();
     ds.init = true;
     ds.supported = false;
     return AG_ERR_UNSUPPORTED;
   }
-  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kGemmK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes));
-  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kGemmM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes));
-  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kFusedK>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
-  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kFusedM>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
+  constexpr int kSmem1 = Pipe<false>::kSmemBytes, kSmem2 = Pipe<true>::kSmemBytes;
+  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kGemmK, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem1));
+  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kGemmM, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem1));
+  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kFusedK, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem1));
+  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kFusedM, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem1));
+  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kGemmK, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem2));
+  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kGemmM, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem2));
+  {
+    // A cluster's two CTAs need two free SMs of one GPC; with 1 CTA per SM not
+    // every SM pairs up.  A persistent grid larger than what fits at once
+    // would leave the extra clusters for a second wave.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(sms & ~1));
+    cfg.blockDim = dim3((unsigned)mode_threads(kGemmK));
+    cfg.dynamicSmemBytes = kSmem2;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    AG_CK(cudaOccupancyMaxActiveClusters(&clusters, agmm_gemm_kernel<kGemmK, true>, &cfg));
+    ds.pair_clusters = clusters;
+  }
   AG_CK(cudaMalloc(&ds.err, 2 * sizeof(unsigned long long)));
   AG_CK(cudaMemset(ds.err, 0, 2 * sizeof(unsigned long long)));
   ds.init = true;
@@ -239,11 +264,30 @@ int grow_workspace(DevState& ds, const Shape& s, bool need_flags, bool need_stag
   return AG_OK;
 }
 
-template <typename Kernel>
-int launch(Kernel k, int grid, int threads, cudaStream_t stream, const GemmParams& p,
-           const char* what) {
-  k<<<grid, threads, kSmemBytes, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+// pair: clusters of two CTAs (grid even), the kernel's CTA-pair variant.
+template <int kMode, bool kPair>
+int launch(int grid, cudaStream_t stream, const GemmParams& p, const char* what) {
+  auto k = agmm_gemm_kernel<kMode, kPair>;
+  cudaError_t e;
+  if constexpr (kPair) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)mode_threads(kMode));
+    cfg.dynamicSmemBytes = Pipe<true>::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, k, p);
+    if (e == cudaSuccess) e = cudaGetLastError();
+  } else {
+    k<<<grid, mode_threads(kMode), Pipe<false>::kSmemBytes, stream>>>(p);
+    e = cudaGetLastError();
+  }
   return e == cudaSuccess ? AG_OK : cuda_fail(e, what);
 }
 
@@ -422,23 +466,31 @@ int run(bool fused, const void** a_shards, int D, int m_per_shard, int K, const 
   p.num_mb = s.num_mb;
   p.num_nb = s.num_nb;
   p.num_kb = s.num_kb;
-  p.num_tiles = s.num_mb * s.num_nb;
+  // The barrier GEMM runs on CTA pairs (256 x 256 tiles); the fused kernel on
+  // single CTAs.
+  const bool pair = !fused && cap >= 2 && ds.pair_clusters >= 1;
+  Shape sched = s;
+  sched.num_mb = pair ? (s.num_mb + 1) / 2 : s.num_mb;
+  const int units = pair ? std::min(cap / 2, ds.pair_clusters) : cap;  // CTAs, or CTA pairs
+  p.pair = pair ? 1 : 0;
+  p.sched_mb = sched.num_mb;
+  p.num_tiles = (sched.num_mb * s.num_nb) << p.pair;
   p.kpf = s.kpf;
   p.G = s.G;
   p.mb_start = fused ? (int)(((int64_t)o.rank * m_per_shard) / kBM) : 0;
-  p.ng = schedule_group(s, cap);
+  p.ng = schedule_group(sched, units);
   p.w0 = std::min(p.ng, s.num_nb);
   p.fp16 = o.dtype == AG_DTYPE_FP16 ? 1 : 0;
   p.inject_skip_flag = fused ? o.inject_skip_flag : -1;
 
-  const int grid = std::max(1, std::min(cap, p.num_tiles));
-  if (fused && layout_m)
-    return launch(agmm_gemm_kernel<kFusedM>, grid, mode_threads(kFusedM), stream, p, "fused kernel");
-  if (fused)
-    return launch(agmm_gemm_kernel<kFusedK>, grid, mode_threads(kFusedK), stream, p, "fused kernel");
+  const int grid = std::max(1, std::min(units, sched.num_mb * s.num_nb)) << p.pair;
+  if (fused && layout_m) return launch<kFusedM, false>(grid, stream, p, "fused kernel");
+  if (fused) return launch<kFusedK, false>(grid, stream, p, "fused kernel");
   if (layout_m)
-    return launch(agmm_gemm_kernel<kGemmM>, grid, mode_threads(kGemmM), stream, p, "gemm kernel");
-  return launch(agmm_gemm_kernel<kGemmK>, grid, mode_threads(kGemmK), stream, p, "gemm kernel");
+    return pair ? launch<kGemmM, true>(grid, stream, p, "gemm kernel")
+                : launch<kGemmM, false>(grid, stream, p, "gemm kernel");
+  return pair ? launch<kGemmK, true>(grid, stream, p, "gemm kernel")
+              : launch<kGemmK, false>(grid, stream, p, "gemm kernel");
 }
 
 }  // namespace
@@ -474,14 +526,15 @@ int noalloc_setup(NoAllocState& ns, int dev) {
   AG_CK(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev));
   AG_CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
   cudaFuncAttributes fa;
-  if (cudaFuncGetAttributes(&fa, agmm_gemm_kernel<kFusedK>) != cudaSuccess || major != 10) {
+  if (cudaFuncGetAttributes(&fa, agmm_gemm_kernel<kFusedK, false>) != cudaSuccess || major != 10) {
     cudaGetLastError();
     ns.init = true;
     ns.supported = false;
     return AG_ERR_UNSUPPORTED;
   }
-  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kFusedK>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
+  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kFusedK, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Pipe<false>::kSmemBytes));
   void* ptr = nullptr;
   AG_CK(cudaGetSymbolAddress(&ptr, g_noalloc_scratch));
   if (!ptr || !aligned(ptr, 256)) {
@@ -577,6 +630,8 @@ int run_noalloc(const void** a_shards, int D, int m_per_shard, int K, const void
   p.num_mb = s.num_mb;
   p.num_nb = s.num_nb;
   p.num_kb = s.num_kb;
+  p.pair = 0;
+  p.sched_mb = s.num_mb;
   p.num_tiles = s.num_mb * s.num_nb;
   p.kpf = s.kpf;
   p.G = s.G;
@@ -587,8 +642,7 @@ int run_noalloc(const void** a_shards, int D, int m_per_shard, int K, const void
   p.inject_skip_flag = o.inject_skip_flag;
   const int cap = o.num_sms ? std::min(o.num_sms, ns.sms) : ns.sms;
   const int grid = std::max(1, std::min(cap, p.num_tiles));
-  return launch(agmm_gemm_kernel<kFusedK>, grid, mode_threads(kFusedK), stream, p,
-                "fused kernel (no-alloc)");
+  return launch<kFusedK, false>(grid, stream, p, "fused kernel (no-alloc)");
 }
 
 }  // namespace

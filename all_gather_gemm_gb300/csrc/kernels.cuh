@@ -60,10 +60,7 @@ constexpr int kBM = 128;  // rows of an output tile (TMEM lanes)
 constexpr int kBN = 256;  // columns of an output tile (TMEM columns per accumulator)
 constexpr int kBK = 64;   // K per stage: 64 x 16 bit = one 128-byte swizzle row
 constexpr int kUmmaK = 16;
-constexpr int kStages = 4;
 constexpr int kAStageBytes = kBM * kBK * 2;  // 16 KB
-constexpr int kBStageBytes = kBN * kBK * 2;  // 32 KB
-constexpr int kStageBytes = kAStageBytes + kBStageBytes;
 constexpr int kMnChunkBytes = 64 * kBK * 2;  // one 64-wide MN chunk of an MN-major operand (8 KB)
 constexpr int kEpiWarps = 4;
 constexpr int kEpiRows = 32;                           // rows per epilogue warp
@@ -97,12 +94,24 @@ constexpr uint32_t kInfoEnd = 8u;      // chunk record: the issuer is done, the 
 constexpr int kRing = 8;
 constexpr int kRingWords = 8;
 
-// full, empty [kStages]; tmem_full, tmem_empty [2]; drain; rfull, rfree [kRing]
-constexpr int kNumBars = 2 * kStages + 4 + 1 + 2 * kRing;
-constexpr int kSmemData = kStages * kStageBytes + kEpiWarps * kEpiBufs * kEpiBufBytes;
-constexpr int kSmemBytes =
-    1024 + kSmemData + 8 * kNumBars + 4 * kStages + 4 * kRing * kRingWords + 16 + 64;
-static_assert(kSmemBytes <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
+// Pipeline shape.  One CTA per output tile (kPair = false): 4 stages of A
+// (128 x 64) + B (64 x 256).  A CTA pair per 256 x 256 tile (kPair = true):
+// each CTA stages its own 128 rows of A and half of B's 256 columns, so a
+// stage is 32 KB and 6 of them fit, half again as much latency cover.
+template <bool kPair>
+struct Pipe {
+  static constexpr int kStages = kPair ? 6 : 4;
+  static constexpr int kBCols = kPair ? kBN / 2 : kBN;  // B columns staged by this CTA
+  static constexpr int kBStageBytes = kBCols * kBK * 2;
+  static constexpr int kStageBytes = kAStageBytes + kBStageBytes;
+  static constexpr int kData = kStages * kStageBytes + kEpiWarps * kEpiBufs * kEpiBufBytes;
+  // full, empty [kStages]; tmem_full, tmem_empty [2]; drain; rfull, rfree
+  // [kRing]; pair: pfull [kStages] (the peer's stage landed)
+  static constexpr int kBars = 2 * kStages + 4 + 1 + 2 * kRing + (kPair ? kStages : 0);
+  static constexpr int kSmemBytes =
+      1024 + kData + 8 * kBars + 4 * kStages + 4 * kRing * kRingWords + 16 + 64;
+  static_assert(kSmemBytes <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
+};
 
 // Error code written to the device error word (matches ag_status).
 constexpr uint32_t kErrTimeout = 4;
@@ -136,6 +145,8 @@ struct GemmParams {
   int64_t pipe_timeout_ns;  // one pipeline (mbarrier) wait
   int M, N, K, D, mps, rank;
   int num_mb, num_nb, num_kb, num_tiles;
+  int pair;                 // 1: CTA pairs, tile slot t = 2 * pair tile + CTA rank
+  int sched_mb;             // rows of the schedule: num_mb, or pairs of row blocks
   int kpf, G;               // k-blocks per flag, flags per row block
   int mb_start;             // first row block of the schedule (ring order)
   int ng;                   // column blocks per schedule pass
@@ -190,15 +201,22 @@ __device__ __forceinline__ void trace_rec(uint64_t* tr, int64_t words, uint32_t 
 // the group's column blocks of one row block consecutively, so concurrently
 // running CTAs share A rows in L2.
 __device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& mb, int& nb) {
-  const int per_pass = p.num_mb * p.ng;
-  const int gq = t / per_pass;
+  // With CTA pairs a schedule row is a pair of row blocks and slot t belongs
+  // to CTA rank t & 1 of the pair that takes pair tile t >> 1 (the grid is
+  // even, so a CTA's slots all have its rank).  Row block num_mb (the second
+  // half of a last, odd pair) lies past M: its loads read zeros, its stores
+  // are skipped.
+  const int u = t >> p.pair;
+  const int per_pass = p.sched_mb * p.ng;
+  const int gq = u / per_pass;
   const int g0 = gq * p.ng;
   const int width = min(p.ng, p.num_nb - g0);
-  const int r = t - gq * per_pass;
+  const int r = u - gq * per_pass;
   const int pos = r / width;
   nb = g0 + (r - pos * width);
-  mb = p.mb_start + pos;
-  if (mb >= p.num_mb) mb -= p.num_mb;
+  int ms = p.mb_start + pos;
+  if (ms >= p.sched_mb) ms -= p.sched_mb;
+  mb = p.pair ? 2 * ms + (t & 1) : ms;
 }
 
 __device__ __forceinline__ int my_tile_count(const GemmParams& p) {
@@ -251,12 +269,13 @@ __device__ __forceinline__ int owner_nb(const GemmParams& p, int g) {
 
 // Schedule index of tile (mb, nb) (inverse of tile_coords).
 __device__ __forceinline__ int tile_index(const GemmParams& p, int mb, int nb) {
-  int pos = mb - p.mb_start;
-  if (pos < 0) pos += p.num_mb;
+  int pos = (mb >> p.pair) - p.mb_start;
+  if (pos < 0) pos += p.sched_mb;
   const int gq = nb / p.ng;
   const int g0 = gq * p.ng;
   const int width = min(p.ng, p.num_nb - g0);
-  return gq * p.num_mb * p.ng + pos * width + (nb - g0);
+  const int u = gq * p.sched_mb * p.ng + pos * width + (nb - g0);
+  return p.pair ? 2 * u + (mb & 1) : u;
 }
 
 __device__ __forceinline__ int chunk_boxes(const GemmParams& p, int g) {
@@ -276,8 +295,11 @@ struct TileCtx {
 template <bool kFused>
 __device__ __forceinline__ void tile_ctx(const GemmParams& p, int t, TileCtx& c) {
   tile_coords(p, t, c.mb, c.nb);
-  c.ws = chunk_start(p, c.nb);
-  c.we = chunk_end(p, c.nb);
+  // Fused: the owned window first (chunk_at).  The barrier GEMM has nothing
+  // to own and runs k in ascending order, which keeps the tiles of a row
+  // block reading the same A k-block at about the same time.
+  c.ws = kFused ? chunk_start(p, c.nb) : 0;
+  c.we = kFused ? chunk_end(p, c.nb) : 0;
   c.kind = kFused ? block_kind(p, c.mb) : kDirect;
   const int lo = c.mb * kBM, hi = min(lo + kBM, p.M);
   c.r0 = lo / p.mps;
@@ -286,12 +308,17 @@ __device__ __forceinline__ void tile_ctx(const GemmParams& p, int t, TileCtx& c)
 
 // Bounded mbarrier wait.  Returns false (after flagging the CTA abort word and
 // recording an error) when the phase does not complete in time.
+// kCluster: acquire at cluster scope (the barrier takes arrivals from the peer CTA).
+template <bool kCluster = false>
 __device__ __forceinline__ bool wait_bar(const GemmParams& p, uint64_t* bar, uint32_t parity,
                                          volatile int* abort_flag, uint32_t site) {
-  if (mbar_try_wait(bar, parity)) return true;
+  auto test = [&]() {
+    return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+  };
+  if (test()) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (test()) return true;
     if ((it & 63u) == 0) {
       if (*abort_flag) return false;
       if (globaltimer_ns() - t0 > (uint64_t)p.pipe_timeout_ns || it > (1u << 28)) {
@@ -503,24 +530,32 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, int fp16) {
 
 // ------------------------------------------------------------------ the kernel
 
-template <int kMode>
+// kPair: launched in clusters of two CTAs; the even CTA (rank 0, the leader)
+// issues tcgen05.mma.cta_group::2 for the pair's 256 x 256 tile, the odd CTA
+// (the peer) relays "my stage has landed" to it, and both run their own TMA
+// issuer and epilogue for their own 128 rows.
+template <int kMode, bool kPair>
 __global__ void __launch_bounds__(mode_threads(kMode), 1)
     agmm_gemm_kernel(const __grid_constant__ GemmParams p) {
+  using P = Pipe<kPair>;
+  constexpr int kStages = P::kStages;
+  constexpr int kStageBytes = P::kStageBytes;
   constexpr bool kFused = mode_fused(kMode);
   constexpr bool kLayoutM = mode_layout_m(kMode);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* epi_smem = smem + kStages * kStageBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kSmemData);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P::kData);
   uint64_t* full = bars;                     // [kStages] TMA landed
-  uint64_t* empty = bars + kStages;          // [kStages] every reader of the stage is done
+  uint64_t* empty = bars + kStages;          // [kStages] the MMAs reading the stage are done
   uint64_t* tmem_full = bars + 2 * kStages;  // [2] accumulator ready
   uint64_t* tmem_empty = tmem_full + 2;      // [2] accumulator drained
   uint64_t* drain = tmem_empty + 2;          // [1] final MMA drain
   uint64_t* rfull = drain + 1;               // [kRing] fused: chunk record written
   uint64_t* rfree = rfull + kRing;           // [kRing] fused: every copier is done with it
-  uint32_t* info = reinterpret_cast<uint32_t*>(rfree + kRing);  // [kStages] stage bits
+  uint64_t* pfull = rfree + kRing;           // [kStages] pair, leader: the peer's stage landed
+  uint32_t* info = reinterpret_cast<uint32_t*>(pfull + (kPair ? kStages : 0));  // [kStages]
   uint32_t* ring = info + kStages;                // [kRing][kRingWords] chunk records
   volatile uint32_t* iseq = ring + kRing * kRingWords;  // issuer progress (chunks), a liveness signal
   uint32_t* tmem_slot = ring + kRing * kRingWords + 1;
@@ -529,11 +564,13 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int my_tiles = my_tile_count(p);
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);  // the MMA commit
+      mbar_init(&empty[s], 1);  // the MMA commit (pair: multicast to both CTAs)
+      if (kPair) mbar_init(&pfull[s], 1);
     }
     for (int r = 0; r < kRing; ++r) {
       mbar_init(&rfull[r], 1);
@@ -541,7 +578,8 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tmem_full[b], 1);
-      mbar_init(&tmem_empty[b], 32 * kEpiWarps);
+      // one arrive per epilogue warp (pair: the leader's barrier takes both CTAs')
+      mbar_init(&tmem_empty[b], kEpiWarps * (kPair ? 2 : 1));
     }
     mbar_init(drain, 1);
     *iseq = 0;
@@ -553,11 +591,13 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
     if (kLayoutM) prefetch_tensormap(&p.tm_a_mk);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, kTmemCols);
-    tmem_relinquish_alloc_permit();
+    tmem_alloc<kPair>(tmem_slot, kTmemCols);
+    tmem_relinquish_alloc_permit<kPair>();
   }
   tcgen05_fence_before_sync();
   __syncthreads();
+  // Pair: both CTAs' barriers are initialised before either signals the other's.
+  if (kPair) cluster_sync();
   tcgen05_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -716,10 +756,11 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
           } else {
             tma_load_2d(a_dst, &p.tm_a, &full[stage], kb * kBK, mb * kBM);
           }
+          // this CTA's columns of the tile's B (pair: the rank's half)
 #pragma unroll
-          for (int q = 0; q < kBN / 64; ++q)
-            tma_load_2d(b_dst + q * kMnChunkBytes, &p.tm_b, &full[stage], nb * kBN + q * 64,
-                        kb * kBK);
+          for (int q = 0; q < P::kBCols / 64; ++q)
+            tma_load_2d(b_dst + q * kMnChunkBytes, &p.tm_b, &full[stage],
+                        nb * kBN + (int)rank * P::kBCols + q * 64, kb * kBK);
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           ++seq;
@@ -779,26 +820,46 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
       }
     }
     __syncwarp();
+  } else if (warp == 1 && kPair && rank != 0) {
+    // ---------------------------------------------------------- pair peer: relay
+    // The leader's MMA reads this CTA's stage too; tell it when the stage has
+    // landed, in fill order.  (This CTA cannot refill a stage before the
+    // leader's commit frees it, so no phase is skipped.)
+    if (lane == 0) {
+      const int total = my_tiles * p.num_kb;
+      for (int i = 0; i < total; ++i) {
+        const int s = i % kStages;
+        if (!wait_bar(p, &full[s], (uint32_t)(i / kStages) & 1u, abort_flag, kSiteFull)) break;
+        // Relaxed: this thread has already observed the stage complete (its
+        // bytes are in this CTA's shared memory); a release here would first
+        // wait for this CTA's later loads still in flight, and that cost the
+        // pair half its throughput.
+        mbar_arrive_remote_relaxed(mapa_shared(smem_u32(&pfull[s]), 0));
+      }
+    }
+    __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t ab_bf16 = p.fp16 ? 0u : 1u;
-      const uint32_t idesc_k = idesc_f16_f32(ab_bf16, 0, 1, kBM, kBN);
-      const uint32_t idesc_mn = idesc_f16_f32(ab_bf16, 1, 1, kBM, kBN);
+      constexpr uint32_t kM = kPair ? 2 * kBM : kBM;
+      const uint32_t idesc_k = idesc_f16_f32(ab_bf16, 0, 1, kM, kBN);
+      const uint32_t idesc_mn = idesc_f16_f32(ab_bf16, 1, 1, kM, kBN);
       bool aborted = false;
       int stage = 0;
       uint32_t phase = 0;
       for (int j = 0; j < my_tiles && !aborted; ++j) {
         const int buf = j & 1;
         const uint32_t use = (uint32_t)(j >> 1);
-        if (!wait_bar(p, &tmem_empty[buf], (use & 1u) ^ 1u, abort_flag, kSiteTmemEmpty)) {
+        if (!wait_bar<kPair>(p, &tmem_empty[buf], (use & 1u) ^ 1u, abort_flag, kSiteTmemEmpty)) {
           aborted = true;
           break;
         }
         tcgen05_fence_after_sync();
         const uint32_t d_tmem = tmem_base + (uint32_t)(buf * kBN);
         for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (!wait_bar(p, &full[stage], phase, abort_flag, kSiteFull)) {
+          if (!wait_bar(p, &full[stage], phase, abort_flag, kSiteFull) ||
+              (kPair && !wait_bar<true>(p, &pfull[stage], phase, abort_flag, kSiteFull))) {
             aborted = true;
             break;
           }
@@ -815,19 +876,31 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
                 a_mn ? smem_desc_sw128(a_addr + ks * 2048, kMnChunkBytes, 1024)
                      : smem_desc_sw128(a_addr + ks * 32, 16, 1024);
             const uint64_t b_desc = smem_desc_sw128(b_addr + ks * 2048, kMnChunkBytes, 1024);
-            umma_f16(d_tmem, a_desc, b_desc, idesc, (kb | ks) != 0 ? 1u : 0u);
+            if constexpr (kPair)
+              umma_f16_pair(d_tmem, a_desc, b_desc, idesc, (kb | ks) != 0 ? 1u : 0u);
+            else
+              umma_f16(d_tmem, a_desc, b_desc, idesc, (kb | ks) != 0 ? 1u : 0u);
           }
-          umma_commit(&empty[stage]);
+          if constexpr (kPair)
+            umma_commit_pair_mc(&empty[stage], 3);  // frees the stage in both CTAs
+          else
+            umma_commit(&empty[stage]);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (aborted) break;
-        umma_commit(&tmem_full[buf]);
+        if constexpr (kPair)
+          umma_commit_pair_mc(&tmem_full[buf], 3);
+        else
+          umma_commit(&tmem_full[buf]);
       }
       // All MMAs issued by this thread complete before TMEM is released.
-      umma_commit(drain);
+      if constexpr (kPair)
+        umma_commit_pair(drain);
+      else
+        umma_commit(drain);
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < 1000000000ull) {
       }
@@ -859,8 +932,16 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
         tmem_ld_32x32b_x32(t_row + c * kEpiCols + 32, r1);
         tmem_ld_wait();
         if (c == kBN / kEpiCols - 1) {
+          // This warp has read its lanes of the accumulator (pair: the peer's
+          // warps arrive on the leader's barrier).
           tcgen05_fence_before_sync();
-          mbar_arrive(&tmem_empty[buf]);
+          __syncwarp();
+          if (lane == 0) {
+            if (kPair && rank != 0)
+              mbar_arrive_remote(mapa_shared(smem_u32(&tmem_empty[buf]), 0));
+            else
+              mbar_arrive(&tmem_empty[buf]);
+          }
         }
         const int n0 = n_tile + c * kEpiCols;
         uint32_t packed[32];
@@ -978,10 +1059,13 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
 
   tcgen05_fence_before_sync();
   __syncthreads();
+  // Pair: neither CTA leaves (or frees TMEM) while the other may still signal
+  // its barriers or the leader's MMAs may still write its TMEM.
+  if (kPair) cluster_sync();
   tcgen05_fence_after_sync();
   if (warp == 1) {
     __syncwarp();
-    tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc<kPair>(tmem_base, kTmemCols);
   }
 }
 
