@@ -166,8 +166,10 @@ int schedule_group(const Shape& s, int sms) {
 // Fused-path metadata: ready flags [num_mb * G], then the per-tile started
 // words [num_mb * num_nb]; both 8 bytes each.
 size_t flags_region(const Shape& s) { return round_kib((size_t)s.num_mb * s.G * 8); }
+// Flags, then one "started" word per tile slot (CTA pairs: an odd row-block
+// count adds a slot per column block).
 size_t flags_bytes(const Shape& s) {
-  return flags_region(s) + round_kib((size_t)s.num_mb * s.num_nb * 8);
+  return flags_region(s) + round_kib((size_t)(s.num_mb + 1) * s.num_nb * 8);
 }
 
 // Device pointers must be device (or managed) memory of the current device:
@@ -211,6 +213,8 @@ int device_init(DevState& ds, int dev) {
   AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kGemmK, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem2));
   AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kGemmM, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem2));
+  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kFusedK, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem2));
   {
     // A cluster's two CTAs need two free SMs of one GPC; with 1 CTA per SM not
@@ -466,9 +470,11 @@ int run(bool fused, const void** a_shards, int D, int m_per_shard, int K, const 
   p.num_mb = s.num_mb;
   p.num_nb = s.num_nb;
   p.num_kb = s.num_kb;
-  // The barrier GEMM runs on CTA pairs (256 x 256 tiles); the fused kernel on
-  // single CTAs.
-  const bool pair = !fused && cap >= 2 && ds.pair_clusters >= 1;
+  // CTA pairs (256 x 256 tiles) whenever two SMs are allowed, except the
+  // fused m-contiguous kernel: one pair MMA reads both CTAs' A halves with one
+  // major-ness, and there a block's A can be K-major (read from a shard) while
+  // its partner's is MN-major (read from the [K, M] staging).
+  const bool pair = !(fused && layout_m) && cap >= 2 && ds.pair_clusters >= 1;
   Shape sched = s;
   sched.num_mb = pair ? (s.num_mb + 1) / 2 : s.num_mb;
   const int units = pair ? std::min(cap / 2, ds.pair_clusters) : cap;  // CTAs, or CTA pairs
@@ -477,7 +483,8 @@ int run(bool fused, const void** a_shards, int D, int m_per_shard, int K, const 
   p.num_tiles = (sched.num_mb * s.num_nb) << p.pair;
   p.kpf = s.kpf;
   p.G = s.G;
-  p.mb_start = fused ? (int)(((int64_t)o.rank * m_per_shard) / kBM) : 0;
+  // schedule rows start at the local shard (pairs: the pair holding its first block)
+  p.mb_start = fused ? (int)(((int64_t)o.rank * m_per_shard) / kBM) >> p.pair : 0;
   p.ng = schedule_group(sched, units);
   p.w0 = std::min(p.ng, s.num_nb);
   p.fp16 = o.dtype == AG_DTYPE_FP16 ? 1 : 0;
@@ -485,7 +492,9 @@ int run(bool fused, const void** a_shards, int D, int m_per_shard, int K, const 
 
   const int grid = std::max(1, std::min(units, sched.num_mb * s.num_nb)) << p.pair;
   if (fused && layout_m) return launch<kFusedM, false>(grid, stream, p, "fused kernel");
-  if (fused) return launch<kFusedK, false>(grid, stream, p, "fused kernel");
+  if (fused)
+    return pair ? launch<kFusedK, true>(grid, stream, p, "fused kernel")
+                : launch<kFusedK, false>(grid, stream, p, "fused kernel");
   if (layout_m)
     return pair ? launch<kGemmM, true>(grid, stream, p, "gemm kernel")
                 : launch<kGemmM, false>(grid, stream, p, "gemm kernel");

@@ -225,7 +225,8 @@ __device__ __forceinline__ int my_tile_count(const GemmParams& p) {
 }
 
 // How a row block's A rows can be fetched.
-enum BlockKind : int { kLocal = 0, kDirect = 1, kRegFetch = 2 };
+// kEmpty: the second row block of a last, odd CTA pair (rows past M).
+enum BlockKind : int { kLocal = 0, kDirect = 1, kRegFetch = 2, kEmpty = 3 };
 
 // Local: every row lies in the local shard.  Direct: one shard holds every
 // row, or the block straddles shards at multiples of 8 rows (8-row TMA boxes).
@@ -300,6 +301,12 @@ __device__ __forceinline__ void tile_ctx(const GemmParams& p, int t, TileCtx& c)
   // block reading the same A k-block at about the same time.
   c.ws = kFused ? chunk_start(p, c.nb) : 0;
   c.we = kFused ? chunk_end(p, c.nb) : 0;
+  if (c.mb >= p.num_mb) {
+    c.kind = kEmpty;
+    c.r0 = 0;
+    c.one_shard = true;
+    return;
+  }
   c.kind = kFused ? block_kind(p, c.mb) : kDirect;
   const int lo = c.mb * kBM, hi = min(lo + kBM, p.M);
   c.r0 = lo / p.mps;
@@ -492,7 +499,7 @@ __device__ __forceinline__ void regfetch_loop(const GemmParams& p, int lane, boo
   for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
     int mb, nb;
     tile_coords(p, t, mb, nb);
-    if (mb == last_mb || block_kind(p, mb) != kRegFetch) continue;
+    if (mb == last_mb || mb >= p.num_mb || block_kind(p, mb) != kRegFetch) continue;
     last_mb = mb;
     for (int g = 0; g < p.G; ++g) {
       const int idx = mb * p.G + g;
@@ -633,14 +640,41 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
       if (t < p.num_tiles) {
         tile_ctx<kFused>(p, t, cur);
         const int g0 = chunk_at(0, cur.ws, cur.we);
-        if (cur.kind != kLocal && !cur.owns(g0))
+        if (cur.kind != kLocal && cur.kind != kEmpty && !cur.owns(g0))
           cur_peek = ld_relaxed_gpu(p.flags + cur.mb * p.G + g0);
         if (t + (int)gridDim.x < p.num_tiles) tile_ctx<kFused>(p, t + gridDim.x, nxt);
       }
       const int last_nbox = chunk_boxes(p, p.G - 1);
       while (t < p.num_tiles && !aborted) {
         const uint64_t t_chunk = p.trace ? globaltimer_ns() : 0;
-        if (kFused && gi == 0) st_relaxed_gpu(p.started + t, p.epoch);
+        if (kFused && gi == 0) {
+          // Before any load of the tile: hand the rest of its owned window to
+          // the copiers, then mark the tile started.  A follower waits
+          // (instead of taking a chunk over) only on a started owner, and
+          // handed chunks are published whatever this CTA's pipeline does --
+          // with CTA pairs that pipeline also waits on the partner CTA.
+          if (cur.kind == kLocal || cur.kind == kDirect) {
+            const uint32_t wbits = cur.kind == kDirect ? (kInfoStage | kInfoPublish) : kInfoStage;
+            for (int wg = cur.ws + cur_pre; wg < cur.we; ++wg) {
+              if (!wait_bar(p, &rfree[rslot], rphase ^ 1u, abort_flag, kSiteRing)) {
+                aborted = true;
+                break;
+              }
+              hand_chunk(ring + rslot * kRingWords, &rfull[rslot], wbits, cur.mb, wg,
+                         chunk_boxes(p, wg), cur.mb * p.G + wg, seq, p);
+              if (p.trace) {
+                const uint64_t now = globaltimer_ns();
+                trace_rec(p.trace, p.trace_words, kTraceClaim, cur.mb, wg, now, now);
+              }
+              if (++rslot == kRing) {
+                rslot = 0;
+                rphase ^= 1u;
+              }
+            }
+            if (aborted) break;
+          }
+          st_relaxed_gpu(p.started + t, p.epoch);
+        }
         const int g = chunk_at(gi, cur.ws, cur.we);
         const int mb = cur.mb, nb = cur.nb;
         const int flag_idx = mb * p.G + g;
@@ -652,14 +686,14 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
           // A window chunk staged ahead is read like a follower's: from the
           // staging its copiers wrote a tile ago (still in L2), not again from
           // the shard.
+          // (Owned chunks were handed to the copiers at the tile start.)
           const bool staged_ahead = cur.owns(g) && g - cur.ws < cur_pre;
           if (kind == kLocal) {
             direct = true;
-            // the owner writes the local rows of a_gathered
-            if (cur.owns(g) && !staged_ahead) bits = kInfoStage;
+          } else if (kind == kEmpty) {
+            // rows past M: a_gathered's map reads zeros there
           } else if (kind == kDirect && cur.owns(g) && !staged_ahead) {
             direct = true;
-            bits = kInfoStage | kInfoPublish;
           } else {
             const uint64_t target = p.fbase + (uint64_t)nbox;
             if (cur_peek >= target) {
@@ -681,7 +715,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
           }
         }
         if (kFused && (bits & kInfoStage)) {
-          // Hand the chunk to the copiers.
+          // A chunk taken over: hand it to the copiers.
           if (!wait_bar(p, &rfree[rslot], rphase ^ 1u, abort_flag, kSiteRing)) {
             aborted = true;
             break;
@@ -715,7 +749,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
         bool nxt_follow = false;
         if (kFused && nt < p.num_tiles) {
           const int ng = chunk_at(ngi, n_ws, n_we);
-          nxt_follow = n_kind != kLocal &&
+          nxt_follow = n_kind != kLocal && n_kind != kEmpty &&
                        !(n_kind == kDirect && ng >= n_ws && ng < n_we && ng - n_ws >= n_pre);
           if (nxt_follow) nxt_peek = ld_relaxed_gpu(p.flags + n_mb * p.G + ng);
         }
@@ -774,7 +808,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
                     (uint32_t)g | (direct ? 1u << 16 : 0u) | ((bits & kInfoStage) ? 2u << 16 : 0u),
                     t_chunk, globaltimer_ns());
         if (kFused && !aborted && !new_tile && t + (int)gridDim.x < p.num_tiles &&
-            nxt.kind != kRegFetch && pre < nxt.we - nxt.ws &&
+            (nxt.kind == kLocal || nxt.kind == kDirect) && pre < nxt.we - nxt.ws &&
             mbar_test_wait(&rfree[rslot], rphase ^ 1u)) {
           // Stage ahead: one chunk of the next tile's window.
           const int pg = nxt.ws + pre;

@@ -56,15 +56,15 @@ def test_status_strings(lib):
 
 def test_workspace_size(lib):
     # flags: 8 row blocks x (128 k-blocks / 8 per flag) x 8 bytes = 1 KiB;
-    # started words: 8 x 14 tiles x 8 bytes = 896 B -> 1 KiB
+    # started words: (8 + 1) x 14 tile slots x 8 bytes = 1008 B -> 1 KiB
     assert agmm.workspace_size(8, 128, 8192, 3584) == 1024 + 1024
-    # 128 row blocks x 16 flags x 8 bytes = 16 KiB, 128 x 14 tiles x 8 B = 14 KiB,
-    # plus [K, M] staging for m-contiguous
-    assert agmm.workspace_size(8, 2048, 8192, 3584) == 16384 + 14336
+    # 128 row blocks x 16 flags x 8 bytes = 16 KiB, (128 + 1) x 14 tile slots x 8 B
+    # = 14448 B -> 15 KiB, plus [K, M] staging for m-contiguous
+    assert agmm.workspace_size(8, 2048, 8192, 3584) == 16384 + 15360
     assert agmm.workspace_size(8, 2048, 8192, 3584, "m_contiguous") == (
-        16384 + 14336 + 16384 * 8192 * 2)
-    assert agmm.workspace_size(8, 2048, 8192, 3584, k_per_flag=1) == 128 * 128 * 8 + 14336
-    assert agmm.workspace_size(8, 2048, 8192, 3584, k_per_flag=16) == 8192 + 14336
+        16384 + 15360 + 16384 * 8192 * 2)
+    assert agmm.workspace_size(8, 2048, 8192, 3584, k_per_flag=1) == 128 * 128 * 8 + 15360
+    assert agmm.workspace_size(8, 2048, 8192, 3584, k_per_flag=16) == 8192 + 15360
     assert agmm.workspace_size(1, 1, 8, 8) == 2048  # one flag and one tile, 1 KiB each
     # automatic granularity: K=384 has 6 k-blocks and N=384 two column blocks,
     # so 3 k-blocks per flag -> 2 flags per row block (3 row blocks): 48 B -> 1 KiB
