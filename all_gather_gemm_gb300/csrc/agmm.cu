@@ -25,15 +25,24 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int64_t kDefaultTimeoutNs = 2000000000LL;
-constexpr int kMaxAutoKPerFlag = 8;
+// Automatic flag granularity (k-blocks per flag), measured over the cube sweep
+// and the Iris shapes.  When every tile fits in one wave of the grid, the
+// followers wait on owners that all start together: K-blocks per column
+// block, clamped to [4, 8] (one-wave cubes: 4; M=1024 with 128 K-blocks: 8).
+// Otherwise 8 for the k-contiguous layout and 16 for the m-contiguous one
+// (fewer flags: fewer waits, fences and copier hand-offs per tile; the
+// owners' longer first chunks are covered by staging ahead).
+constexpr int kAutoKpfOneWave = 4, kAutoKpfOneWaveMax = 8, kAutoKpfK = 8, kAutoKpfM = 16;
 
-// Default flag granularity: at most 8 k-blocks per flag, but at least as many
-// flags per row block as there are column blocks, so that every column
-// block's tiles own a chunk to start on and none waits out another tile's
-// whole k-loop (with fewer flags than column blocks, several tiles start on
-// the same chunk and all but its owner wait for it).
-int auto_k_per_flag(int num_kb, int num_nb) {
-  return std::max(1, std::min(kMaxAutoKPerFlag, num_kb / std::max(1, num_nb)));
+// Granularity the workspace is sized for when k_per_flag is automatic: the
+// finest automatic choice, so the flags fit whichever one a launch makes.
+int sizing_k_per_flag(int num_kb) { return std::max(1, std::min(kAutoKpfOneWave, num_kb)); }
+
+int auto_k_per_flag(int num_kb, int num_nb, bool one_wave, bool layout_m) {
+  const int k = one_wave ? std::min(kAutoKpfOneWaveMax,
+                                    std::max(kAutoKpfOneWave, num_kb / std::max(1, num_nb)))
+                         : (layout_m ? kAutoKpfM : kAutoKpfK);
+  return std::max(1, std::min(k, num_kb));
 }
 
 thread_local char t_cuda_msg[320] = "no CUDA error recorded on this thread";
@@ -142,7 +151,7 @@ int validate(const void** a_shards, int D, int m_per_shard, int K, const void* b
   sh->num_mb = (int)((M + kBM - 1) / kBM);
   sh->num_nb = (N + kBN - 1) / kBN;
   sh->num_kb = (K + kBK - 1) / kBK;
-  sh->kpf = o.k_per_flag ? o.k_per_flag : auto_k_per_flag(sh->num_kb, sh->num_nb);
+  sh->kpf = o.k_per_flag ? o.k_per_flag : sizing_k_per_flag(sh->num_kb);
   sh->G = (sh->num_kb + sh->kpf - 1) / sh->kpf;
   if ((int64_t)sh->num_mb * sh->num_nb > INT32_MAX || (int64_t)sh->num_mb * sh->G > 0xFFFFFF)
     return AG_ERR_UNSUPPORTED;
@@ -481,8 +490,11 @@ int run(bool fused, const void** a_shards, int D, int m_per_shard, int K, const 
   p.pair = pair ? 1 : 0;
   p.sched_mb = sched.num_mb;
   p.num_tiles = (sched.num_mb * s.num_nb) << p.pair;
-  p.kpf = s.kpf;
-  p.G = s.G;
+  // (the workspace is sized for s.G, which is >= the automatic choice's G)
+  p.kpf = o.k_per_flag ? s.kpf
+                       : auto_k_per_flag(s.num_kb, s.num_nb,
+                                         (int64_t)sched.num_mb * s.num_nb <= units, layout_m);
+  p.G = (s.num_kb + p.kpf - 1) / p.kpf;
   // schedule rows start at the local shard (pairs: the pair holding its first block)
   p.mb_start = fused ? (int)(((int64_t)o.rank * m_per_shard) / kBM) >> p.pair : 0;
   p.ng = schedule_group(sched, units);
@@ -642,14 +654,14 @@ int run_noalloc(const void** a_shards, int D, int m_per_shard, int K, const void
   p.pair = 0;
   p.sched_mb = s.num_mb;
   p.num_tiles = s.num_mb * s.num_nb;
-  p.kpf = s.kpf;
-  p.G = s.G;
+  const int cap = o.num_sms ? std::min(o.num_sms, ns.sms) : ns.sms;
+  p.kpf = o.k_per_flag ? s.kpf : auto_k_per_flag(s.num_kb, s.num_nb, p.num_tiles <= cap, false);
+  p.G = (s.num_kb + p.kpf - 1) / p.kpf;
   p.mb_start = (int)(((int64_t)o.rank * m_per_shard) / kBM);
-  p.ng = schedule_group(s, o.num_sms ? std::min(o.num_sms, ns.sms) : ns.sms);
+  p.ng = schedule_group(s, cap);
   p.w0 = std::min(p.ng, s.num_nb);
   p.fp16 = o.dtype == AG_DTYPE_FP16 ? 1 : 0;
   p.inject_skip_flag = o.inject_skip_flag;
-  const int cap = o.num_sms ? std::min(o.num_sms, ns.sms) : ns.sms;
   const int grid = std::max(1, std::min(cap, p.num_tiles));
   return launch<kFusedK, false>(grid, stream, p, "fused kernel (no-alloc)");
 }
@@ -710,7 +722,7 @@ size_t ag_workspace_size(int D, int m_per_shard, int K, int N, const ag_options*
   s.num_mb = (int)((M + kBM - 1) / kBM);
   s.num_nb = (N + kBN - 1) / kBN;
   s.num_kb = (K + kBK - 1) / kBK;
-  s.kpf = o.k_per_flag ? o.k_per_flag : auto_k_per_flag(s.num_kb, s.num_nb);
+  s.kpf = o.k_per_flag ? o.k_per_flag : sizing_k_per_flag(s.num_kb);
   s.G = (s.num_kb + s.kpf - 1) / s.kpf;
   return flags_bytes(s) + (o.layout == AG_LAYOUT_M_CONTIGUOUS ? (size_t)K * M * 2 : 0);
 }

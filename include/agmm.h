@@ -108,8 +108,11 @@ typedef struct ag_options {
   int32_t dtype;            /* ag_dtype of a_shards, b, a_gathered, out (default bf16) */
   int32_t layout;           /* ag_layout of the staged A (default k-contiguous) */
   int32_t rank;             /* the local shard, 0 <= rank < D (default 0) */
-  int32_t k_per_flag;       /* 64-column K blocks covered by one ready flag; 0 = automatic:
-                               min(8, max(1, K-blocks / column blocks)) (default) */
+  int32_t k_per_flag;       /* 64-column K blocks covered by one ready flag; 0 = automatic
+                               (default): when every output tile fits in one wave of the
+                               grid, K blocks per 256-column block clamped to [4, 8], else
+                               8 (k-contiguous) or 16 (m-contiguous); at most the number
+                               of K blocks */
   int32_t num_sms;          /* cap on the persistent grid (CTAs); 0 = every SM */
   int32_t inject_skip_flag; /* fault injection: the producer never publishes this flag index
                                (-1 = off); the consumer wait then times out */
@@ -149,6 +152,8 @@ int ag_then_matmul_ex(const void** a_shards, int D, int m_per_shard, int K, cons
 
 /* Bytes a caller workspace must hold for a fused call of this shape and
  * these options (flags, plus the [K, M] staging for the m-contiguous layout).
+ * With the automatic k_per_flag the flags are sized for the finest automatic
+ * granularity (4), which covers whatever a launch picks.
  * The workspace must be 256-byte aligned and zero-filled before its first use
  * with this library; after that the library owns its contents.  Returns 0 on
  * invalid sizes. */
@@ -200,7 +205,7 @@ int ag_num_sms(void);
  * scratch -- 256 bytes plus ag_workspace_size() for the k-contiguous layout --
  * exceeds AG_NOALLOC_SCRATCH_BYTES is rejected with AG_ERR_TOO_LARGE before
  * anything is enqueued.  With the automatic k_per_flag that admits, for
- * example, M = 16384, N = 3584, K = 8192 (about 30 KB of scratch).  All other
+ * example, M = 16384, N = 3584, K = 8192 (about 48 KB of scratch).  All other
  * arguments and errors are as for ag_matmul_ex; device-side timeouts are
  * reported by ag_get_device_error.
  *

@@ -55,19 +55,20 @@ def test_status_strings(lib):
 
 
 def test_workspace_size(lib):
-    # flags: 8 row blocks x (128 k-blocks / 8 per flag) x 8 bytes = 1 KiB;
+    # automatic k_per_flag is sized at its finest, 4 k-blocks per flag:
+    # flags: 8 row blocks x (128 k-blocks / 4 per flag) x 8 bytes = 2 KiB;
     # started words: (8 + 1) x 14 tile slots x 8 bytes = 1008 B -> 1 KiB
-    assert agmm.workspace_size(8, 128, 8192, 3584) == 1024 + 1024
-    # 128 row blocks x 16 flags x 8 bytes = 16 KiB, (128 + 1) x 14 tile slots x 8 B
+    assert agmm.workspace_size(8, 128, 8192, 3584) == 2048 + 1024
+    # 128 row blocks x 32 flags x 8 bytes = 32 KiB, (128 + 1) x 14 tile slots x 8 B
     # = 14448 B -> 15 KiB, plus [K, M] staging for m-contiguous
-    assert agmm.workspace_size(8, 2048, 8192, 3584) == 16384 + 15360
+    assert agmm.workspace_size(8, 2048, 8192, 3584) == 32768 + 15360
     assert agmm.workspace_size(8, 2048, 8192, 3584, "m_contiguous") == (
-        16384 + 15360 + 16384 * 8192 * 2)
+        32768 + 15360 + 16384 * 8192 * 2)
     assert agmm.workspace_size(8, 2048, 8192, 3584, k_per_flag=1) == 128 * 128 * 8 + 15360
     assert agmm.workspace_size(8, 2048, 8192, 3584, k_per_flag=16) == 8192 + 15360
     assert agmm.workspace_size(1, 1, 8, 8) == 2048  # one flag and one tile, 1 KiB each
-    # automatic granularity: K=384 has 6 k-blocks and N=384 two column blocks,
-    # so 3 k-blocks per flag -> 2 flags per row block (3 row blocks): 48 B -> 1 KiB
+    # automatic granularity, sized at 4 k-blocks per flag: K=384 has 6 k-blocks
+    # -> 2 flags per row block (3 row blocks): 48 B -> 1 KiB
     assert agmm.workspace_size(8, 48, 384, 384) == 1024 + 1024
     assert agmm.workspace_size(8, 48, 384, 384, k_per_flag=8) == 1024 + 1024
     assert agmm.workspace_size(0, 1, 8, 8) == 0

@@ -308,7 +308,7 @@ def test_trace_records_overlap_roles():
     x = inp.make_inputs(w)
     shards, b, _ = to_device(x)
     tr = torch.zeros(1 + 4 * 8192, dtype=torch.int64, device="cuda")
-    agmm.ag_matmul(shards, b, rank=0, trace=tr)
+    agmm.ag_matmul(shards, b, rank=0, trace=tr, k_per_flag=4)
     assert agmm.device_error() == (0, 0)
     t = tr.cpu().numpy().view(np.uint64)
     n = int(t[0])
@@ -319,7 +319,7 @@ def test_trace_records_overlap_roles():
     fetch = rec[(rec[:, 2] >> np.uint64(56)) == 1]
     # every (row block, k-group) chunk is staged by its owner (or a follower
     # that took it over) at least once
-    num_mb, G = 2048 // 128, 2048 // 64 // 4  # automatic k_per_flag: 32 k-blocks / 8 column blocks
+    num_mb, G = 2048 // 128, 2048 // 64 // 4  # 32 k-blocks, 4 per flag
     keys = ((fetch[:, 2] >> np.uint64(20)) & np.uint64(0xFFFFF)) * np.uint64(G) + (fetch[:, 2] & np.uint64(0xFFFFF))
     assert set(keys.tolist()) == set(range(num_mb * G))
     assert len(keys) < 2 * num_mb * G
