@@ -34,6 +34,15 @@ constexpr int64_t kDefaultTimeoutNs = 2000000000LL;
 // owners' longer first chunks are covered by staging ahead).
 constexpr int kAutoKpfOneWave = 4, kAutoKpfOneWaveMax = 8, kAutoKpfK = 8, kAutoKpfM = 16;
 
+// log2 of the row count of the boxes that load a row block straddling shards:
+// the largest of 64, 32, 16, 8 rows dividing m_per_shard (3 if none does; such
+// blocks are then copied by the register fetcher instead).
+int straddle_log2(int m_per_shard) {
+  for (int l = 6; l > 3; --l)
+    if (m_per_shard % (1 << l) == 0) return l;
+  return 3;
+}
+
 // Granularity the workspace is sized for when k_per_flag is automatic: the
 // finest automatic choice, so the flags fit whichever one a launch makes.
 int sizing_k_per_flag(int num_kb) { return std::max(1, std::min(kAutoKpfOneWave, num_kb)); }
@@ -445,15 +454,17 @@ int run(bool fused, const void** a_shards, int D, int m_per_shard, int K, const 
       (st = make_map(&p.tm_a_mk, staging, (uint64_t)s.M, (uint64_t)K, 64, kBK)) != AG_OK)
     return st;
   if (fused) {
-    // Row blocks that straddle shards are loaded in 8-row boxes when the shard
+    // Row blocks that straddle shards are loaded in boxes of 2^sh_log2 rows
+    // (the largest of 64, 32, 16, 8 that divides m_per_shard) when the shard
     // boundaries fall on multiples of 8 rows.
     const bool straddle8 = D > 1 && (m_per_shard % kBM) != 0 && (m_per_shard % 8) == 0;
+    p.sh_log2 = straddle_log2(m_per_shard);
     for (int r = 0; r < D; ++r) {
       if ((st = make_map(&p.tm_shard[r], a_shards[r], (uint64_t)K, (uint64_t)m_per_shard, kBK,
                          kBM)) != AG_OK)
         return st;
       if (straddle8 && (st = make_map(&p.tm_shard8[r], a_shards[r], (uint64_t)K,
-                                      (uint64_t)m_per_shard, kBK, 8)) != AG_OK)
+                                      (uint64_t)m_per_shard, kBK, 1u << p.sh_log2)) != AG_OK)
         return st;
     }
   }
@@ -618,12 +629,13 @@ int run_noalloc(const void** a_shards, int D, int m_per_shard, int K, const void
   if ((st = make_map(&p.tm_out, out, (uint64_t)N, (uint64_t)s.M, kEpiCols, kEpiRows)) != AG_OK)
     return st;
   const bool straddle8 = D > 1 && (m_per_shard % kBM) != 0 && (m_per_shard % 8) == 0;
+  p.sh_log2 = straddle_log2(m_per_shard);
   for (int r = 0; r < D; ++r) {
     if ((st = make_map(&p.tm_shard[r], a_shards[r], (uint64_t)K, (uint64_t)m_per_shard, kBK,
                        kBM)) != AG_OK)
       return st;
     if (straddle8 && (st = make_map(&p.tm_shard8[r], a_shards[r], (uint64_t)K,
-                                    (uint64_t)m_per_shard, kBK, 8)) != AG_OK)
+                                    (uint64_t)m_per_shard, kBK, 1u << p.sh_log2)) != AG_OK)
       return st;
   }
   const uint64_t epoch = g_epoch.fetch_add(1) + 1;

@@ -129,7 +129,7 @@ struct GemmParams {
   CUtensorMap tm_b;                    // b [K, N]: box {64, 64}, 128B swizzle (MN-major B)
   CUtensorMap tm_out;                  // out [M, N]: box {64, 32}, 128B swizzle (store)
   CUtensorMap tm_shard[kMaxShards];    // shard r [m_per_shard, K]: box {64, 128}
-  CUtensorMap tm_shard8[kMaxShards];   // shard r: box {64, 8} (row blocks straddling shards)
+  CUtensorMap tm_shard8[kMaxShards];   // shard r: box {64, 2^sh_log2} (row blocks straddling shards)
   const uint16_t* shards[kMaxShards];
   uint16_t* a_gathered;
   uint16_t* staging_mk;
@@ -151,6 +151,7 @@ struct GemmParams {
   int mb_start;             // first row block of the schedule (ring order)
   int ng;                   // column blocks per schedule pass
   int w0;                   // column blocks of the first pass (they own the chunks)
+  int sh_log2;              // log2 of the rows of a tm_shard8 box (3..6; divides m_per_shard)
   int fp16;                 // 1: fp16, 0: bf16
   int inject_skip_flag;     // this flag index is never published (fault injection)
 };
@@ -770,14 +771,16 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
             if (one_shard) {
               tma_load_2d(a_dst, &p.tm_shard[r0], &full[stage], kb * kBK, mb * kBM - r0 * p.mps);
             } else {
-              // Walk the 8-row groups across shard boundaries (m_per_shard is a
-              // multiple of 8 here) without a division per group.  Past the
-              // last shard the row stays out of range: TMA zero-fills it.
+              // Walk the row groups (2^sh_log2 rows, which divides both 128
+              // and m_per_shard, so no group straddles a boundary) across the
+              // shards without a division per group.  Past the last shard the
+              // row stays out of range: TMA zero-fills it.
+              const int h = 1 << p.sh_log2;
               int r = r0, lr = mb * kBM - r0 * p.mps;
 #pragma unroll 1
-              for (int q = 0; q < kBM / 8; ++q) {
-                tma_load_2d(a_dst + q * 1024, &p.tm_shard8[r], &full[stage], kb * kBK, lr);
-                lr += 8;
+              for (int q = 0; q < (kBM >> p.sh_log2); ++q) {
+                tma_load_2d(a_dst + q * h * 128, &p.tm_shard8[r], &full[stage], kb * kBK, lr);
+                lr += h;
                 if (lr >= p.mps && r < p.D - 1) {
                   lr -= p.mps;
                   ++r;
