@@ -204,6 +204,28 @@ int check_device_ptr(const void* p, int dev) {
   return AG_OK;
 }
 
+// Number of CTA pairs of the pair kernels that can be resident at once (0 if
+// a cluster launch is not possible).  A cluster's two CTAs need two free SMs
+// of one GPC; with 1 CTA per SM not every SM pairs up, and a persistent grid
+// larger than what fits at once would leave the extra clusters for a second
+// wave.  Allocates nothing.
+int query_pair_clusters(int sms, int* clusters) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(sms & ~1));
+  cfg.blockDim = dim3((unsigned)mode_threads(kFusedK));
+  cfg.dynamicSmemBytes = Pipe<true>::kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  *clusters = 0;
+  AG_CK(cudaOccupancyMaxActiveClusters(clusters, agmm_gemm_kernel<kFusedK, true>, &cfg));
+  return AG_OK;
+}
+
 int device_init(DevState& ds, int dev) {
   if (ds.init) return ds.supported ? AG_OK : AG_ERR_UNSUPPORTED;
   int major = 0, minor = 0, sms = 0;
@@ -234,25 +256,7 @@ int device_init(DevState& ds, int dev) {
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem2));
   AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kFusedK, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem2));
-  {
-    // A cluster's two CTAs need two free SMs of one GPC; with 1 CTA per SM not
-    // every SM pairs up.  A persistent grid larger than what fits at once
-    // would leave the extra clusters for a second wave.
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(sms & ~1));
-    cfg.blockDim = dim3((unsigned)mode_threads(kGemmK));
-    cfg.dynamicSmemBytes = kSmem2;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int clusters = 0;
-    AG_CK(cudaOccupancyMaxActiveClusters(&clusters, agmm_gemm_kernel<kGemmK, true>, &cfg));
-    ds.pair_clusters = clusters;
-  }
+  if (int st = query_pair_clusters(sms, &ds.pair_clusters)) return st;
   AG_CK(cudaMalloc(&ds.err, 2 * sizeof(unsigned long long)));
   AG_CK(cudaMemset(ds.err, 0, 2 * sizeof(unsigned long long)));
   ds.init = true;
@@ -284,6 +288,33 @@ int grow_workspace(DevState& ds, const Shape& s, bool need_flags, bool need_stag
     ds.staging_cap = stage_elems;
   }
   return AG_OK;
+}
+
+// The launch plan shared by every entry point: CTA pairs (256 x 256 tiles)
+// whenever two SMs are allowed, except the fused m-contiguous kernel (one pair
+// MMA reads both CTAs' A halves with one major-ness, and there a block's A can
+// be K-major, read from a shard, while its partner's is MN-major, read from the
+// [K, M] staging); the schedule; the automatic k_per_flag (the workspace is
+// sized for s.G, which is >= the automatic choice's G).  Fills the schedule
+// fields of p and returns the grid (CTAs; even for pairs).
+int plan_launch(GemmParams& p, const Shape& s, int cap, int pair_clusters, bool fused,
+                bool layout_m, int k_per_flag, int rank) {
+  const bool pair = !(fused && layout_m) && cap >= 2 && pair_clusters >= 1;
+  Shape sched = s;
+  sched.num_mb = pair ? (s.num_mb + 1) / 2 : s.num_mb;
+  const int units = pair ? std::min(cap / 2, pair_clusters) : cap;  // CTAs, or CTA pairs
+  p.pair = pair ? 1 : 0;
+  p.sched_mb = sched.num_mb;
+  p.num_tiles = (sched.num_mb * s.num_nb) << p.pair;
+  p.kpf = k_per_flag ? s.kpf
+                     : auto_k_per_flag(s.num_kb, s.num_nb,
+                                       (int64_t)sched.num_mb * s.num_nb <= units, layout_m);
+  p.G = (s.num_kb + p.kpf - 1) / p.kpf;
+  // schedule rows start at the local shard (pairs: the pair holding its first block)
+  p.mb_start = fused ? (int)(((int64_t)rank * s.mps) / kBM) >> p.pair : 0;
+  p.ng = schedule_group(sched, units);
+  p.w0 = std::min(p.ng, s.num_nb);
+  return std::max(1, std::min(units, sched.num_mb * s.num_nb)) << p.pair;
 }
 
 // pair: clusters of two CTAs (grid even), the kernel's CTA-pair variant.
@@ -490,30 +521,11 @@ int run(bool fused, const void** a_shards, int D, int m_per_shard, int K, const 
   p.num_mb = s.num_mb;
   p.num_nb = s.num_nb;
   p.num_kb = s.num_kb;
-  // CTA pairs (256 x 256 tiles) whenever two SMs are allowed, except the
-  // fused m-contiguous kernel: one pair MMA reads both CTAs' A halves with one
-  // major-ness, and there a block's A can be K-major (read from a shard) while
-  // its partner's is MN-major (read from the [K, M] staging).
-  const bool pair = !(fused && layout_m) && cap >= 2 && ds.pair_clusters >= 1;
-  Shape sched = s;
-  sched.num_mb = pair ? (s.num_mb + 1) / 2 : s.num_mb;
-  const int units = pair ? std::min(cap / 2, ds.pair_clusters) : cap;  // CTAs, or CTA pairs
-  p.pair = pair ? 1 : 0;
-  p.sched_mb = sched.num_mb;
-  p.num_tiles = (sched.num_mb * s.num_nb) << p.pair;
-  // (the workspace is sized for s.G, which is >= the automatic choice's G)
-  p.kpf = o.k_per_flag ? s.kpf
-                       : auto_k_per_flag(s.num_kb, s.num_nb,
-                                         (int64_t)sched.num_mb * s.num_nb <= units, layout_m);
-  p.G = (s.num_kb + p.kpf - 1) / p.kpf;
-  // schedule rows start at the local shard (pairs: the pair holding its first block)
-  p.mb_start = fused ? (int)(((int64_t)o.rank * m_per_shard) / kBM) >> p.pair : 0;
-  p.ng = schedule_group(sched, units);
-  p.w0 = std::min(p.ng, s.num_nb);
+  const int grid = plan_launch(p, s, cap, ds.pair_clusters, fused, layout_m, o.k_per_flag,
+                               fused ? o.rank : 0);
   p.fp16 = o.dtype == AG_DTYPE_FP16 ? 1 : 0;
   p.inject_skip_flag = fused ? o.inject_skip_flag : -1;
-
-  const int grid = std::max(1, std::min(units, sched.num_mb * s.num_nb)) << p.pair;
+  const bool pair = p.pair != 0;
   if (fused && layout_m) return launch<kFusedM, false>(grid, stream, p, "fused kernel");
   if (fused)
     return pair ? launch<kFusedK, true>(grid, stream, p, "fused kernel")
@@ -543,6 +555,7 @@ struct NoAllocState {
   bool init = false;
   bool supported = false;
   int sms = 0;
+  int pair_clusters = 0;
   uint8_t* scratch = nullptr;  // device address of g_noalloc_scratch on this device
   uint64_t reported_epoch = 0;
 };
@@ -567,6 +580,10 @@ int noalloc_setup(NoAllocState& ns, int dev) {
   AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kFusedK, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Pipe<false>::kSmemBytes));
+  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kFusedK, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Pipe<true>::kSmemBytes));
+  if (int st = query_pair_clusters(sms, &ns.pair_clusters)) return st;
   void* ptr = nullptr;
   AG_CK(cudaGetSymbolAddress(&ptr, g_noalloc_scratch));
   if (!ptr || !aligned(ptr, 256)) {
@@ -663,19 +680,12 @@ int run_noalloc(const void** a_shards, int D, int m_per_shard, int K, const void
   p.num_mb = s.num_mb;
   p.num_nb = s.num_nb;
   p.num_kb = s.num_kb;
-  p.pair = 0;
-  p.sched_mb = s.num_mb;
-  p.num_tiles = s.num_mb * s.num_nb;
   const int cap = o.num_sms ? std::min(o.num_sms, ns.sms) : ns.sms;
-  p.kpf = o.k_per_flag ? s.kpf : auto_k_per_flag(s.num_kb, s.num_nb, p.num_tiles <= cap, false);
-  p.G = (s.num_kb + p.kpf - 1) / p.kpf;
-  p.mb_start = (int)(((int64_t)o.rank * m_per_shard) / kBM);
-  p.ng = schedule_group(s, cap);
-  p.w0 = std::min(p.ng, s.num_nb);
+  const int grid = plan_launch(p, s, cap, ns.pair_clusters, true, false, o.k_per_flag, o.rank);
   p.fp16 = o.dtype == AG_DTYPE_FP16 ? 1 : 0;
   p.inject_skip_flag = o.inject_skip_flag;
-  const int grid = std::max(1, std::min(cap, p.num_tiles));
-  return launch<kFusedK, false>(grid, stream, p, "fused kernel (no-alloc)");
+  return p.pair ? launch<kFusedK, true>(grid, stream, p, "fused kernel (no-alloc)")
+                : launch<kFusedK, false>(grid, stream, p, "fused kernel (no-alloc)");
 }
 
 }  // namespace
