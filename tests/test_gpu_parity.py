@@ -286,12 +286,14 @@ def test_host_pointer_is_rejected():
 # ---------------------------------------------------------------- failure detection
 
 def test_ready_flag_timeout_is_reported_and_context_survives(oracle_mod):
-    """Fault injection: the CTA that stages chunk 0 (row block 0, which lies
-    in the non-local shard) never publishes its flag, so the other CTA that
-    needs that row block runs its bounded wait out; the kernel records
-    AG_ERR_TIMEOUT with the flag index, finishes, and the next call on the
-    same context is correct.  Two column blocks give row block 0 two readers."""
-    w = inp.Workload("inject", D=2, m_per_shard=128, K=256, N=512, dtype="bf16")
+    """Fault injection: chunk 0 (row block 0, which lies in the non-local
+    shard) is never published, so a reader of that row block runs its bounded
+    wait out; the kernel records AG_ERR_TIMEOUT with the flag index, finishes,
+    and the next call on the same context is correct.  Three column blocks
+    give the chunk an owner and two readers: a reader that finds the owner not
+    yet started takes the chunk over (and never publishes it either), which
+    leaves the other reader waiting, so the timeout does not depend on timing."""
+    w = inp.Workload("inject", D=2, m_per_shard=128, K=256, N=768, dtype="bf16")
     x = inp.make_inputs(w)
     shards, b, _ = to_device(x)
     agmm.device_error()  # clear anything older

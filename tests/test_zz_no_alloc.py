@@ -93,10 +93,11 @@ def test_noalloc_rejects_what_its_scratch_cannot_hold():
 
 def test_noalloc_device_timeout_is_reported():
     """A chunk whose ready flag is never published (fault injection, host-set)
-    makes the follower's bounded wait run out; the error recorded in the
-    no-alloc scratch comes back through ag_get_device_error, and the next call
-    is correct again."""
-    w = inp.Workload("noalloc_inject", D=2, m_per_shard=128, K=256, N=512, dtype="bf16")
+    makes a reader's bounded wait run out; the error recorded in the no-alloc
+    scratch comes back through ag_get_device_error, and the next call is
+    correct again.  Three column blocks give the chunk two readers besides its
+    owner, so one of them waits even if the other takes the chunk over."""
+    w = inp.Workload("noalloc_inject", D=2, m_per_shard=128, K=256, N=768, dtype="bf16")
     x = inp.make_inputs(w)
     shards = [s.cuda() for s in x.shards]
     b = x.b.cuda()
