@@ -256,6 +256,8 @@ int device_init(DevState& ds, int dev) {
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem2));
   AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kFusedK, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem2));
+  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kFusedM, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem2));
   if (int st = query_pair_clusters(sms, &ds.pair_clusters)) return st;
   AG_CK(cudaMalloc(&ds.err, 2 * sizeof(unsigned long long)));
   AG_CK(cudaMemset(ds.err, 0, 2 * sizeof(unsigned long long)));
@@ -291,15 +293,12 @@ int grow_workspace(DevState& ds, const Shape& s, bool need_flags, bool need_stag
 }
 
 // The launch plan shared by every entry point: CTA pairs (256 x 256 tiles)
-// whenever two SMs are allowed, except the fused m-contiguous kernel (one pair
-// MMA reads both CTAs' A halves with one major-ness, and there a block's A can
-// be K-major, read from a shard, while its partner's is MN-major, read from the
-// [K, M] staging); the schedule; the automatic k_per_flag (the workspace is
-// sized for s.G, which is >= the automatic choice's G).  Fills the schedule
-// fields of p and returns the grid (CTAs; even for pairs).
+// whenever two SMs are allowed; the schedule; the automatic k_per_flag (the
+// workspace is sized for s.G, which is >= the automatic choice's G).  Fills
+// the schedule fields of p and returns the grid (CTAs; even for pairs).
 int plan_launch(GemmParams& p, const Shape& s, int cap, int pair_clusters, bool fused,
                 bool layout_m, int k_per_flag, int rank) {
-  const bool pair = !(fused && layout_m) && cap >= 2 && pair_clusters >= 1;
+  const bool pair = cap >= 2 && pair_clusters >= 1;
   Shape sched = s;
   sched.num_mb = pair ? (s.num_mb + 1) / 2 : s.num_mb;
   const int units = pair ? std::min(cap / 2, pair_clusters) : cap;  // CTAs, or CTA pairs
@@ -526,7 +525,9 @@ int run(bool fused, const void** a_shards, int D, int m_per_shard, int K, const 
   p.fp16 = o.dtype == AG_DTYPE_FP16 ? 1 : 0;
   p.inject_skip_flag = fused ? o.inject_skip_flag : -1;
   const bool pair = p.pair != 0;
-  if (fused && layout_m) return launch<kFusedM, false>(grid, stream, p, "fused kernel");
+  if (fused && layout_m)
+    return pair ? launch<kFusedM, true>(grid, stream, p, "fused kernel")
+                : launch<kFusedM, false>(grid, stream, p, "fused kernel");
   if (fused)
     return pair ? launch<kFusedK, true>(grid, stream, p, "fused kernel")
                 : launch<kFusedK, false>(grid, stream, p, "fused kernel");

@@ -550,6 +550,10 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
   constexpr int kStageBytes = P::kStageBytes;
   constexpr bool kFused = mode_fused(kMode);
   constexpr bool kLayoutM = mode_layout_m(kMode);
+  // Fused m-contiguous on CTA pairs: every A tile is read from the [K, M]
+  // staging (MN-major) -- the owner's window and local rows included, once
+  // published -- because one pair MMA reads both CTAs' A with one major-ness.
+  constexpr bool kAllStaged = kFused && kLayoutM && kPair;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -641,7 +645,8 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
       if (t < p.num_tiles) {
         tile_ctx<kFused>(p, t, cur);
         const int g0 = chunk_at(0, cur.ws, cur.we);
-        if (cur.kind != kLocal && cur.kind != kEmpty && !cur.owns(g0))
+        if (kAllStaged ? cur.kind != kEmpty
+                       : (cur.kind != kLocal && cur.kind != kEmpty && !cur.owns(g0)))
           cur_peek = ld_relaxed_gpu(p.flags + cur.mb * p.G + g0);
         if (t + (int)gridDim.x < p.num_tiles) tile_ctx<kFused>(p, t + gridDim.x, nxt);
       }
@@ -655,7 +660,8 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
           // handed chunks are published whatever this CTA's pipeline does --
           // with CTA pairs that pipeline also waits on the partner CTA.
           if (cur.kind == kLocal || cur.kind == kDirect) {
-            const uint32_t wbits = cur.kind == kDirect ? (kInfoStage | kInfoPublish) : kInfoStage;
+            const uint32_t wbits =
+                (cur.kind == kDirect || kAllStaged) ? (kInfoStage | kInfoPublish) : kInfoStage;
             for (int wg = cur.ws + cur_pre; wg < cur.we; ++wg) {
               if (!wait_bar(p, &rfree[rslot], rphase ^ 1u, abort_flag, kSiteRing)) {
                 aborted = true;
@@ -689,11 +695,11 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
           // the shard.
           // (Owned chunks were handed to the copiers at the tile start.)
           const bool staged_ahead = cur.owns(g) && g - cur.ws < cur_pre;
-          if (kind == kLocal) {
+          if (kind == kLocal && !kAllStaged) {
             direct = true;
           } else if (kind == kEmpty) {
-            // rows past M: a_gathered's map reads zeros there
-          } else if (kind == kDirect && cur.owns(g) && !staged_ahead) {
+            // rows past M: the gathered copy's maps read zeros there
+          } else if (kind == kDirect && cur.owns(g) && !staged_ahead && !kAllStaged) {
             direct = true;
           } else {
             const uint64_t target = p.fbase + (uint64_t)nbox;
@@ -701,10 +707,31 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
               fence_acquire_gpu();  // the relaxed read saw it published: make it an acquire
             } else {
               const uint64_t t0 = p.trace ? globaltimer_ns() : 0;
-              const int owner_tile = kind == kDirect ? tile_index(p, mb, owner_nb(p, g)) : -1;
+              const int owner_tile =
+                  (kind == kDirect || (kAllStaged && kind == kLocal))
+                      ? tile_index(p, mb, owner_nb(p, g)) : -1;
               if (wait_or_take(p, flag_idx, target, owner_tile)) {
-                direct = true;
-                bits = kInfoStage | kInfoPublish;
+                if constexpr (kAllStaged) {
+                  // Taken over: have it staged here, then read it like anyone else.
+                  if (!wait_bar(p, &rfree[rslot], rphase ^ 1u, abort_flag, kSiteRing)) {
+                    aborted = true;
+                    break;
+                  }
+                  hand_chunk(ring + rslot * kRingWords, &rfull[rslot], kInfoStage | kInfoPublish,
+                             mb, g, nbox, flag_idx, seq, p);
+                  if (++rslot == kRing) {
+                    rslot = 0;
+                    rphase ^= 1u;
+                  }
+                  if (p.trace) {
+                    const uint64_t now = globaltimer_ns();
+                    trace_rec(p.trace, p.trace_words, kTraceClaim, mb, g, now, now);
+                  }
+                  wait_or_take(p, flag_idx, target, -1);
+                } else {
+                  direct = true;
+                  bits = kInfoStage | kInfoPublish;
+                }
               }
               if (p.trace) trace_rec(p.trace, p.trace_words, kTraceWait, mb, g, t0, globaltimer_ns());
             }
@@ -750,8 +777,10 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
         bool nxt_follow = false;
         if (kFused && nt < p.num_tiles) {
           const int ng = chunk_at(ngi, n_ws, n_we);
-          nxt_follow = n_kind != kLocal && n_kind != kEmpty &&
-                       !(n_kind == kDirect && ng >= n_ws && ng < n_we && ng - n_ws >= n_pre);
+          nxt_follow = kAllStaged ? n_kind != kEmpty
+                                  : (n_kind != kLocal && n_kind != kEmpty &&
+                                     !(n_kind == kDirect && ng >= n_ws && ng < n_we &&
+                                       ng - n_ws >= n_pre));
           if (nxt_follow) nxt_peek = ld_relaxed_gpu(p.flags + n_mb * p.G + ng);
         }
 
@@ -816,7 +845,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
           // Stage ahead: one chunk of the next tile's window.
           const int pg = nxt.ws + pre;
           hand_chunk(ring + rslot * kRingWords, &rfull[rslot],
-                     kInfoStage | (nxt.kind == kDirect ? kInfoPublish : 0u), nxt.mb, pg,
+                     kInfoStage | ((nxt.kind == kDirect || kAllStaged) ? kInfoPublish : 0u), nxt.mb, pg,
                      chunk_boxes(p, pg), nxt.mb * p.G + pg, seq, p);
           if (p.trace) {
             const uint64_t now = globaltimer_ns();
