@@ -31,7 +31,8 @@ LAYOUTS = {"k_contiguous": 0, "m_contiguous": 1}
 DTYPES = {"bf16": 0, "fp16": 1}
 EXPORTS = ("ag_options_default", "ag_matmul", "ag_then_matmul", "ag_matmul_ex",
            "ag_then_matmul_ex", "ag_workspace_size", "ag_get_device_error",
-           "ag_release_workspace", "ag_status_string", "ag_num_sms", "ag_matmul_noalloc")
+           "ag_release_workspace", "ag_status_string", "ag_num_sms", "ag_matmul_noalloc",
+           "ag_chunked_matmul_ex")
 
 
 class AgmmError(RuntimeError):
@@ -94,6 +95,8 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.ag_num_sms.restype = i32
     lib.ag_matmul_noalloc.argtypes = core + [ctypes.POINTER(AgOptions)]
     lib.ag_matmul_noalloc.restype = i32
+    lib.ag_chunked_matmul_ex.argtypes = core + [ctypes.POINTER(AgOptions), i32]
+    lib.ag_chunked_matmul_ex.restype = i32
     _lib = lib
     return lib
 
@@ -149,7 +152,7 @@ def ag_matmul_raw(fused: bool, shard_ptrs, D, m_per_shard, K, b_ptr, N, bias_ptr
 
 
 def _call(fused, shards, b, bias, a_gathered, out, stream, layout, rank, k_per_flag, num_sms,
-          timeout_ns, inject_skip_flag, trace, workspace):
+          timeout_ns, inject_skip_flag, trace, workspace, chunks=0):
     import torch
     if not shards:
         raise ValueError("need at least one shard")
@@ -183,6 +186,17 @@ def _call(fused, shards, b, bias, a_gathered, out, stream, layout, rank, k_per_f
     if workspace is not None:
         o.workspace = workspace.data_ptr()
         o.workspace_bytes = workspace.numel() * workspace.element_size()
+    if chunks:
+        lib = library()
+        arr = (ctypes.c_void_p * D)(*[ctypes.c_void_p(s.data_ptr()) for s in shards])
+        st = lib.ag_chunked_matmul_ex(
+            arr, D, m, K, ctypes.c_void_p(b.data_ptr()), N,
+            ctypes.c_void_p(bias.data_ptr()) if bias is not None else None,
+            ctypes.c_void_p(a_gathered.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+            _stream_handle(stream), ctypes.byref(o), chunks)
+        if st != 0:
+            raise AgmmError(st, "ag_chunked_matmul")
+        return a_gathered, out
     st = ag_matmul_raw(fused, [s.data_ptr() for s in shards], D, m, K, b.data_ptr(), N,
                        bias.data_ptr() if bias is not None else 0, a_gathered.data_ptr(),
                        out.data_ptr(), _stream_handle(stream), o)
@@ -206,6 +220,17 @@ def ag_then_matmul(shards, b, bias=None, *, a_gathered=None, out=None, stream=No
     """Barrier baseline: gather kernel, then GEMM kernel.  Returns (a_gathered, out)."""
     return _call(False, shards, b, bias, a_gathered, out, stream, layout, 0, k_per_flag,
                  num_sms, timeout_ns, -1, trace, None)
+
+
+def ag_chunked_matmul(shards, b, bias=None, *, chunks: int = 4, a_gathered=None, out=None,
+                      stream=None, num_sms: int = 0, timeout_ns: int = 0):
+    """Chunked pipeline: chunk s = the s-th sub-block of every shard; per chunk
+    (four streams round-robin) gather it, then multiply its rows.  Returns
+    (a_gathered, out); bitwise equal to ag_then_matmul's."""
+    if chunks < 1:
+        raise ValueError("chunks must be >= 1")
+    return _call(False, shards, b, bias, a_gathered, out, stream, "k_contiguous", 0, 0,
+                 num_sms, timeout_ns, -1, None, None, chunks=chunks)
 
 
 def device_error(stream=None):

@@ -89,6 +89,11 @@ struct DevState {
   int sms = 0;
   int pair_clusters = 0;  // CTA pairs of the pair kernels that fit on the GPU at once
   unsigned long long* err = nullptr;  // [2] device error word
+  // chunked pipeline: its streams and fork/join events (created on first use)
+  static constexpr int kChunkStreams = 4;
+  bool chunk_init = false;
+  cudaStream_t cstream[kChunkStreams] = {};
+  cudaEvent_t fork_ev = nullptr, join_ev[kChunkStreams] = {};
   uint64_t* flags = nullptr;
   size_t flags_cap = 0;  // words
   uint16_t* staging = nullptr;
@@ -458,6 +463,10 @@ int run(bool fused, const void** a_shards, int D, int m_per_shard, int K, const 
     gp.M = (int)s.M;
     gp.K = K;
     gp.mps = m_per_shard;
+    gp.row0 = 0;
+    gp.row1 = (int)s.M;
+    gp.loc0 = 0;
+    gp.loc1 = m_per_shard;
     gp.trace = o.trace;
     gp.trace_words = o.trace_words;
     if (layout_m) {
@@ -536,6 +545,136 @@ int run(bool fused, const void** a_shards, int D, int m_per_shard, int K, const 
                 : launch<kGemmM, false>(grid, stream, p, "gemm kernel");
   return pair ? launch<kGemmK, true>(grid, stream, p, "gemm kernel")
               : launch<kGemmK, false>(grid, stream, p, "gemm kernel");
+}
+
+}  // namespace
+
+namespace {
+
+// ---------------------------------------------------------------------------
+// The chunked pipeline: the third way to run the operation, between the
+// barrier (one gather, then one GEMM) and the fused kernel (tile-level flags).
+// A is taken as [S, D, m/S, K] (S chunks, D shards): chunk s is the s-th
+// sub-block of every shard, local rows [s*m/S, (s+1)*m/S).  For each chunk,
+// round-robin over four streams: gather the chunk (every shard contributes),
+// then multiply its D row segments (the barrier GEMM core, k ascending, one
+// launch per segment).  The caller's stream forks to the chunk streams and
+// joins back.
+
+// One barrier-core GEMM on rows [r0, r1) of a_gathered into the same rows of out.
+int gemm_rows(DevState& ds, const Shape& s, int r0, int r1, const void* a_gathered, const void* b,
+              const void* bias, void* out, int cap, const ag_options& o, uint64_t epoch,
+              int64_t timeout, cudaStream_t stream) {
+  Shape sc = s;
+  sc.M = r1 - r0;
+  sc.num_mb = (r1 - r0 + kBM - 1) / kBM;
+  const uint16_t* a_rows = static_cast<const uint16_t*>(a_gathered) + (int64_t)r0 * s.K;
+  uint16_t* out_rows = static_cast<uint16_t*>(out) + (int64_t)r0 * s.N;
+  GemmParams p;
+  memset(&p, 0, sizeof p);
+  int st;
+  if ((st = make_map(&p.tm_a, a_rows, (uint64_t)s.K, (uint64_t)sc.M, kBK, kBM)) != AG_OK) return st;
+  if ((st = make_map(&p.tm_b, b, (uint64_t)s.N, (uint64_t)s.K, 64, kBK)) != AG_OK) return st;
+  if ((st = make_map(&p.tm_out, out_rows, (uint64_t)s.N, (uint64_t)sc.M, kEpiCols, kEpiRows)) !=
+      AG_OK)
+    return st;
+  p.a_gathered = const_cast<uint16_t*>(a_rows);
+  p.bias = static_cast<const float*>(bias);
+  p.err = ds.err;
+  p.epoch = epoch;
+  p.fbase = epoch << kFlagShift;
+  p.timeout_ns = timeout;
+  p.pipe_timeout_ns = 4 * timeout + 2000000000LL;
+  p.M = (int)sc.M;
+  p.N = s.N;
+  p.K = s.K;
+  p.D = 1;
+  p.mps = (int)sc.M;
+  p.num_mb = sc.num_mb;
+  p.num_nb = sc.num_nb;
+  p.num_kb = sc.num_kb;
+  p.sh_log2 = 3;
+  p.fp16 = o.dtype == AG_DTYPE_FP16 ? 1 : 0;
+  p.inject_skip_flag = -1;
+  const int grid = plan_launch(p, sc, cap, ds.pair_clusters, false, false, o.k_per_flag, 0);
+  return p.pair ? launch<kGemmK, true>(grid, stream, p, "gemm kernel (chunk)")
+                : launch<kGemmK, false>(grid, stream, p, "gemm kernel (chunk)");
+}
+
+int run_chunked(const void** a_shards, int D, int m_per_shard, int K, const void* b, int N,
+                const void* bias, void* a_gathered, void* out, cudaStream_t stream,
+                const ag_options* opt_in, int chunks) {
+  ag_options o;
+  ag_options_default(&o);
+  if (opt_in) o = *opt_in;
+  Shape s;
+  int st = validate(a_shards, D, m_per_shard, K, b, N, bias, a_gathered, out, o, false, &s);
+  if (st != AG_OK) return st;
+  if (chunks < 1 || chunks > 4096) return AG_ERR_INVALID_ARG;
+  if (o.layout != AG_LAYOUT_K_CONTIGUOUS) return AG_ERR_UNSUPPORTED;
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  AG_CK(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices) return AG_ERR_UNSUPPORTED;
+  DevState& ds = g_dev[dev];
+  if ((st = device_init(ds, dev)) != AG_OK) return st;
+  for (int r = 0; r < D; ++r)
+    if ((st = check_device_ptr(a_shards[r], dev)) != AG_OK) return st;
+  if ((st = check_device_ptr(b, dev)) != AG_OK || (st = check_device_ptr(a_gathered, dev)) != AG_OK ||
+      (st = check_device_ptr(out, dev)) != AG_OK)
+    return st;
+  if (bias && (st = check_device_ptr(bias, dev)) != AG_OK) return st;
+  if (!ds.chunk_init) {
+    for (int i = 0; i < DevState::kChunkStreams; ++i) {
+      AG_CK(cudaStreamCreateWithFlags(&ds.cstream[i], cudaStreamNonBlocking));
+      AG_CK(cudaEventCreateWithFlags(&ds.join_ev[i], cudaEventDisableTiming));
+    }
+    AG_CK(cudaEventCreateWithFlags(&ds.fork_ev, cudaEventDisableTiming));
+    ds.chunk_init = true;
+  }
+
+  const uint64_t epoch = g_epoch.fetch_add(1) + 1;
+  const int64_t timeout = o.timeout_ns ? o.timeout_ns : kDefaultTimeoutNs;
+  const int cap = o.num_sms ? std::min(o.num_sms, ds.sms) : ds.sms;
+  const int S = std::min(chunks, m_per_shard);  // every sub-block has a row
+  const int used = std::min(S, DevState::kChunkStreams);
+  AG_CK(cudaEventRecord(ds.fork_ev, stream));
+  for (int i = 0; i < used; ++i) AG_CK(cudaStreamWaitEvent(ds.cstream[i], ds.fork_ev, 0));
+
+  for (int c = 0; c < S; ++c) {
+    cudaStream_t cs = ds.cstream[c % DevState::kChunkStreams];
+    const int lo = (int)((int64_t)c * m_per_shard / S);
+    const int hi = (int)((int64_t)(c + 1) * m_per_shard / S);
+    GatherParams gp;
+    memset(&gp, 0, sizeof gp);
+    for (int r = 0; r < D; ++r) gp.shards[r] = static_cast<const uint16_t*>(a_shards[r]);
+    gp.a_gathered = static_cast<uint16_t*>(a_gathered);
+    gp.vec_per_shard = (int64_t)m_per_shard * K / 8;
+    gp.M = (int)s.M;
+    gp.K = K;
+    gp.mps = m_per_shard;
+    gp.row0 = 0;
+    gp.row1 = (int)s.M;
+    gp.loc0 = lo;
+    gp.loc1 = hi;
+    const int64_t blocks = ((int64_t)(hi - lo) * K / 8 + 255) / 256;
+    const int gx = (int)std::max<int64_t>(1, std::min<int64_t>((ds.sms * 4 + D - 1) / D, blocks));
+    agmm_gather_kernel<<<dim3(gx, D), 256, 0, cs>>>(gp);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "gather kernel launch (chunk)");
+    for (int d = 0; d < D; ++d) {
+      const int r0 = d * m_per_shard + lo, r1 = d * m_per_shard + hi;
+      if ((st = gemm_rows(ds, s, r0, r1, a_gathered, b, bias, out, cap, o, epoch, timeout, cs)) !=
+          AG_OK)
+        return st;
+    }
+  }
+  for (int i = 0; i < used; ++i) {
+    AG_CK(cudaEventRecord(ds.join_ev[i], ds.cstream[i]));
+    AG_CK(cudaStreamWaitEvent(stream, ds.join_ev[i], 0));
+  }
+  return AG_OK;
 }
 
 }  // namespace
@@ -727,6 +866,13 @@ int ag_then_matmul_ex(const void** a_shards, int D, int m_per_shard, int K, cons
                       const void* bias_or_null, void* a_gathered, void* out, cudaStream_t stream,
                       const ag_options* opt) {
   return run(false, a_shards, D, m_per_shard, K, b, N, bias_or_null, a_gathered, out, stream, opt);
+}
+
+int ag_chunked_matmul_ex(const void** a_shards, int D, int m_per_shard, int K, const void* b,
+                         int N, const void* bias_or_null, void* a_gathered, void* out,
+                         cudaStream_t stream, const ag_options* opt, int chunks) {
+  return run_chunked(a_shards, D, m_per_shard, K, b, N, bias_or_null, a_gathered, out, stream,
+                     opt, chunks);
 }
 
 size_t ag_workspace_size(int D, int m_per_shard, int K, int N, const ag_options* opt) {

@@ -162,6 +162,8 @@ struct GatherParams {
   uint16_t* staging_mk;     // [K, M] or null
   int64_t vec_per_shard;    // 16-byte vectors per shard
   int M, K, mps;
+  int row0, row1;           // agmm_gather_kernel copies gathered rows [row0, row1) ...
+  int loc0, loc1;           // ... that are also local rows [loc0, loc1) of their shard
   uint64_t* trace;
   int64_t trace_words;
 };
@@ -1136,14 +1138,21 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
 }
 
 // Barrier-path gather: shard r is copied to rows [r*m_per_shard, ...) of
-// a_gathered.  Each shard is one contiguous block, so this is D flat copies;
+// a_gathered, restricted to gathered rows [row0, row1) and to local rows
+// [loc0, loc1) of each shard (everything for the barrier baseline; for the
+// chunked pipeline, chunk s's sub-block of every shard).  What a shard
+// contributes is one contiguous block, so this is at most D flat copies;
 // blockIdx.y selects the shard.
 __global__ void __launch_bounds__(256) agmm_gather_kernel(const __grid_constant__ GatherParams gp) {
   const uint64_t t0 = gp.trace ? globaltimer_ns() : 0;
   const int s = blockIdx.y;
-  const uint4* src = reinterpret_cast<const uint4*>(gp.shards[s]);
-  uint4* dst = reinterpret_cast<uint4*>(gp.a_gathered) + (int64_t)s * gp.vec_per_shard;
-  const int64_t n = gp.vec_per_shard;
+  const int64_t lo = max(max(0, gp.row0 - s * gp.mps), gp.loc0);
+  const int64_t hi = min(min(gp.mps, gp.row1 - s * gp.mps), gp.loc1);
+  if (hi <= lo) return;
+  const int64_t vk = gp.K / 8;  // 16-byte vectors per row (K % 8 == 0)
+  const uint4* src = reinterpret_cast<const uint4*>(gp.shards[s]) + lo * vk;
+  uint4* dst = reinterpret_cast<uint4*>(gp.a_gathered) + ((int64_t)s * gp.mps + lo) * vk;
+  const int64_t n = (hi - lo) * vk;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   constexpr int U = 4;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride * U) {

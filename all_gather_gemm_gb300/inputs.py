@@ -101,6 +101,16 @@ def iris_m4096_bias() -> Workload:
                     b_scale="inv_sqrt_k", bias=True, layouts=("m_contiguous",))
 
 
+def iris_m16384_colshard(D: int = 8) -> Workload:
+    """Output-sharded form of the M=16384 workload: one rank's column slice,
+    N = 3584 / D (b column-sharded), the same gathered A (M=16384, K=8192,
+    fp16, D shards).  The gather is unchanged while the GEMM is D times
+    smaller."""
+    return Workload(f"m16384_d{D}_colshard", D=D, m_per_shard=16384 // D, K=8192,
+                    N=3584 // D, dtype="fp16", a_dist="normal", a_scale="one",
+                    b_dist="normal", b_scale="inv_sqrt_k")
+
+
 def all_workloads() -> list:
     return ([small_two_shard()] + cube_sweep() + [iris_m1024(d) for d in (2, 4, 8)]
             + [iris_m16384(), iris_m4096_bias()])

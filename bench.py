@@ -44,6 +44,8 @@ if ROOT not in sys.path:
 METRIC = "ag_matmul TFLOPS & µs on 1 GB300 vs tensor peak; speedup over gather-then-GEMM"
 UNIT = "TFLOPS"
 L2_FLUSH_BYTES = 512 << 20
+# chunked pipeline: S chunks (the Fuser page's pipelined AG+GEMM; four streams)
+CHUNKS = 4
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = [os.path.join(ROOT, "all_gather_gemm_gb300", "csrc", f)
                   for f in ("agmm.cu", "kernels.cuh", "ptx.cuh")]
@@ -66,6 +68,16 @@ def load_peaks():
             float(d["hbm_gbs"]), "measured"
     except Exception:
         return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+def pct(xs, q):
+    """q-th percentile (linear interpolation between order statistics)."""
+    v = sorted(xs)
+    if len(v) == 1:
+        return v[0]
+    x = (len(v) - 1) * q / 100.0
+    i = int(x)
+    return v[i] + (v[min(i + 1, len(v) - 1)] - v[i]) * (x - i)
 
 
 def load_traffic(workload_name: str, layout: str):
@@ -149,7 +161,8 @@ def headline_workload(name: str):
     table = {"m16384_d8": inp.iris_m16384(), "m4096_d8_bias": inp.iris_m4096_bias(),
              "m1024_d8": inp.iris_m1024(8), "m1024_d2": inp.iris_m1024(2),
              "m1024_d4": inp.iris_m1024(4), "two_shard_256": inp.small_two_shard(),
-             "cube_4096": inp.cube(4096), "cube_2048": inp.cube(2048)}
+             "cube_4096": inp.cube(4096), "cube_2048": inp.cube(2048),
+             "m16384_d8_colshard": inp.iris_m16384_colshard()}
     return table[name]
 
 
@@ -204,7 +217,8 @@ def run_reference(args, w, rank, world):
 def run_sweep(args):
     """Fused vs barrier device time (and host time per call) on the workloads of
     the parity configs: the two-shard case, the cube sweep, M=1024 at D=2/4/8,
-    M=16384 (both layouts) and M=4096 with bias (m-contiguous)."""
+    M=16384 (both layouts) and M=4096 with bias (m-contiguous); plus the
+    output-sharded M=16384 slice (N = 3584 / 8, both layouts)."""
     import torch
 
     import all_gather_gemm_gb300 as agmm
@@ -215,6 +229,9 @@ def run_sweep(args):
     cases += [(inp.iris_m1024(d), "k_contiguous") for d in (2, 4, 8)]
     cases += [(inp.iris_m16384(), "k_contiguous"), (inp.iris_m16384(), "m_contiguous"),
               (inp.iris_m4096_bias(), "m_contiguous")]
+    # output-sharded variant: one rank's N/8 column slice of the M=16384 problem
+    cases += [(inp.iris_m16384_colshard(), "k_contiguous"),
+              (inp.iris_m16384_colshard(), "m_contiguous")]
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
     steps = max(args.steps // 5, 5)
     for w, layout in cases:
@@ -229,6 +246,9 @@ def run_sweep(args):
                                             layout=layout),
             "barrier": lambda: agmm.ag_then_matmul(shards, b, bias, a_gathered=a_g, out=out,
                                                    layout=layout)}
+        if layout == "k_contiguous":
+            calls["chunked"] = lambda: agmm.ag_chunked_matmul(shards, b, bias, chunks=CHUNKS,
+                                                              a_gathered=a_g, out=out)
         for fn in calls.values():
             for _ in range(3):
                 fn()
@@ -256,6 +276,11 @@ def run_sweep(args):
                           "fused_tflops": w.flops / (f_us * 1e-6) / 1e12,
                           "host_us_fused": statistics.median(host["fused"]),
                           "host_us_barrier": statistics.median(host["barrier"]),
+                          "chunked_us": statistics.median(dev["chunked"]) if "chunked" in dev
+                          else None,
+                          "chunks": CHUNKS if "chunked" in dev else None,
+                          "host_us_chunked": statistics.median(host["chunked"])
+                          if "chunked" in dev else None,
                           "device_error": code}), flush=True)
 
 
@@ -362,6 +387,45 @@ def main():
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         t_f, t_b = tt.tolist()
 
+    # ---------------- chunked pipeline (k-contiguous only): the third comparison
+    # point, timed like the headline (flushed, per call) but outside its region
+    chunked = None
+    if args.layout == "k_contiguous":
+        a_g3 = torch.empty((w.M, w.K), dtype=b.dtype, device="cuda")
+        out3 = torch.empty((w.M, w.N), dtype=b.dtype, device="cuda")
+
+        def chunked_call():
+            agmm.ag_chunked_matmul(shards, b, bias, chunks=CHUNKS, a_gathered=a_g3, out=out3,
+                                   stream=stream)
+        for _ in range(3):
+            chunked_call()
+        c_ev = [(ev(), ev()) for _ in range(max(5, min(args.steps, 20)))]
+        for i, (s_, e_) in enumerate(c_ev):
+            flush.fill_(i)
+            s_.record(stream)
+            chunked_call()
+            e_.record(stream)
+        torch.cuda.synchronize()
+        c_ms = [s_.elapsed_time(e_) for s_, e_ in c_ev]
+        chunked = {"chunks": CHUNKS, "us_median": statistics.median(c_ms) * 1e3,
+                   "us_p10_p90": [pct(c_ms, 10) * 1e3, pct(c_ms, 90) * 1e3],
+                   "speedup_of_fused": statistics.median(c_ms) / statistics.median(f_ms),
+                   "note": "gather + GEMM per chunk (s-th sub-block of every shard), chunks "
+                           "round-robin over 4 streams; L2 flushed between calls"}
+
+    # ---------------- hot L2: back-to-back calls, no flush (reported beside the
+    # flushed headline; not part of `value`)
+    hot = {"fused": [], "barrier": []}
+    for name, fn in (("fused", fused), ("barrier", barrier)):
+        h_ev = [(ev(), ev()) for _ in range(20)]
+        fn()
+        for s_, e_ in h_ev:
+            s_.record(stream)
+            fn()
+            e_.record(stream)
+        torch.cuda.synchronize()
+        hot[name] = [s_.elapsed_time(e_) for s_, e_ in h_ev]
+
     # ---------------- end to end through the public API from pinned host memory
     e2e = None
     if not args.no_e2e:
@@ -434,12 +498,18 @@ def main():
             "speedup_vs_barrier": t_b / t_f,
             "fused_us_median": statistics.median(f_ms) * 1e3,
             "barrier_us_median": statistics.median(b_ms) * 1e3,
+            "fused_us_p10_p90": [pct(f_ms, 10) * 1e3, pct(f_ms, 90) * 1e3],
+            "barrier_us_p10_p90": [pct(b_ms, 10) * 1e3, pct(b_ms, 90) * 1e3],
+            "chunked_pipeline": chunked,
+            "hot_l2": {"fused_us_median": statistics.median(hot["fused"]) * 1e3,
+                       "barrier_us_median": statistics.median(hot["barrier"]) * 1e3,
+                       "note": "20 back-to-back calls each, no flush"},
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "clocks": clocks,
             "gpu_launches": args.steps * 3,
-            "gpu_launches_note": "per step: 1 fused kernel + 2 barrier-baseline kernels",
+            "gpu_launches_note": "per timed step: 1 fused kernel + 2 barrier-baseline kernels",
         }
         print(json.dumps(line), flush=True)
     if world > 1:

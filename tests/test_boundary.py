@@ -128,6 +128,24 @@ def test_m_contiguous_needs_m_multiple_of_8(lib, fused):
     assert _call(lib, fused, D=3, m=3, opt=opts(layout=1)) == UNSUPPORTED
 
 
+def _chunked(lib, chunks, opt=None, D=2, m=128, K=256, N=256, b=BASE + (1 << 30)):
+    arr = (ctypes.c_void_p * D)(*[ctypes.c_void_p(BASE + (r << 24)) for r in range(D)])
+    o = opt if opt is not None else agmm.default_options()
+    return lib.ag_chunked_matmul_ex(arr, D, m, K, ctypes.c_void_p(b), N, None,
+                                    ctypes.c_void_p(BASE + (2 << 30)),
+                                    ctypes.c_void_p(BASE + (3 << 30)), None, ctypes.byref(o),
+                                    chunks)
+
+
+def test_chunked_pipeline_arguments_are_checked_before_cuda(lib):
+    assert _chunked(lib, 0) == INVALID
+    assert _chunked(lib, -3) == INVALID
+    assert _chunked(lib, 4097) == INVALID
+    assert _chunked(lib, 4, b=0) == INVALID
+    assert _chunked(lib, 4, K=250) == INVALID
+    assert _chunked(lib, 4, opt=opts(layout=1)) == UNSUPPORTED  # k-contiguous only
+
+
 def test_valid_call_without_a_gpu_reports_cuda_not_a_crash(lib):
     import torch
     if torch.cuda.is_available():

@@ -134,6 +134,18 @@ def test_iris_m16384_both_layouts(oracle_mod):
     assert_bitwise(o_bm, o_b, "out barrier m_contiguous vs barrier k_contiguous")
 
 
+@pytest.mark.parametrize("layout", ["k_contiguous", "m_contiguous"])
+def test_output_sharded_slice(oracle_mod, layout):
+    """Output-sharded form: one rank's N/8 column slice of the M=16384 problem
+    (b column-sharded) through the same entry points; the gather is the full
+    one, the GEMM eight times smaller."""
+    w = inp.iris_m16384_colshard()
+    x = inp.make_inputs(w)
+    (a_f, o_f), (a_b, o_b) = run_both(x, layout=layout)
+    check(oracle_mod, x, a_f, o_f, sample_rows(w, 24, seed=448), what=f"colshard {layout}",
+          more=((a_b, o_b, f"barrier colshard {layout}"),))
+
+
 def test_iris_m4096_bias_m_contiguous(oracle_mod):
     w = inp.iris_m4096_bias()
     x = inp.make_inputs(w)
@@ -241,6 +253,30 @@ def test_barrier_small_grids_odd_row_blocks(oracle_mod, num_sms, layout):
     a_b, o_b = agmm.ag_then_matmul(shards, b, bias, layout=layout, num_sms=num_sms)
     assert agmm.device_error() == (0, 0)
     check(oracle_mod, x, a_b, o_b, what=f"barrier num_sms={num_sms} {layout}")
+
+
+@pytest.mark.parametrize("name,chunks", [("two_shard", 1), ("two_shard", 3), ("ragged", 4),
+                                         ("cube_1280", 4), ("m1024_d8", 8), ("m16384_d8", 4)])
+def test_chunked_pipeline(oracle_mod, name, chunks):
+    """The chunked pipeline (chunk s = the s-th sub-block of every shard,
+    gathered then multiplied, chunks round-robin over four streams) gives
+    a_gathered bitwise and the barrier's out bitwise (same GEMM core and k
+    order), which the oracle checks on sampled rows."""
+    w = {"two_shard": inp.small_two_shard(), "cube_1280": inp.cube(1280),
+         "m1024_d8": inp.iris_m1024(8), "m16384_d8": inp.iris_m16384(),
+         "ragged": inp.Workload("ragged_chunk", D=3, m_per_shard=37, K=200, N=136, dtype="bf16",
+                                a_dist="uniform", b_dist="uniform", b_scale="one",
+                                bias=True)}[name]
+    x = inp.make_inputs(w)
+    shards, b, bias = to_device(x)
+    a_c, o_c = agmm.ag_chunked_matmul(shards, b, bias, chunks=chunks)
+    a_b, o_b = agmm.ag_then_matmul(shards, b, bias)
+    torch.cuda.synchronize()
+    assert agmm.device_error() == (0, 0)
+    assert_bitwise(a_c, a_b, "chunked a_gathered")
+    assert_bitwise(o_c, o_b, "chunked out vs barrier")
+    rows = None if w.M <= 1024 else sample_rows(w, 16, seed=chunks)
+    check(oracle_mod, x, a_c, o_c, rows, what=f"chunked {name} S={chunks}")
 
 
 def test_repeat_calls_are_deterministic():
