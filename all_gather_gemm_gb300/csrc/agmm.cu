@@ -321,6 +321,31 @@ int plan_launch(GemmParams& p, const Shape& s, int cap, int pair_clusters, bool 
   return std::max(1, std::min(units, sched.num_mb * s.num_nb)) << p.pair;
 }
 
+// A 3-D view of D equal row segments, `rows` x `inner` each, `seg_stride`
+// rows apart: dims {inner, rows, D}; box {box_inner, box_rows, 1}; 128-byte
+// swizzle.  Not cached (the chunked pipeline encodes one per chunk).
+int make_map3(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t D,
+              uint64_t seg_stride, uint32_t box_inner, uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) {
+    snprintf(t_cuda_msg, sizeof t_cuda_msg, "cuTensorMapEncodeTiled entry point unavailable");
+    return AG_ERR_CUDA;
+  }
+  cuuint64_t dims[3] = {inner, rows, D};
+  cuuint64_t strides[2] = {inner * 2, seg_stride * inner * 2};
+  cuuint32_t box[3] = {box_inner, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(t_cuda_msg, sizeof t_cuda_msg, "cuTensorMapEncodeTiled (3-D) failed (CUresult %d)",
+             (int)r);
+    return AG_ERR_CUDA;
+  }
+  return AG_OK;
+}
+
 // pair: clusters of two CTAs (grid even), the kernel's CTA-pair variant.
 template <int kMode, bool kPair>
 int launch(int grid, cudaStream_t stream, const GemmParams& p, const char* what) {
@@ -557,28 +582,36 @@ namespace {
 // A is taken as [S, D, m/S, K] (S chunks, D shards): chunk s is the s-th
 // sub-block of every shard, local rows [s*m/S, (s+1)*m/S).  For each chunk,
 // round-robin over four streams: gather the chunk (every shard contributes),
-// then multiply its D row segments (the barrier GEMM core, k ascending, one
-// launch per segment).  The caller's stream forks to the chunk streams and
-// joins back.
+// then multiply its D row segments in one launch of the barrier GEMM core
+// (k ascending).  The caller's stream forks to the chunk streams and joins
+// back.
 
-// One barrier-core GEMM on rows [r0, r1) of a_gathered into the same rows of out.
-int gemm_rows(DevState& ds, const Shape& s, int r0, int r1, const void* a_gathered, const void* b,
-              const void* bias, void* out, int cap, const ag_options& o, uint64_t epoch,
-              int64_t timeout, cudaStream_t stream) {
+// One barrier-core GEMM over D row segments of a_gathered -- rows
+// [d*m_per_shard + lo, d*m_per_shard + hi) for every d -- into the same rows
+// of out: A and out as 3-D views {K or N, hi - lo, D}, each segment padded to
+// whole row blocks (rows past a segment's end load as zeros and are not
+// stored).
+int gemm_segments(DevState& ds, const Shape& s, int lo, int hi, const void* a_gathered,
+                  const void* b, const void* bias, void* out, int cap, const ag_options& o,
+                  uint64_t epoch, int64_t timeout, cudaStream_t stream) {
+  const int seg_rows = hi - lo;
+  const int seg_blocks = (seg_rows + kBM - 1) / kBM;
   Shape sc = s;
-  sc.M = r1 - r0;
-  sc.num_mb = (r1 - r0 + kBM - 1) / kBM;
-  const uint16_t* a_rows = static_cast<const uint16_t*>(a_gathered) + (int64_t)r0 * s.K;
-  uint16_t* out_rows = static_cast<uint16_t*>(out) + (int64_t)r0 * s.N;
+  sc.num_mb = s.D * seg_blocks;
+  sc.M = (int64_t)sc.num_mb * kBM;
+  const uint16_t* a_base = static_cast<const uint16_t*>(a_gathered) + (int64_t)lo * s.K;
+  uint16_t* out_base = static_cast<uint16_t*>(out) + (int64_t)lo * s.N;
   GemmParams p;
   memset(&p, 0, sizeof p);
   int st;
-  if ((st = make_map(&p.tm_a, a_rows, (uint64_t)s.K, (uint64_t)sc.M, kBK, kBM)) != AG_OK) return st;
-  if ((st = make_map(&p.tm_b, b, (uint64_t)s.N, (uint64_t)s.K, 64, kBK)) != AG_OK) return st;
-  if ((st = make_map(&p.tm_out, out_rows, (uint64_t)s.N, (uint64_t)sc.M, kEpiCols, kEpiRows)) !=
-      AG_OK)
+  if ((st = make_map3(&p.tm_a, a_base, (uint64_t)s.K, (uint64_t)seg_rows, (uint64_t)s.D,
+                      (uint64_t)s.mps, kBK, kBM)) != AG_OK)
     return st;
-  p.a_gathered = const_cast<uint16_t*>(a_rows);
+  if ((st = make_map(&p.tm_b, b, (uint64_t)s.N, (uint64_t)s.K, 64, kBK)) != AG_OK) return st;
+  if ((st = make_map3(&p.tm_out, out_base, (uint64_t)s.N, (uint64_t)seg_rows, (uint64_t)s.D,
+                      (uint64_t)s.mps, kEpiCols, kEpiRows)) != AG_OK)
+    return st;
+  p.a_gathered = const_cast<uint16_t*>(a_base);
   p.bias = static_cast<const float*>(bias);
   p.err = ds.err;
   p.epoch = epoch;
@@ -588,12 +621,14 @@ int gemm_rows(DevState& ds, const Shape& s, int r0, int r1, const void* a_gather
   p.M = (int)sc.M;
   p.N = s.N;
   p.K = s.K;
-  p.D = 1;
+  p.D = s.D;
   p.mps = (int)sc.M;
   p.num_mb = sc.num_mb;
   p.num_nb = sc.num_nb;
   p.num_kb = sc.num_kb;
   p.sh_log2 = 3;
+  p.seg_blocks = seg_blocks;
+  p.seg_rows = seg_rows;
   p.fp16 = o.dtype == AG_DTYPE_FP16 ? 1 : 0;
   p.inject_skip_flag = -1;
   const int grid = plan_launch(p, sc, cap, ds.pair_clusters, false, false, o.k_per_flag, 0);
@@ -637,7 +672,9 @@ int run_chunked(const void** a_shards, int D, int m_per_shard, int K, const void
   const uint64_t epoch = g_epoch.fetch_add(1) + 1;
   const int64_t timeout = o.timeout_ns ? o.timeout_ns : kDefaultTimeoutNs;
   const int cap = o.num_sms ? std::min(o.num_sms, ds.sms) : ds.sms;
-  const int S = std::min(chunks, m_per_shard);  // every sub-block has a row
+  // Sub-blocks shorter than a 128-row tile would be padded to one (wasted
+  // MMA work), so S is at most m_per_shard / 128 (at least 1).
+  const int S = std::max(1, std::min(chunks, m_per_shard / kBM));
   const int used = std::min(S, DevState::kChunkStreams);
   AG_CK(cudaEventRecord(ds.fork_ev, stream));
   for (int i = 0; i < used; ++i) AG_CK(cudaStreamWaitEvent(ds.cstream[i], ds.fork_ev, 0));
@@ -663,12 +700,9 @@ int run_chunked(const void** a_shards, int D, int m_per_shard, int K, const void
     agmm_gather_kernel<<<dim3(gx, D), 256, 0, cs>>>(gp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "gather kernel launch (chunk)");
-    for (int d = 0; d < D; ++d) {
-      const int r0 = d * m_per_shard + lo, r1 = d * m_per_shard + hi;
-      if ((st = gemm_rows(ds, s, r0, r1, a_gathered, b, bias, out, cap, o, epoch, timeout, cs)) !=
-          AG_OK)
-        return st;
-    }
+    if ((st = gemm_segments(ds, s, lo, hi, a_gathered, b, bias, out, cap, o, epoch, timeout, cs)) !=
+        AG_OK)
+      return st;
   }
   for (int i = 0; i < used; ++i) {
     AG_CK(cudaEventRecord(ds.join_ev[i], ds.cstream[i]));

@@ -152,6 +152,8 @@ struct GemmParams {
   int ng;                   // column blocks per schedule pass
   int w0;                   // column blocks of the first pass (they own the chunks)
   int sh_log2;              // log2 of the rows of a tm_shard8 box (3..6; divides m_per_shard)
+  int seg_blocks;           // barrier GEMM over row segments (0: off): tm_a / tm_out are 3-D
+  int seg_rows;             // [.., seg_rows, segments]; row block mb = segment mb / seg_blocks
   int fp16;                 // 1: fp16, 0: bf16
   int inject_skip_flag;     // this flag index is never published (fault injection)
 };
@@ -289,6 +291,7 @@ __device__ __forceinline__ int chunk_boxes(const GemmParams& p, int g) {
 // Per-tile facts the TMA issuer needs for every chunk, computed once per tile.
 struct TileCtx {
   int mb, nb;
+  int sd, sy;      // segmented barrier GEMM: segment and first row of the block in it
   int kind;        // BlockKind (kDirect for the barrier-path GEMM)
   int r0;          // shard holding the block's first row
   bool one_shard;  // every row of the block lies in shard r0
@@ -304,6 +307,10 @@ __device__ __forceinline__ void tile_ctx(const GemmParams& p, int t, TileCtx& c)
   // block reading the same A k-block at about the same time.
   c.ws = kFused ? chunk_start(p, c.nb) : 0;
   c.we = kFused ? chunk_end(p, c.nb) : 0;
+  if (!kFused && p.seg_blocks) {
+    c.sd = c.mb / p.seg_blocks;
+    c.sy = (c.mb - c.sd * p.seg_blocks) * kBM;
+  }
   if (c.mb >= p.num_mb) {
     c.kind = kEmpty;
     c.r0 = 0;
@@ -821,6 +828,8 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
           } else if (kLayoutM) {
             tma_load_2d(a_dst, &p.tm_a_mk, &full[stage], mb * kBM, kb * kBK);
             tma_load_2d(a_dst + kMnChunkBytes, &p.tm_a_mk, &full[stage], mb * kBM + 64, kb * kBK);
+          } else if (!kFused && p.seg_blocks) {
+            tma_load_3d(a_dst, &p.tm_a, &full[stage], kb * kBK, cur.sy, cur.sd);
           } else {
             tma_load_2d(a_dst, &p.tm_a, &full[stage], kb * kBK, mb * kBM);
           }
@@ -990,7 +999,12 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
       if (!__all_sync(0xffffffffu, ok)) break;
       tcgen05_fence_after_sync();
       const uint64_t t0 = p.trace ? globaltimer_ns() : 0;
-      const int m0 = mb * kBM + q * kEpiRows;
+      int m0 = mb * kBM + q * kEpiRows, sd = 0, m_end = p.M;
+      if (!kFused && p.seg_blocks) {  // segmented: rows within segment sd
+        sd = mb / p.seg_blocks;
+        m0 = (mb - sd * p.seg_blocks) * kBM + q * kEpiRows;
+        m_end = sd < p.D ? p.seg_rows : 0;  // (a pair's half past the last segment)
+      }
       const int n_tile = nb * kBN;
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kBN);
 #pragma unroll 1
@@ -1027,7 +1041,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
           packed[i] = pack2(v0, v1, p.fp16);
           packed[16 + i] = pack2(w0, w1, p.fp16);
         }
-        const bool store = (m0 < p.M) && (n0 < p.N);
+        const bool store = (m0 < m_end) && (n0 < p.N);
         const int eb = chunk_count & 1;
         if (lane == 0) bulk_wait_group_read<kEpiBufs - 1>();
         __syncwarp();
@@ -1038,7 +1052,12 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
                        packed[4 * ch + 2], packed[4 * ch + 3]);
         fence_proxy_async_shared();
         __syncwarp();
-        if (lane == 0 && store) tma_store_2d(&p.tm_out, my_bufs + eb * kEpiBufBytes, n0, m0);
+        if (lane == 0 && store) {
+          if (!kFused && p.seg_blocks)
+            tma_store_3d(&p.tm_out, my_bufs + eb * kEpiBufBytes, n0, m0, sd);
+          else
+            tma_store_2d(&p.tm_out, my_bufs + eb * kEpiBufBytes, n0, m0);
+        }
         if (lane == 0) bulk_commit_group();
         ++chunk_count;
       }

@@ -154,12 +154,13 @@ int ag_then_matmul_ex(const void** a_shards, int D, int m_per_shard, int K, cons
  * stream-pipelined AG+GEMM of "Lower distributed matmul to pipelined
  * algorithm for fine-grained overlap: AG+GEMM layout" (NVIDIA/Fuser #3695,
  * section "What"): A is taken as [S, D, m_per_shard / S, K] with S = `chunks`
- * (at most m_per_shard), so chunk s is the s-th sub-block of every shard
+ * (at most m_per_shard / 128, at least 1: a shorter sub-block would be padded
+ * to a 128-row tile), so chunk s is the s-th sub-block of every shard
  * (local rows [s*m/S, (s+1)*m/S)).  Chunk by chunk, round-robin over four
  * library-owned streams that fork from and join back to `stream`: gather the
  * chunk into a_gathered (every shard contributes), then multiply its D row
- * segments into the same rows of out (the barrier GEMM core, one launch per
- * segment).  A chunk's GEMMs wait for the chunk's whole gather; different
+ * segments into the same rows of out (one launch of the barrier GEMM core over
+ * the D segments).  A chunk's GEMMs wait for the chunk's whole gather; different
  * chunks overlap.  Results equal ag_then_matmul_ex's bitwise (same GEMM core
  * and k order).  Arguments and errors as for ag_then_matmul_ex; chunks < 1 or
  * > 4096 is AG_ERR_INVALID_ARG, the m-contiguous layout AG_ERR_UNSUPPORTED.

@@ -256,7 +256,8 @@ def test_barrier_small_grids_odd_row_blocks(oracle_mod, num_sms, layout):
 
 
 @pytest.mark.parametrize("name,chunks", [("two_shard", 1), ("two_shard", 3), ("ragged", 4),
-                                         ("cube_1280", 4), ("m1024_d8", 8), ("m16384_d8", 4)])
+                                         ("cube_1280", 4), ("m1024_d8", 8), ("m16384_d8", 4),
+                                         ("uneven", 3), ("uneven", 64)])
 def test_chunked_pipeline(oracle_mod, name, chunks):
     """The chunked pipeline (chunk s = the s-th sub-block of every shard,
     gathered then multiplied, chunks round-robin over four streams) gives
@@ -266,7 +267,11 @@ def test_chunked_pipeline(oracle_mod, name, chunks):
          "m1024_d8": inp.iris_m1024(8), "m16384_d8": inp.iris_m16384(),
          "ragged": inp.Workload("ragged_chunk", D=3, m_per_shard=37, K=200, N=136, dtype="bf16",
                                 a_dist="uniform", b_dist="uniform", b_scale="one",
-                                bias=True)}[name]
+                                bias=True),
+         # 640-row shards in 3 (or, capped, 5) chunks: 213/213/214-row sub-blocks,
+         # each padded to 2 row blocks
+         "uneven": inp.Workload("uneven_chunk", D=3, m_per_shard=640, K=512, N=392,
+                                dtype="fp16", bias=True)}[name]
     x = inp.make_inputs(w)
     shards, b, bias = to_device(x)
     a_c, o_c = agmm.ag_chunked_matmul(shards, b, bias, chunks=chunks)
