@@ -297,6 +297,8 @@ def main():
     ap.add_argument("--reference-rows", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-chunked", action="store_true",
+                    help="skip the chunked-pipeline comparison (profiling runs)")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the bench line: fused vs barrier on every workload of the "
                          "parity configs, one JSON line each")
@@ -390,7 +392,7 @@ def main():
     # ---------------- chunked pipeline (k-contiguous only): the third comparison
     # point, timed like the headline (flushed, per call) but outside its region
     chunked = None
-    if args.layout == "k_contiguous":
+    if args.layout == "k_contiguous" and not args.no_chunked:
         a_g3 = torch.empty((w.M, w.K), dtype=b.dtype, device="cuda")
         out3 = torch.empty((w.M, w.N), dtype=b.dtype, device="cuda")
 
