@@ -70,6 +70,23 @@ def load_peaks():
         return 1900.0, 1700.0, 6800.0, "fallback"
 
 
+def max_over_ranks(values, world: int, device="cuda"):
+    """Element-wise maximum over ranks of this rank's timings (every rank calls
+    it with its own list; the slowest rank sets the job's time)."""
+    if world == 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_tflops(flops_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job throughput: every rank's work over the slowest rank's time."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
+
+
 def pct(xs, q):
     """q-th percentile (linear interpolation between order statistics)."""
     v = sorted(xs)
@@ -382,12 +399,7 @@ def main():
         raise SystemExit(f"device error {code} info {info:#x} in the timed region")
     f_ms = [s.elapsed_time(e) for s, e in f_ev]
     b_ms = [s.elapsed_time(e) for s, e in b_ev]
-    t_f = sum(f_ms) / len(f_ms)
-    t_b = sum(b_ms) / len(b_ms)
-    if world > 1:
-        tt = torch.tensor([t_f, t_b], device="cuda", dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_f, t_b = tt.tolist()
+    t_f, t_b = max_over_ranks([sum(f_ms) / len(f_ms), sum(b_ms) / len(b_ms)], world)
 
     # ---------------- chunked pipeline (k-contiguous only): the third comparison
     # point, timed like the headline (flushed, per call) but outside its region
@@ -449,14 +461,10 @@ def main():
             h_out.copy_(out, non_blocking=True)
             e_ev[i][1].record(stream)
         barrier_sync()
-        t_e = statistics.mean(s.elapsed_time(e) for s, e in e_ev)
-        if world > 1:
-            tt = torch.tensor([t_e], device="cuda", dtype=torch.float64)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            t_e = tt.item()
+        t_e = max_over_ranks([statistics.mean(s.elapsed_time(e) for s, e in e_ev)], world)[0]
         h2d = sum(s.numel() * 2 for s in x.shards) + x.b.numel() * 2 + (
             x.bias.numel() * 4 if x.bias is not None else 0)
-        e2e = {"value": world * w.flops / (t_e * 1e-3) / 1e12, "unit": UNIT,
+        e2e = {"value": job_tflops(w.flops, world, t_e), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": w.M * w.N * 2,
                "ms_per_step": t_e}
 
@@ -478,7 +486,7 @@ def main():
     if rank == 0:
         line = {
             "metric": METRIC,
-            "value": world * w.flops / (t_f * 1e-3) / 1e12,
+            "value": job_tflops(w.flops, world, t_f),
             "unit": UNIT,
             "n_gpus": world,
             "steps": args.steps,
