@@ -922,9 +922,23 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
       constexpr uint32_t kM = kPair ? 2 * kBM : kBM;
       const uint32_t idesc_k = idesc_f16_f32(ab_bf16, 0, 1, kM, kBN);
       const uint32_t idesc_mn = idesc_f16_f32(ab_bf16, 1, 1, kM, kBN);
+      // A's major-ness: K-major for the k-contiguous layout, MN-major for the
+      // [K, M] staging; only the single-CTA fused m-contiguous kernel mixes
+      // the two (shard rows K-major), and reads it from the stage record.
+      constexpr int kAMajor = !kLayoutM ? 0 : (kFused && !kPair) ? 2 : 1;
       bool aborted = false;
       int stage = 0;
       uint32_t phase = 0;
+      // The MMA issue queue is shallow: whatever this thread waits on between
+      // two stages' MMAs idles the tensor pipe.  So the next stage's barriers
+      // are tested (without blocking) before this stage's MMAs are issued,
+      // and the result is used after them; a blocking wait happens only when
+      // that stage had not landed yet.  A completed phase stays completed
+      // until the stage is refilled, which needs this thread's commit, so a
+      // positive test also holds across a tile boundary.
+      bool ready = false;  // stage `stage` (phase `phase`) is known to have landed
+      const int total = my_tiles * p.num_kb;
+      int done = 0;
       for (int j = 0; j < my_tiles && !aborted; ++j) {
         const int buf = j & 1;
         const uint32_t use = (uint32_t)(j >> 1);
@@ -934,14 +948,22 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
         }
         tcgen05_fence_after_sync();
         const uint32_t d_tmem = tmem_base + (uint32_t)(buf * kBN);
-        for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (!wait_bar(p, &full[stage], phase, abort_flag, kSiteFull) ||
-              (kPair && !wait_bar<true>(p, &pfull[stage], phase, abort_flag, kSiteFull))) {
+        for (int kb = 0; kb < p.num_kb; ++kb, ++done) {
+          if (!ready && (!wait_bar(p, &full[stage], phase, abort_flag, kSiteFull) ||
+                         (kPair && !wait_bar<true>(p, &pfull[stage], phase, abort_flag, kSiteFull)))) {
             aborted = true;
             break;
           }
           tcgen05_fence_after_sync();
-          const bool a_mn = (info[stage] & kInfoAmn) != 0;
+          const int s1 = stage + 1 == kStages ? 0 : stage + 1;
+          const uint32_t ph1 = stage + 1 == kStages ? phase ^ 1u : phase;
+          const bool more = done + 1 < total;
+          bool t_full = false, t_pfull = true;
+          if (more) {
+            t_full = mbar_test_wait(&full[s1], ph1);
+            if constexpr (kPair) t_pfull = mbar_test_wait_cluster(&pfull[s1], ph1);
+          }
+          const bool a_mn = kAMajor == 2 ? (info[stage] & kInfoAmn) != 0 : kAMajor == 1;
           const uint32_t idesc = a_mn ? idesc_mn : idesc_k;
           const uint32_t a_addr = smem_u32(smem + stage * kStageBytes);
           const uint32_t b_addr = a_addr + kAStageBytes;
@@ -962,10 +984,9 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
             umma_commit_pair_mc(&empty[stage], 3);  // frees the stage in both CTAs
           else
             umma_commit(&empty[stage]);
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          stage = s1;
+          phase = ph1;
+          ready = more && t_full && t_pfull;
         }
         if (aborted) break;
         if constexpr (kPair)
