@@ -78,8 +78,14 @@ enum Mode : int { kGemmK = 0, kGemmM = 1, kFusedK = 2, kFusedM = 3 };
 
 __host__ __device__ constexpr bool mode_fused(int m) { return m >= kFusedK; }
 __host__ __device__ constexpr bool mode_layout_m(int m) { return m == kGemmM || m == kFusedM; }
+// Warp roles: 0 A loads (and, fused, the ready-flag protocol), 1 MMA (pair
+// peer: relay), 2..5 epilogue, 6 B loads; fused: 7 register fetcher, 8..11
+// copiers.
+constexpr int kBWarp = 2 + kEpiWarps;
+constexpr int kRegWarp = 3 + kEpiWarps;
+constexpr int kCopyWarp0 = 4 + kEpiWarps;
 __host__ __device__ constexpr int mode_threads(int m) {
-  return 32 * (2 + kEpiWarps + (mode_fused(m) ? 1 + kCopyWarps : 0));
+  return 32 * (3 + kEpiWarps + (mode_fused(m) ? 1 + kCopyWarps : 0));
 }
 
 // Bits of a stage's record (read by the MMA warp once the stage is full) and
@@ -589,7 +595,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], 2);  // the A and the B loads of the stage
       mbar_init(&empty[s], 1);  // the MMA commit (pair: multicast to both CTAs)
       if (kPair) mbar_init(&pfull[s], 1);
     }
@@ -803,8 +809,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
           }
           info[stage] = bits;
           uint8_t* a_dst = smem + stage * kStageBytes;
-          uint8_t* b_dst = a_dst + kAStageBytes;
-          mbar_arrive_expect_tx(&full[stage], kStageBytes);
+          mbar_arrive_expect_tx(&full[stage], kAStageBytes);
           if (direct) {
             if (one_shard) {
               tma_load_2d(a_dst, &p.tm_shard[r0], &full[stage], kb * kBK, mb * kBM - r0 * p.mps);
@@ -833,11 +838,6 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
           } else {
             tma_load_2d(a_dst, &p.tm_a, &full[stage], kb * kBK, mb * kBM);
           }
-          // this CTA's columns of the tile's B (pair: the rank's half)
-#pragma unroll
-          for (int q = 0; q < P::kBCols / 64; ++q)
-            tma_load_2d(b_dst + q * kMnChunkBytes, &p.tm_b, &full[stage],
-                        nb * kBN + (int)rank * P::kBCols + q * 64, kb * kBK);
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           ++seq;
@@ -1087,7 +1087,58 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
     }
     if (lane == 0) bulk_wait_group<0>();
     __syncwarp();
-  } else if (kFused && warp == 2 + kEpiWarps) {
+  } else if (warp == kBWarp) {
+    // ---------------------------------------------------------- B loader
+    // The tile's B k-blocks in the A issuer's order (owned window first):
+    // one thread issuing both operands' loads could not keep up with the
+    // tensor pipe.  Each loader arrives on `full` for its own bytes.
+    if (lane == 0) {
+      uint32_t issued_mask = 0, issued_parity = 0;
+      bool aborted = false;
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int t = blockIdx.x; t < p.num_tiles && !aborted; t += gridDim.x) {
+        int mb, nb;
+        tile_coords(p, t, mb, nb);
+        const int ws = kFused ? chunk_start(p, nb) : 0;
+        const int we = kFused ? chunk_end(p, nb) : 0;
+        const int n0 = nb * kBN + (int)rank * P::kBCols;  // this CTA's columns (pair: the rank's half)
+        for (int gi = 0; gi < p.G && !aborted; ++gi) {
+          const int g = chunk_at(gi, ws, we);
+          const int nbox = chunk_boxes(p, g);
+          for (int j = 0; j < nbox; ++j) {
+            const int kb = g * p.kpf + j;
+            if (!wait_bar(p, &empty[stage], phase ^ 1u, abort_flag, kSiteEmpty)) {
+              aborted = true;
+              break;
+            }
+            uint8_t* b_dst = smem + stage * kStageBytes + kAStageBytes;
+            mbar_arrive_expect_tx(&full[stage], P::kBStageBytes);
+#pragma unroll
+            for (int q = 0; q < P::kBCols / 64; ++q)
+              tma_load_2d(b_dst + q * kMnChunkBytes, &p.tm_b, &full[stage], n0 + q * 64, kb * kBK);
+            issued_mask |= 1u << stage;
+            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+      if (aborted || *abort_flag) {
+        // Let every issued load land before shared memory is released.
+        for (int s = 0; s < kStages; ++s)
+          if (issued_mask & (1u << s)) {
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(&full[s], (issued_parity >> s) & 1u) &&
+                   globaltimer_ns() - t0 < 1000000000ull) {
+            }
+          }
+      }
+    }
+    __syncwarp();
+  } else if (kFused && warp == kRegWarp) {
     // ---------------------------------------------------------- register fetcher
     regfetch_loop(p, lane, kLayoutM);
     __syncwarp();
@@ -1103,7 +1154,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
     // boxes of a chunk then adds one to the record's done count (acq_rel, CTA
     // scope); the one that completes it publishes the chunk (release, GPU
     // scope), so the flag follows every copier's writes.
-    const int w = warp - (3 + kEpiWarps);
+    const int w = warp - kCopyWarp0;
     const int ch = lane & 7;  // 16-byte column chunk of a 128-byte box row
     for (uint32_t n = 0;; ++n) {
       const int slot = (int)(n % kRing);
