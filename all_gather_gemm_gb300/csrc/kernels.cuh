@@ -698,7 +698,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
           st_relaxed_gpu(p.started + t, p.epoch);
         }
         const int g = chunk_at(gi, cur.ws, cur.we);
-        const int mb = cur.mb, nb = cur.nb;
+        const int mb = cur.mb;
         const int flag_idx = mb * p.G + g;
         const int nbox = g == p.G - 1 ? last_nbox : p.kpf;
         const int kind = cur.kind;
