@@ -112,8 +112,8 @@ struct Pipe {
   static constexpr int kStageBytes = kAStageBytes + kBStageBytes;
   static constexpr int kData = kStages * kStageBytes + kEpiWarps * kEpiBufs * kEpiBufBytes;
   // full, empty [kStages]; tmem_full, tmem_empty [2]; drain; rfull, rfree
-  // [kRing]; pair: pfull [kStages] (the peer's stage landed)
-  static constexpr int kBars = 2 * kStages + 4 + 1 + 2 * kRing + (kPair ? kStages : 0);
+  // [kRing]
+  static constexpr int kBars = 2 * kStages + 4 + 1 + 2 * kRing;
   static constexpr int kSmemBytes =
       1024 + kData + 8 * kBars + 4 * kStages + 4 * kRing * kRingWords + 16 + 64;
   static_assert(kSmemBytes <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
@@ -551,12 +551,60 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, int fp16) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// A stage's tiled loads: counted on this CTA's `full` barrier, or (CTA pair)
+// on the leader's, whose shared::cluster address is bar_c.
+template <bool kPair>
+__device__ __forceinline__ void stage_load_2d(void* dst, const CUtensorMap* m, uint64_t* bar,
+                                              uint32_t bar_c, int32_t x, int32_t y) {
+  if constexpr (kPair)
+    tma_load_2d_pair(dst, m, bar_c, x, y);
+  else
+    tma_load_2d(dst, m, bar, x, y);
+}
+
+template <bool kPair>
+__device__ __forceinline__ void stage_load_3d(void* dst, const CUtensorMap* m, uint64_t* bar,
+                                              uint32_t bar_c, int32_t x, int32_t y, int32_t z) {
+  if constexpr (kPair)
+    tma_load_3d_pair(dst, m, bar_c, x, y, z);
+  else
+    tma_load_3d(dst, m, bar, x, y, z);
+}
+
+// After an abort: let this thread's issued loads land before the CTA (and
+// its shared memory) goes away.  Waits on the stages' `full` phases, bounded;
+// the pair's peer cannot observe its loads (they count on the leader's
+// barriers) and waits a fixed 200 us instead, far above a load's latency.
+template <bool kPair>
+__device__ __forceinline__ void drain_loads(uint64_t* full, uint32_t issued_mask,
+                                            uint32_t issued_parity, uint32_t rank) {
+  if (kPair && rank != 0) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 200000ull) {
+    }
+    return;
+  }
+  constexpr int kStages = Pipe<kPair>::kStages;
+  for (int s = 0; s < kStages; ++s)
+    if (issued_mask & (1u << s)) {
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(&full[s], (issued_parity >> s) & 1u) &&
+             globaltimer_ns() - t0 < 1000000000ull) {
+      }
+    }
+}
+
 // ------------------------------------------------------------------ the kernel
 
 // kPair: launched in clusters of two CTAs; the even CTA (rank 0, the leader)
-// issues tcgen05.mma.cta_group::2 for the pair's 256 x 256 tile, the odd CTA
-// (the peer) relays "my stage has landed" to it, and both run their own TMA
-// issuer and epilogue for their own 128 rows.
+// issues tcgen05.mma.cta_group::2 for the pair's 256 x 256 tile.  Both CTAs
+// load their own 128 rows of A and half of B's columns into their own shared
+// memory, but every load of the pair counts its bytes on the LEADER's `full`
+// barrier (cta_group::2 loads), whose two arrivals (the leader's A and B
+// loaders) expect the bytes of both CTAs; the peer's `full` barriers are
+// unused.  A stage of the peer is refilled only after the MMA commit that
+// frees it (multicast to both CTAs' `empty`), which follows the completion of
+// the leader's phase, so no load of a new phase can land in an old one.
 template <int kMode, bool kPair>
 __global__ void __launch_bounds__(mode_threads(kMode), 1)
     agmm_gemm_kernel(const __grid_constant__ GemmParams p) {
@@ -581,8 +629,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
   uint64_t* drain = tmem_empty + 2;          // [1] final MMA drain
   uint64_t* rfull = drain + 1;               // [kRing] fused: chunk record written
   uint64_t* rfree = rfull + kRing;           // [kRing] fused: every copier is done with it
-  uint64_t* pfull = rfree + kRing;           // [kStages] pair, leader: the peer's stage landed
-  uint32_t* info = reinterpret_cast<uint32_t*>(pfull + (kPair ? kStages : 0));  // [kStages]
+  uint32_t* info = reinterpret_cast<uint32_t*>(rfree + kRing);  // [kStages]
   uint32_t* ring = info + kStages;                // [kRing][kRingWords] chunk records
   volatile uint32_t* iseq = ring + kRing * kRingWords;  // issuer progress (chunks), a liveness signal
   uint32_t* tmem_slot = ring + kRing * kRingWords + 1;
@@ -595,9 +642,8 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 2);  // the A and the B loads of the stage
+      mbar_init(&full[s], 2);  // the A and the B loader (pair: the leader's, for both CTAs' bytes)
       mbar_init(&empty[s], 1);  // the MMA commit (pair: multicast to both CTAs)
-      if (kPair) mbar_init(&pfull[s], 1);
     }
     for (int r = 0; r < kRing; ++r) {
       mbar_init(&rfull[r], 1);
@@ -627,6 +673,8 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
   if (kPair) cluster_sync();
   tcgen05_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  // Pair: the leader's `full` barriers, where both CTAs' loads count their bytes.
+  const uint32_t full_c = kPair ? mapa_shared(smem_u32(&full[0]), 0) : 0u;
 
   if (warp == 0) {
     // ---------------------------------------------------------- TMA issuer
@@ -809,10 +857,13 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
           }
           info[stage] = bits;
           uint8_t* a_dst = smem + stage * kStageBytes;
-          mbar_arrive_expect_tx(&full[stage], kAStageBytes);
+          const uint32_t bar_c = full_c + 8u * (uint32_t)stage;
+          if (!kPair || rank == 0)
+            mbar_arrive_expect_tx(&full[stage], kPair ? 2 * kAStageBytes : kAStageBytes);
           if (direct) {
             if (one_shard) {
-              tma_load_2d(a_dst, &p.tm_shard[r0], &full[stage], kb * kBK, mb * kBM - r0 * p.mps);
+              stage_load_2d<kPair>(a_dst, &p.tm_shard[r0], &full[stage], bar_c, kb * kBK,
+                                   mb * kBM - r0 * p.mps);
             } else {
               // Walk the row groups (2^sh_log2 rows, which divides both 128
               // and m_per_shard, so no group straddles a boundary) across the
@@ -822,7 +873,8 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
               int r = r0, lr = mb * kBM - r0 * p.mps;
 #pragma unroll 1
               for (int q = 0; q < (kBM >> p.sh_log2); ++q) {
-                tma_load_2d(a_dst + q * h * 128, &p.tm_shard8[r], &full[stage], kb * kBK, lr);
+                stage_load_2d<kPair>(a_dst + q * h * 128, &p.tm_shard8[r], &full[stage], bar_c,
+                                     kb * kBK, lr);
                 lr += h;
                 if (lr >= p.mps && r < p.D - 1) {
                   lr -= p.mps;
@@ -831,12 +883,13 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
               }
             }
           } else if (kLayoutM) {
-            tma_load_2d(a_dst, &p.tm_a_mk, &full[stage], mb * kBM, kb * kBK);
-            tma_load_2d(a_dst + kMnChunkBytes, &p.tm_a_mk, &full[stage], mb * kBM + 64, kb * kBK);
+            stage_load_2d<kPair>(a_dst, &p.tm_a_mk, &full[stage], bar_c, mb * kBM, kb * kBK);
+            stage_load_2d<kPair>(a_dst + kMnChunkBytes, &p.tm_a_mk, &full[stage], bar_c,
+                                 mb * kBM + 64, kb * kBK);
           } else if (!kFused && p.seg_blocks) {
-            tma_load_3d(a_dst, &p.tm_a, &full[stage], kb * kBK, cur.sy, cur.sd);
+            stage_load_3d<kPair>(a_dst, &p.tm_a, &full[stage], bar_c, kb * kBK, cur.sy, cur.sd);
           } else {
-            tma_load_2d(a_dst, &p.tm_a, &full[stage], kb * kBK, mb * kBM);
+            stage_load_2d<kPair>(a_dst, &p.tm_a, &full[stage], bar_c, kb * kBK, mb * kBM);
           }
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -885,36 +938,13 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
         ring[rslot * kRingWords] = kInfoEnd;
         mbar_arrive(&rfull[rslot]);
       }
-      if (aborted || *abort_flag) {
-        // Let every issued load land before shared memory is released.
-        for (int s = 0; s < kStages; ++s)
-          if (issued_mask & (1u << s)) {
-            const uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(&full[s], (issued_parity >> s) & 1u) &&
-                   globaltimer_ns() - t0 < 1000000000ull) {
-            }
-          }
-      }
+      if (aborted || *abort_flag) drain_loads<kPair>(full, issued_mask, issued_parity, rank);
     }
     __syncwarp();
   } else if (warp == 1 && kPair && rank != 0) {
-    // ---------------------------------------------------------- pair peer: relay
-    // The leader's MMA reads this CTA's stage too; tell it when the stage has
-    // landed, in fill order.  (This CTA cannot refill a stage before the
-    // leader's commit frees it, so no phase is skipped.)
-    if (lane == 0) {
-      const int total = my_tiles * p.num_kb;
-      for (int i = 0; i < total; ++i) {
-        const int s = i % kStages;
-        if (!wait_bar(p, &full[s], (uint32_t)(i / kStages) & 1u, abort_flag, kSiteFull)) break;
-        // Relaxed: this thread has already observed the stage complete (its
-        // bytes are in this CTA's shared memory); a release here would first
-        // wait for this CTA's later loads still in flight, and that cost the
-        // pair half its throughput.
-        mbar_arrive_remote_relaxed(mapa_shared(smem_u32(&pfull[s]), 0));
-      }
-    }
-    __syncwarp();
+    // ---------------------------------------------------------- pair peer
+    // Nothing to do: the leader issues the pair's MMAs, and this CTA's loads
+    // count their bytes on the leader's barriers themselves.
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
@@ -949,8 +979,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
         tcgen05_fence_after_sync();
         const uint32_t d_tmem = tmem_base + (uint32_t)(buf * kBN);
         for (int kb = 0; kb < p.num_kb; ++kb, ++done) {
-          if (!ready && (!wait_bar(p, &full[stage], phase, abort_flag, kSiteFull) ||
-                         (kPair && !wait_bar<true>(p, &pfull[stage], phase, abort_flag, kSiteFull)))) {
+          if (!ready && !wait_bar(p, &full[stage], phase, abort_flag, kSiteFull)) {
             aborted = true;
             break;
           }
@@ -958,11 +987,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
           const int s1 = stage + 1 == kStages ? 0 : stage + 1;
           const uint32_t ph1 = stage + 1 == kStages ? phase ^ 1u : phase;
           const bool more = done + 1 < total;
-          bool t_full = false, t_pfull = true;
-          if (more) {
-            t_full = mbar_test_wait(&full[s1], ph1);
-            if constexpr (kPair) t_pfull = mbar_test_wait_cluster(&pfull[s1], ph1);
-          }
+          const bool t_full = more && mbar_test_wait(&full[s1], ph1);
           const bool a_mn = kAMajor == 2 ? (info[stage] & kInfoAmn) != 0 : kAMajor == 1;
           const uint32_t idesc = a_mn ? idesc_mn : idesc_k;
           const uint32_t a_addr = smem_u32(smem + stage * kStageBytes);
@@ -986,7 +1011,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
             umma_commit(&empty[stage]);
           stage = s1;
           phase = ph1;
-          ready = more && t_full && t_pfull;
+          ready = t_full;
         }
         if (aborted) break;
         if constexpr (kPair)
@@ -1113,10 +1138,13 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
               break;
             }
             uint8_t* b_dst = smem + stage * kStageBytes + kAStageBytes;
-            mbar_arrive_expect_tx(&full[stage], P::kBStageBytes);
+            const uint32_t bar_c = full_c + 8u * (uint32_t)stage;
+            if (!kPair || rank == 0)
+              mbar_arrive_expect_tx(&full[stage], kPair ? 2 * P::kBStageBytes : P::kBStageBytes);
 #pragma unroll
             for (int q = 0; q < P::kBCols / 64; ++q)
-              tma_load_2d(b_dst + q * kMnChunkBytes, &p.tm_b, &full[stage], n0 + q * 64, kb * kBK);
+              stage_load_2d<kPair>(b_dst + q * kMnChunkBytes, &p.tm_b, &full[stage], bar_c,
+                                   n0 + q * 64, kb * kBK);
             issued_mask |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
             if (++stage == kStages) {
@@ -1126,16 +1154,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
           }
         }
       }
-      if (aborted || *abort_flag) {
-        // Let every issued load land before shared memory is released.
-        for (int s = 0; s < kStages; ++s)
-          if (issued_mask & (1u << s)) {
-            const uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(&full[s], (issued_parity >> s) & 1u) &&
-                   globaltimer_ns() - t0 < 1000000000ull) {
-            }
-          }
-      }
+      if (aborted || *abort_flag) drain_loads<kPair>(full, issued_mask, issued_parity, rank);
     }
     __syncwarp();
   } else if (kFused && warp == kRegWarp) {
