@@ -27,6 +27,7 @@ its own GPU; value = all ranks' FLOPs / the slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import math
@@ -112,8 +113,9 @@ def load_traffic(workload_name: str, layout: str):
 
 
 class ClockSampler:
-    """nvidia-smi samples during the timed region (SM clock, reasons)."""
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples (every 100 ms) around the timed region; the summary
+    keeps the samples whose timestamps fall inside it (mark_start/mark_end)."""
+    QUERY = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -121,6 +123,13 @@ class ClockSampler:
         self.index = index
         self.proc = None
         self.path = None
+        self.t0 = self.t1 = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
 
     def __enter__(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
@@ -162,6 +171,22 @@ class ClockSampler:
                 return float(x)
             except ValueError:
                 return None
+        def stamp(x):
+            try:
+                return datetime.datetime.strptime(x, "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                return None
+        total = len(rows)
+        window = "all samples (none inside the timed region)"
+        if self.t0 is not None and self.t1 is not None:
+            inside = []
+            for r in rows:
+                t = stamp(r[0])
+                if t is not None and self.t0 <= t <= self.t1:
+                    inside.append(r)
+            if inside:
+                rows = inside
+                window = "samples inside the timed region"
         sm = [num(r[1]) for r in rows if num(r[1]) is not None]
         smax = [num(r[2]) for r in rows if num(r[2]) is not None]
         power = [num(r[3]) for r in rows if num(r[3]) is not None]
@@ -170,7 +195,8 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
                 "power_w_max": max(power) if power else None,
-                "samples": len(rows), "reasons": reasons}
+                "samples": len(rows), "samples_total": total, "window": window,
+                "reasons": reasons}
 
 
 def headline_workload(name: str):
@@ -304,7 +330,7 @@ def run_sweep(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="m16384_d8")
@@ -383,6 +409,7 @@ def main():
     barrier_sync()
     with sampler:
         barrier_sync()
+        sampler.mark_start()
         for i in range(args.steps):
             flush.fill_(i)  # write 512 MB: evicts L2 (129 MB) between timed calls
             f_ev[i][0].record(stream)
@@ -393,6 +420,7 @@ def main():
             barrier()
             b_ev[i][1].record(stream)
         barrier_sync()
+        sampler.mark_end()
     clocks = sampler.summary()
     code, info = agmm.device_error()
     if code != 0:
