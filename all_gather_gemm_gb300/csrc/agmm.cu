@@ -177,8 +177,10 @@ size_t round_kib(size_t n) { return (n + 1023) & ~size_t(1023); }
 // Column blocks per schedule pass (see tile_coords).  A grid that runs every
 // tile in one wave gains nothing from passes; otherwise a pass keeps its
 // slice of b (K x 256 columns x 2 bytes per column block) near 32 MB so it
-// stays in L2 while A streams past (measured at M=16384, N=3584, K=8192:
-// 7 of 14 column blocks per pass was the fastest grouping).
+// stays in L2 while A streams past.  Measured at N=3584, K=8192 (8 of 14
+// column blocks per pass): at M=16384 it ties one pass and beats 4 or 7 per
+// pass (7 costs the m-contiguous kernel 6%); at M=4096 m-contiguous it beats
+// one pass by 5%.
 int schedule_group(const Shape& s, int sms) {
   if ((int64_t)s.num_mb * s.num_nb <= sms) return s.num_nb;
   const int64_t slice = (int64_t)s.K * kBN * 2;
