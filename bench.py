@@ -53,10 +53,15 @@ KERNEL_SOURCES = [os.path.join(ROOT, "all_gather_gemm_gb300", "csrc", f)
 
 
 def kernel_source_hash() -> str:
+    """Hash of the kernel and launch code with `//` comments, trailing blanks
+    and empty lines removed: edits to comments keep a capture valid."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f, encoding="utf-8") as fh:
+            for line in fh:
+                code = line.split("//", 1)[0].rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 
