@@ -11,6 +11,10 @@ library is missing, every call raises.
 D row shards of A, each its own allocation); ``b`` is [K, N] of the same
 dtype; ``bias`` an optional fp32 [N].  ``a_gathered`` = concat(shards) and
 ``out`` = a_gathered @ b (+ bias), computed with fp32 accumulation.
+
+FP8 (``torch.float8_e4m3fn`` shards): ``b`` is given transposed, [N, K] e4m3,
+``out`` is bf16 and ``out = scale_a * scale_b * (a_gathered @ b.T) + bias``
+(k-contiguous layout only).
 """
 from __future__ import annotations
 
@@ -28,7 +32,7 @@ __all__ = [
 STATUS = {0: "AG_OK", 1: "AG_ERR_INVALID_ARG", 2: "AG_ERR_UNSUPPORTED", 3: "AG_ERR_CUDA",
           4: "AG_ERR_TIMEOUT", 5: "AG_ERR_WORKSPACE", 6: "AG_ERR_TOO_LARGE"}
 LAYOUTS = {"k_contiguous": 0, "m_contiguous": 1}
-DTYPES = {"bf16": 0, "fp16": 1}
+DTYPES = {"bf16": 0, "fp16": 1, "fp8_e4m3": 2}
 EXPORTS = ("ag_options_default", "ag_matmul", "ag_then_matmul", "ag_matmul_ex",
            "ag_then_matmul_ex", "ag_workspace_size", "ag_get_device_error",
            "ag_release_workspace", "ag_status_string", "ag_num_sms", "ag_matmul_noalloc",
@@ -55,6 +59,8 @@ class AgOptions(ctypes.Structure):
         ("trace_words", ctypes.c_int64),
         ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_int64),
+        ("scale_a", ctypes.c_float),
+        ("scale_b", ctypes.c_float),
     ]
 
 
@@ -134,7 +140,9 @@ def _dtype_name(t) -> str:
         return "bf16"
     if t.dtype == torch.float16:
         return "fp16"
-    raise TypeError(f"unsupported dtype {t.dtype}; use bfloat16 or float16")
+    if t.dtype == getattr(torch, "float8_e4m3fn", None):
+        return "fp8_e4m3"
+    raise TypeError(f"unsupported dtype {t.dtype}; use bfloat16, float16 or float8_e4m3fn")
 
 
 def ag_matmul_raw(fused: bool, shard_ptrs, D, m_per_shard, K, b_ptr, N, bias_ptr, ag_ptr, out_ptr,
@@ -152,24 +160,34 @@ def ag_matmul_raw(fused: bool, shard_ptrs, D, m_per_shard, K, b_ptr, N, bias_ptr
 
 
 def _call(fused, shards, b, bias, a_gathered, out, stream, layout, rank, k_per_flag, num_sms,
-          timeout_ns, inject_skip_flag, trace, workspace, chunks=0):
+          timeout_ns, inject_skip_flag, trace, workspace, chunks=0, scale_a=1.0, scale_b=1.0):
     import torch
     if not shards:
         raise ValueError("need at least one shard")
     D = len(shards)
     m, K = shards[0].shape
-    K2, N = b.shape
     dt = _dtype_name(b)
+    fp8 = dt == "fp8_e4m3"
+    if fp8:
+        N, K2 = b.shape  # FP8: b is given transposed, [N, K]
+    else:
+        K2, N = b.shape
     for s in shards:
         if s.shape != (m, K) or s.dtype != b.dtype or not s.is_cuda or not s.is_contiguous():
             raise ValueError("shards must be contiguous CUDA tensors of one shape and b's dtype")
     if K2 != K or not b.is_cuda or not b.is_contiguous():
-        raise ValueError("b must be a contiguous CUDA tensor [K, N]")
+        raise ValueError("b must be a contiguous CUDA tensor [N, K]" if fp8
+                         else "b must be a contiguous CUDA tensor [K, N]")
     M = D * m
+    out_dtype = torch.bfloat16 if fp8 else b.dtype
     if a_gathered is None:
         a_gathered = torch.empty((M, K), dtype=b.dtype, device=b.device)
     if out is None:
-        out = torch.empty((M, N), dtype=b.dtype, device=b.device)
+        out = torch.empty((M, N), dtype=out_dtype, device=b.device)
+    if (a_gathered.shape != (M, K) or a_gathered.dtype != b.dtype or out.shape != (M, N)
+            or out.dtype != out_dtype):
+        raise ValueError("a_gathered must be [M, K] of the inputs' dtype and out [M, N] of "
+                         + ("bf16" if fp8 else "the inputs' dtype"))
     if bias is not None and (bias.dtype != torch.float32 or bias.shape != (N,) or not bias.is_cuda):
         raise ValueError("bias must be a CUDA fp32 tensor [N]")
     o = default_options()
@@ -180,6 +198,8 @@ def _call(fused, shards, b, bias, a_gathered, out, stream, layout, rank, k_per_f
     o.num_sms = num_sms
     o.timeout_ns = timeout_ns
     o.inject_skip_flag = inject_skip_flag
+    o.scale_a = scale_a
+    o.scale_b = scale_b
     if trace is not None:
         o.trace = trace.data_ptr()
         o.trace_words = trace.numel()
@@ -208,18 +228,20 @@ def _call(fused, shards, b, bias, a_gathered, out, stream, layout, rank, k_per_f
 def ag_matmul(shards, b, bias=None, *, a_gathered=None, out=None, stream=None,
               layout: str = "k_contiguous", rank: int = 0, k_per_flag: int = 0,
               num_sms: int = 0, timeout_ns: int = 0, inject_skip_flag: int = -1, trace=None,
-              workspace=None):
-    """Fused all-gather matmul (one persistent kernel).  Returns (a_gathered, out)."""
+              workspace=None, scale_a: float = 1.0, scale_b: float = 1.0):
+    """Fused all-gather matmul (one persistent kernel).  Returns (a_gathered, out).
+    ``scale_a``/``scale_b``: FP8 per-tensor scales (ignored for 16-bit inputs)."""
     return _call(True, shards, b, bias, a_gathered, out, stream, layout, rank, k_per_flag,
-                 num_sms, timeout_ns, inject_skip_flag, trace, workspace)
+                 num_sms, timeout_ns, inject_skip_flag, trace, workspace,
+                 scale_a=scale_a, scale_b=scale_b)
 
 
 def ag_then_matmul(shards, b, bias=None, *, a_gathered=None, out=None, stream=None,
                    layout: str = "k_contiguous", k_per_flag: int = 0, num_sms: int = 0,
-                   timeout_ns: int = 0, trace=None):
+                   timeout_ns: int = 0, trace=None, scale_a: float = 1.0, scale_b: float = 1.0):
     """Barrier baseline: gather kernel, then GEMM kernel.  Returns (a_gathered, out)."""
     return _call(False, shards, b, bias, a_gathered, out, stream, layout, 0, k_per_flag,
-                 num_sms, timeout_ns, -1, trace, None)
+                 num_sms, timeout_ns, -1, trace, None, scale_a=scale_a, scale_b=scale_b)
 
 
 def ag_chunked_matmul(shards, b, bias=None, *, chunks: int = 4, a_gathered=None, out=None,
@@ -243,10 +265,12 @@ def device_error(stream=None):
     return code.value, info.value
 
 
-def workspace_size(D, m_per_shard, K, N, layout: str = "k_contiguous", k_per_flag: int = 0) -> int:
+def workspace_size(D, m_per_shard, K, N, layout: str = "k_contiguous", k_per_flag: int = 0,
+                   dtype: str = "bf16") -> int:
     o = default_options()
     o.layout = LAYOUTS[layout]
     o.k_per_flag = k_per_flag
+    o.dtype = DTYPES[dtype]
     return int(library().ag_workspace_size(D, m_per_shard, K, N, ctypes.byref(o)))
 
 

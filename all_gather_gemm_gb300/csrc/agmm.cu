@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <atomic>
 #include <cstdint>
 #include <cstdio>
@@ -130,7 +131,12 @@ int validate(const void** a_shards, int D, int m_per_shard, int K, const void* b
   if (D > AG_MAX_SHARDS) return AG_ERR_UNSUPPORTED;
   const int64_t M = (int64_t)D * m_per_shard;
   if (M > INT32_MAX) return AG_ERR_INVALID_ARG;
-  if (o.dtype != AG_DTYPE_BF16 && o.dtype != AG_DTYPE_FP16) return AG_ERR_INVALID_ARG;
+  if (o.dtype != AG_DTYPE_BF16 && o.dtype != AG_DTYPE_FP16 && o.dtype != AG_DTYPE_FP8_E4M3)
+    return AG_ERR_INVALID_ARG;
+  if (o.dtype == AG_DTYPE_FP8_E4M3) {
+    if (!std::isfinite(o.scale_a) || !std::isfinite(o.scale_b)) return AG_ERR_INVALID_ARG;
+    if (o.layout != AG_LAYOUT_K_CONTIGUOUS) return AG_ERR_UNSUPPORTED;
+  }
   if (o.layout != AG_LAYOUT_K_CONTIGUOUS && o.layout != AG_LAYOUT_M_CONTIGUOUS)
     return AG_ERR_INVALID_ARG;
   if (o.rank < 0 || o.rank >= D) return AG_ERR_INVALID_ARG;
@@ -229,7 +235,7 @@ int query_pair_clusters(int sms, int* clusters) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   *clusters = 0;
-  AG_CK(cudaOccupancyMaxActiveClusters(clusters, agmm_gemm_kernel<kFusedK, true>, &cfg));
+  AG_CK(cudaOccupancyMaxActiveClusters(clusters, agmm_gemm_kernel<kFusedK, true, false>, &cfg));
   return AG_OK;
 }
 
@@ -242,28 +248,36 @@ int device_init(DevState& ds, int dev) {
   ds.sms = sms;
   // The kernels are built for sm_103a only; a missing image is "unsupported".
   cudaFuncAttributes fa;
-  if (cudaFuncGetAttributes(&fa, agmm_gemm_kernel<kFusedK, false>) != cudaSuccess || major != 10) {
+  if (cudaFuncGetAttributes(&fa, agmm_gemm_kernel<kFusedK, false, false>) != cudaSuccess || major != 10) {
     cudaGetLastError();
     ds.init = true;
     ds.supported = false;
     return AG_ERR_UNSUPPORTED;
   }
   constexpr int kSmem1 = Pipe<false>::kSmemBytes, kSmem2 = Pipe<true>::kSmemBytes;
-  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kGemmK, false>,
+  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kGemmK, false, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem1));
-  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kGemmM, false>,
+  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kGemmM, false, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem1));
-  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kFusedK, false>,
+  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kFusedK, false, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem1));
-  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kFusedM, false>,
+  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kFusedM, false, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem1));
-  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kGemmK, true>,
+  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kGemmK, true, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem2));
-  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kGemmM, true>,
+  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kGemmM, true, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem2));
-  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kFusedK, true>,
+  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kFusedK, true, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem2));
-  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kFusedM, true>,
+  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kFusedM, true, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem2));
+  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kGemmK, false, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem1));
+  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kFusedK, false, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem1));
+  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kGemmK, true, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem2));
+  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kFusedK, true, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem2));
   if (int st = query_pair_clusters(sms, &ds.pair_clusters)) return st;
   AG_CK(cudaMalloc(&ds.err, 2 * sizeof(unsigned long long)));
@@ -349,9 +363,9 @@ int make_map3(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, u
 }
 
 // pair: clusters of two CTAs (grid even), the kernel's CTA-pair variant.
-template <int kMode, bool kPair>
+template <int kMode, bool kPair, bool kF8 = false>
 int launch(int grid, cudaStream_t stream, const GemmParams& p, const char* what) {
-  auto k = agmm_gemm_kernel<kMode, kPair>;
+  auto k = agmm_gemm_kernel<kMode, kPair, kF8>;
   cudaError_t e;
   if constexpr (kPair) {
     cudaLaunchConfig_t cfg = {};
@@ -437,6 +451,14 @@ int run(bool fused, const void** a_shards, int D, int m_per_shard, int K, const 
   ag_options o;
   ag_options_default(&o);
   if (opt_in) o = *opt_in;
+  // FP8: a row of K bytes is moved as K/2 16-bit words, so from here on K
+  // counts those words (shapes, maps, flags, copies); only b's map, the MMA
+  // and the epilogue know the elements are 8-bit.
+  const bool fp8 = o.dtype == AG_DTYPE_FP8_E4M3;
+  if (fp8) {
+    if (K < 16 || K % 16) return AG_ERR_INVALID_ARG;
+    K /= 2;
+  }
   Shape s;
   int st = validate(a_shards, D, m_per_shard, K, b, N, bias, a_gathered, out, o, fused, &s);
   if (st != AG_OK) return st;
@@ -513,7 +535,7 @@ int run(bool fused, const void** a_shards, int D, int m_per_shard, int K, const 
   GemmParams p;
   memset(&p, 0, sizeof p);
   if ((st = make_map(&p.tm_a, a_gathered, (uint64_t)K, (uint64_t)s.M, kBK, kBM)) != AG_OK) return st;
-  if ((st = make_map(&p.tm_b, b, (uint64_t)N, (uint64_t)K, 64, kBK)) != AG_OK) return st;
+  if (!fp8 && (st = make_map(&p.tm_b, b, (uint64_t)N, (uint64_t)K, 64, kBK)) != AG_OK) return st;
   if ((st = make_map(&p.tm_out, out, (uint64_t)N, (uint64_t)s.M, kEpiCols, kEpiRows)) != AG_OK)
     return st;
   if (layout_m &&
@@ -558,9 +580,21 @@ int run(bool fused, const void** a_shards, int D, int m_per_shard, int K, const 
   p.num_kb = s.num_kb;
   const int grid = plan_launch(p, s, cap, ds.pair_clusters, fused, layout_m, o.k_per_flag,
                                fused ? o.rank : 0);
-  p.fp16 = o.dtype == AG_DTYPE_FP16 ? 1 : 0;
+  p.fp16 = o.dtype == AG_DTYPE_FP16 ? 1 : 0;  // FP8 writes bf16
   p.inject_skip_flag = fused ? o.inject_skip_flag : -1;
   const bool pair = p.pair != 0;
+  if (fp8) {
+    // b is [N, K] (K-major): boxes of this CTA's b columns (pair: 128 of the
+    // tile's 256) x 128 bytes of K.
+    if ((st = make_map(&p.tm_b, b, (uint64_t)K, (uint64_t)N, kBK, pair ? kBN / 2 : kBN)) != AG_OK)
+      return st;
+    p.scale_ab = o.scale_a * o.scale_b;
+    if (fused)
+      return pair ? launch<kFusedK, true, true>(grid, stream, p, "fused kernel (fp8)")
+                  : launch<kFusedK, false, true>(grid, stream, p, "fused kernel (fp8)");
+    return pair ? launch<kGemmK, true, true>(grid, stream, p, "gemm kernel (fp8)")
+                : launch<kGemmK, false, true>(grid, stream, p, "gemm kernel (fp8)");
+  }
   if (fused && layout_m)
     return pair ? launch<kFusedM, true>(grid, stream, p, "fused kernel")
                 : launch<kFusedM, false>(grid, stream, p, "fused kernel");
@@ -644,6 +678,7 @@ int run_chunked(const void** a_shards, int D, int m_per_shard, int K, const void
   ag_options o;
   ag_options_default(&o);
   if (opt_in) o = *opt_in;
+  if (o.dtype == AG_DTYPE_FP8_E4M3) return AG_ERR_UNSUPPORTED;
   Shape s;
   int st = validate(a_shards, D, m_per_shard, K, b, N, bias, a_gathered, out, o, false, &s);
   if (st != AG_OK) return st;
@@ -747,16 +782,16 @@ int noalloc_setup(NoAllocState& ns, int dev) {
   AG_CK(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev));
   AG_CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
   cudaFuncAttributes fa;
-  if (cudaFuncGetAttributes(&fa, agmm_gemm_kernel<kFusedK, false>) != cudaSuccess || major != 10) {
+  if (cudaFuncGetAttributes(&fa, agmm_gemm_kernel<kFusedK, false, false>) != cudaSuccess || major != 10) {
     cudaGetLastError();
     ns.init = true;
     ns.supported = false;
     return AG_ERR_UNSUPPORTED;
   }
-  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kFusedK, false>,
+  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kFusedK, false, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Pipe<false>::kSmemBytes));
-  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kFusedK, true>,
+  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kFusedK, true, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Pipe<true>::kSmemBytes));
   if (int st = query_pair_clusters(sms, &ns.pair_clusters)) return st;
@@ -795,6 +830,7 @@ int run_noalloc(const void** a_shards, int D, int m_per_shard, int K, const void
   ag_options_default(&o);
   if (opt_in) o = *opt_in;
   if (o.workspace) return AG_ERR_INVALID_ARG;  // the scratch is fixed
+  if (o.dtype == AG_DTYPE_FP8_E4M3) return AG_ERR_UNSUPPORTED;
   if (o.layout != AG_LAYOUT_K_CONTIGUOUS) return AG_ERR_UNSUPPORTED;
   Shape s;
   int st = validate(a_shards, D, m_per_shard, K, b, N, bias, a_gathered, out, o, true, &s);
@@ -878,6 +914,8 @@ void ag_options_default(ag_options* opt) {
   opt->num_sms = 0;
   opt->inject_skip_flag = -1;
   opt->timeout_ns = kDefaultTimeoutNs;
+  opt->scale_a = 1.0f;
+  opt->scale_b = 1.0f;
 }
 
 int ag_matmul(const void** a_shards, int D, int m_per_shard, int K, const void* b, int N,
@@ -915,6 +953,10 @@ size_t ag_workspace_size(int D, int m_per_shard, int K, int N, const ag_options*
   ag_options o;
   ag_options_default(&o);
   if (opt) o = *opt;
+  if (o.dtype == AG_DTYPE_FP8_E4M3) {  // sized like the 16-bit problem with K/2 columns
+    if (K % 16) return 0;
+    K /= 2;
+  }
   if (D < 1 || D > AG_MAX_SHARDS || m_per_shard < 1 || K < 8 || N < 8 || K % 8 || N % 8 ||
       o.k_per_flag < 0)
     return 0;

@@ -160,7 +160,8 @@ struct GemmParams {
   int sh_log2;              // log2 of the rows of a tm_shard8 box (3..6; divides m_per_shard)
   int seg_blocks;           // barrier GEMM over row segments (0: off): tm_a / tm_out are 3-D
   int seg_rows;             // [.., seg_rows, segments]; row block mb = segment mb / seg_blocks
-  int fp16;                 // 1: fp16, 0: bf16
+  int fp16;                 // 1: fp16, 0: bf16 (the output's type for FP8 inputs)
+  float scale_ab;           // FP8 inputs: scale_a * scale_b, applied to the fp32 sum
   int inject_skip_flag;     // this flag index is never published (fault injection)
 };
 
@@ -605,9 +606,15 @@ __device__ __forceinline__ void drain_loads(uint64_t* full, uint32_t issued_mask
 // unused.  A stage of the peer is refilled only after the MMA commit that
 // frees it (multicast to both CTAs' `empty`), which follows the completion of
 // the leader's phase, so no load of a new phase can land in an old one.
-template <int kMode, bool kPair>
+// kF8: A and b are FP8 E4M3 (kind::f8f6f4 MMAs), b given K-major ([N, K]),
+// out bf16 scaled by scale_ab.  All data movement treats a row of K bytes as
+// K/2 16-bit words, so p.K, the boxes, the flags and the copiers are those of
+// a 16-bit problem with half the columns; only the MMA, B's major-ness and
+// the epilogue differ.  k-contiguous layout only.
+template <int kMode, bool kPair, bool kF8>
 __global__ void __launch_bounds__(mode_threads(kMode), 1)
     agmm_gemm_kernel(const __grid_constant__ GemmParams p) {
+  static_assert(!kF8 || !mode_layout_m(kMode), "FP8 runs with the k-contiguous layout only");
   using P = Pipe<kPair>;
   constexpr int kStages = P::kStages;
   constexpr int kStageBytes = P::kStageBytes;
@@ -950,7 +957,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
     if (lane == 0) {
       const uint32_t ab_bf16 = p.fp16 ? 0u : 1u;
       constexpr uint32_t kM = kPair ? 2 * kBM : kBM;
-      const uint32_t idesc_k = idesc_f16_f32(ab_bf16, 0, 1, kM, kBN);
+      const uint32_t idesc_k = kF8 ? idesc_e4m3_f32(kM, kBN) : idesc_f16_f32(ab_bf16, 0, 1, kM, kBN);
       const uint32_t idesc_mn = idesc_f16_f32(ab_bf16, 1, 1, kM, kBN);
       // A's major-ness: K-major for the k-contiguous layout, MN-major for the
       // [K, M] staging; only the single-CTA fused m-contiguous kernel mixes
@@ -999,11 +1006,18 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
             const uint64_t a_desc =
                 a_mn ? smem_desc_sw128(a_addr + ks * 2048, kMnChunkBytes, 1024)
                      : smem_desc_sw128(a_addr + ks * 32, 16, 1024);
-            const uint64_t b_desc = smem_desc_sw128(b_addr + ks * 2048, kMnChunkBytes, 1024);
-            if constexpr (kPair)
-              umma_f16_pair(d_tmem, a_desc, b_desc, idesc, (kb | ks) != 0 ? 1u : 0u);
+            // B: MN-major 16-bit [K, N] boxes, or (FP8) K-major rows of [N, K].
+            const uint64_t b_desc = kF8 ? smem_desc_sw128(b_addr + ks * 32, 16, 1024)
+                                        : smem_desc_sw128(b_addr + ks * 2048, kMnChunkBytes, 1024);
+            const uint32_t acc = (kb | ks) != 0 ? 1u : 0u;
+            if constexpr (kF8 && kPair)
+              umma_f8_pair(d_tmem, a_desc, b_desc, idesc, acc);
+            else if constexpr (kF8)
+              umma_f8(d_tmem, a_desc, b_desc, idesc, acc);
+            else if constexpr (kPair)
+              umma_f16_pair(d_tmem, a_desc, b_desc, idesc, acc);
             else
-              umma_f16(d_tmem, a_desc, b_desc, idesc, (kb | ks) != 0 ? 1u : 0u);
+              umma_f16(d_tmem, a_desc, b_desc, idesc, acc);
           }
           if constexpr (kPair)
             umma_commit_pair_mc(&empty[stage], 3);  // frees the stage in both CTAs
@@ -1077,6 +1091,12 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
         for (int i = 0; i < 16; ++i) {
           float v0 = __uint_as_float(r0[2 * i]), v1 = __uint_as_float(r0[2 * i + 1]);
           float w0 = __uint_as_float(r1[2 * i]), w1 = __uint_as_float(r1[2 * i + 1]);
+          if constexpr (kF8) {
+            v0 *= p.scale_ab;
+            v1 *= p.scale_ab;
+            w0 *= p.scale_ab;
+            w1 *= p.scale_ab;
+          }
           if (p.bias) {
             const int na = n0 + 2 * i, nb2 = n0 + 32 + 2 * i;
             v0 += na < p.N ? __ldg(p.bias + na) : 0.f;
@@ -1141,10 +1161,15 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
             const uint32_t bar_c = full_c + 8u * (uint32_t)stage;
             if (!kPair || rank == 0)
               mbar_arrive_expect_tx(&full[stage], kPair ? 2 * P::kBStageBytes : P::kBStageBytes);
+            if constexpr (kF8) {
+              // [N, K] rows: one box of this CTA's columns x 128 bytes of K
+              stage_load_2d<kPair>(b_dst, &p.tm_b, &full[stage], bar_c, kb * kBK, n0);
+            } else {
 #pragma unroll
-            for (int q = 0; q < P::kBCols / 64; ++q)
-              stage_load_2d<kPair>(b_dst + q * kMnChunkBytes, &p.tm_b, &full[stage], bar_c,
-                                   n0 + q * 64, kb * kBK);
+              for (int q = 0; q < P::kBCols / 64; ++q)
+                stage_load_2d<kPair>(b_dst + q * kMnChunkBytes, &p.tm_b, &full[stage], bar_c,
+                                     n0 + q * 64, kb * kBK);
+            }
             issued_mask |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
             if (++stage == kStages) {

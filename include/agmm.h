@@ -44,7 +44,8 @@
  * The caller allocates and owns every pointer argument.  Outputs must not
  * overlap each other or any input.  The dtype of a_shards, b, a_gathered and
  * out is the same (ag_options.dtype; bf16 for the entry points without
- * options).
+ * options), except with AG_DTYPE_FP8_E4M3 (8-bit inputs, b transposed, bf16
+ * out; see ag_dtype).
  *
  * Semantics: asynchronous.  A call validates its arguments, enqueues one
  * (fused) or two (barrier) kernels on `stream` and returns; it never
@@ -90,7 +91,20 @@ typedef enum ag_status {
   AG_ERR_TOO_LARGE = 6    /* problem needs more than ag_matmul_noalloc's fixed scratch */
 } ag_status;
 
-typedef enum ag_dtype { AG_DTYPE_BF16 = 0, AG_DTYPE_FP16 = 1 } ag_dtype;
+/* Storage types.  AG_DTYPE_FP8_E4M3 is an extension the pages do not cover:
+ * 8-bit A and b in the OCP FP8 E4M3 encoding (1 sign, 4 exponent bits with
+ * bias 7, 3 mantissa bits, no infinities, S.1111.111 is NaN), with per-tensor
+ * scales ag_options.scale_a and scale_b.  With it:
+ *   a_shards[r]  [m_per_shard, K] e4m3, row-major;
+ *   b            given TRANSPOSED: [N, K] e4m3, row-major (K fastest), the
+ *                layout FP8 GEMMs take their second operand in;
+ *   a_gathered   [M, K] e4m3;
+ *   out          [M, N] bf16:  out = bf16(scale_a * scale_b * (a @ b) + bias),
+ *                products and sums in fp32, the scale applied to the fp32 sum;
+ *   K % 16 == 0 (16-byte rows), N % 8 == 0, layout k-contiguous only (the
+ *   m-contiguous staging, ag_chunked_matmul_ex and ag_matmul_noalloc return
+ *   AG_ERR_UNSUPPORTED for it). */
+typedef enum ag_dtype { AG_DTYPE_BF16 = 0, AG_DTYPE_FP16 = 1, AG_DTYPE_FP8_E4M3 = 2 } ag_dtype;
 
 /* Layout of the staged A in HBM ("Fused all-gather+GEMM HBM-buffer kernel for
  * iris.ops", section "New kernel": k_contiguous and m_contiguous staged-A
@@ -122,6 +136,8 @@ typedef struct ag_options {
   int64_t trace_words;      /* capacity of `trace` in 64-bit words */
   void* workspace;          /* caller-owned DEVICE workspace or NULL (library-owned) */
   int64_t workspace_bytes;  /* its size; must be >= ag_workspace_size() */
+  float scale_a;            /* AG_DTYPE_FP8_E4M3: per-tensor scale of A (default 1); ignored otherwise */
+  float scale_b;            /* AG_DTYPE_FP8_E4M3: per-tensor scale of b (default 1); must be finite */
 } ag_options;
 
 /* Fill `opt` with the defaults listed above.  Never fails (NULL is ignored). */

@@ -75,6 +75,19 @@ def _load():
                                          ctypes.c_int64, f32p, ctypes.c_int, i64p,
                                          ctypes.c_int64, f32p, u16p, f32p, ctypes.c_int]
         lib.oracle_gemm_rows.restype = ctypes.c_int
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        lib.oracle_e4m3_to_f32.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_to_f32.restype = ctypes.c_float
+        lib.oracle_e4m3_to_f32_array.argtypes = [u8p, ctypes.c_int64, f32p]
+        lib.oracle_e4m3_to_f32_array.restype = None
+        lib.oracle_all_gather_bytes.argtypes = [ctypes.POINTER(u8p), ctypes.c_int,
+                                                ctypes.c_int64, ctypes.c_int64, u8p]
+        lib.oracle_all_gather_bytes.restype = None
+        lib.oracle_gemm_rows_fp8.argtypes = [u8p, ctypes.c_int64, ctypes.c_int64, u8p,
+                                             ctypes.c_int64, ctypes.c_float, ctypes.c_float,
+                                             f32p, i64p, ctypes.c_int64, f32p, u16p, f32p,
+                                             ctypes.c_int]
+        lib.oracle_gemm_rows_fp8.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -184,3 +197,75 @@ def within_tolerance(got_f32, ref_f32, abs_ab, rel: float = 1e-2, atol: float = 
     if bad.any():
         return False, ratio, tuple(int(v) for v in np.argwhere(bad)[0])
     return True, ratio, None
+
+
+# ---------------------------------------------------------------- FP8 E4M3
+# An extension the pages do not cover: 8-bit inputs with per-tensor scales,
+#     out_f32[i, j] = (scale_a * scale_b) * sum_k f32(a[i, k]) * f32(bt[j, k])
+#                     (+ bias[j]),   out = bf16(out_f32)
+# with b given transposed (bt = [N, K]); sums in fp32, k increasing.
+
+
+def _u8(x) -> np.ndarray:
+    x = np.ascontiguousarray(x)
+    if x.dtype != np.uint8:
+        raise TypeError(f"expected uint8 bit patterns, got {x.dtype}")
+    return x
+
+
+def e4m3_to_f32(bits) -> np.ndarray:
+    """Decode E4M3 bit patterns to fp32 (exact)."""
+    bits = _u8(bits)
+    out = np.empty(bits.shape, np.float32)
+    _load().oracle_e4m3_to_f32_array(_ptr(bits, ctypes.c_uint8), bits.size,
+                                     _ptr(out, ctypes.c_float))
+    return out
+
+
+def all_gather_bytes(shards) -> np.ndarray:
+    """Row concatenation of D equally shaped 2-D byte arrays (any element type
+    stored as uint8)."""
+    shards = [_u8(s) for s in shards]
+    D = len(shards)
+    mps, row = shards[0].shape
+    for s in shards:
+        if s.shape != (mps, row):
+            raise ValueError("all shards must have the same shape")
+    out = np.empty((D * mps, row), np.uint8)
+    arr = (ctypes.POINTER(ctypes.c_uint8) * D)(*[_ptr(s, ctypes.c_uint8) for s in shards])
+    _load().oracle_all_gather_bytes(arr, D, mps, row, _ptr(out, ctypes.c_uint8))
+    return out
+
+
+def gemm_rows_fp8(a, bt, scale_a: float = 1.0, scale_b: float = 1.0, bias=None, *, rows=None,
+                  want_abs: bool = True, nthreads: int = 0):
+    """Rows ``rows`` of scale_a*scale_b * (a @ bt.T) (+ bias) for E4M3 ``a`` [M, K]
+    and ``bt`` [N, K] (uint8 bit patterns).  Returns (out_f32, out_bf16_bits,
+    abs_ab, threads) with ``abs_ab = |scale_a*scale_b| * sum_k |a| |b|``."""
+    a = _u8(a)
+    bt = _u8(bt)
+    M, K = a.shape
+    N, K2 = bt.shape
+    if K2 != K:
+        raise ValueError("inner dimensions differ")
+    if rows is None:
+        rows = np.arange(M, dtype=np.int64)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    if rows.size and (rows.min() < 0 or rows.max() >= M):
+        raise IndexError("row index out of range")
+    nr = rows.size
+    out_f32 = np.empty((nr, N), np.float32)
+    out = np.empty((nr, N), np.uint16)
+    abs_ab = np.empty((nr, N), np.float32) if want_abs else None
+    bias_p = None
+    if bias is not None:
+        bias = np.ascontiguousarray(bias, dtype=np.float32)
+        if bias.shape != (N,):
+            raise ValueError("bias must be [N]")
+        bias_p = _ptr(bias, ctypes.c_float)
+    th = _load().oracle_gemm_rows_fp8(
+        _ptr(a, ctypes.c_uint8), M, K, _ptr(bt, ctypes.c_uint8), N, float(scale_a),
+        float(scale_b), bias_p, _ptr(rows, ctypes.c_int64), nr, _ptr(out_f32, ctypes.c_float),
+        _ptr(out, ctypes.c_uint16), _ptr(abs_ab, ctypes.c_float) if want_abs else None,
+        nthreads)
+    return out_f32, out, abs_ab, th

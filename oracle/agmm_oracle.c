@@ -24,6 +24,10 @@
  * The 16-bit <-> fp32 conversions are written here from the IEEE-754 binary16
  * and bfloat16 encodings; they use no library conversion routine.
  *
+ * Extension (not on the pages): FP8 E4M3 inputs with per-tensor scales,
+ * out = bf16(scale_a * scale_b * (a @ b) + bias), b given as [N, K]; the
+ * E4M3 decoding is written from the OCP 8-bit floating-point definition.
+ *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared -pthread
  * (-ffp-contract=off keeps a*b+c as two roundings on every host, so results
  * do not depend on whether the compiler would emit FMA.)
@@ -142,6 +146,30 @@ void oracle_all_gather(const uint16_t* const* shards, int D, int64_t m_per_shard
     memcpy(a_gathered + (size_t)r * shard_elems, shards[r], shard_elems * sizeof(uint16_t));
 }
 
+/* ---------------- FP8 E4M3 (an extension the pages do not cover) ----------
+ * The OCP 8-bit floating-point format E4M3: 1 sign bit, 4 exponent bits with
+ * bias 7, 3 mantissa bits.  Exponent field 0 holds subnormals m * 2^-9;
+ * otherwise the value is (1 + m/8) * 2^(e-7) = (8 + m) * 2^(e-10).  There are
+ * no infinities; S.1111.111 is NaN, so the largest finite value is 448. */
+float oracle_e4m3_to_f32(uint8_t v) {
+  const int sign = v >> 7, e = (v >> 3) & 15, m = v & 7;
+  if (e == 15 && m == 7) return sign ? -NAN : NAN;
+  const float x = e == 0 ? ldexpf((float)m, -9) : ldexpf((float)(8 + m), e - 10);
+  return sign ? -x : x;
+}
+
+void oracle_e4m3_to_f32_array(const uint8_t* src, int64_t n, float* dst) {
+  for (int64_t i = 0; i < n; ++i) dst[i] = oracle_e4m3_to_f32(src[i]);
+}
+
+/* Byte-wise all-gather (any element size): row concatenation of D shards of
+ * row_bytes * m_per_shard bytes each. */
+void oracle_all_gather_bytes(const uint8_t* const* shards, int D, int64_t m_per_shard,
+                             int64_t row_bytes, uint8_t* a_gathered) {
+  size_t shard_bytes = (size_t)m_per_shard * (size_t)row_bytes;
+  for (int r = 0; r < D; ++r) memcpy(a_gathered + (size_t)r * shard_bytes, shards[r], shard_bytes);
+}
+
 /* ---------------- the GEMM: naive i-k-j loop, fp32 accumulate ------------ */
 
 typedef struct {
@@ -213,6 +241,89 @@ int oracle_gemm_rows(const uint16_t* a, int64_t M, int64_t K, const uint16_t* b,
     j->first = nrows * t / nthreads;
     j->last = nrows * (t + 1) / nthreads;
     pthread_create(&tids[t], NULL, gemm_worker, j);
+  }
+  for (int t = 0; t < nthreads; ++t) pthread_join(tids[t], NULL);
+  free(tids);
+  free(jobs);
+  free(b32);
+  return nthreads;
+}
+
+/* ---------------- FP8 GEMM: E4M3 a [M, K] and b given as [N, K] ------------
+ * out_f32[t, j] = (scale_a * scale_b) * sum_k f32(a[rows[t], k]) * f32(bt[j, k])
+ *                 (+ bias[j]),  the sum in fp32 over k in increasing order, the
+ * product of the two scales rounded to fp32 once, then bf16 by RNE.
+ * abs_ab[t, j] = |scale_a * scale_b| * sum_k |a| |b|  (the tolerance scale). */
+typedef struct {
+  const uint8_t* a;
+  const float* b32; /* [K, N], widened and transposed once */
+  const float* bias;
+  const int64_t* rows;
+  int64_t K, N;
+  float scale;
+  float* out_f32;
+  uint16_t* out;
+  float* abs_ab;
+  int64_t first, last;
+} gemm8_job;
+
+static void* gemm8_worker(void* arg) {
+  gemm8_job* j = (gemm8_job*)arg;
+  const int64_t K = j->K, N = j->N;
+  float* acc = (float*)malloc((size_t)N * sizeof(float));
+  float* absacc = j->abs_ab ? (float*)malloc((size_t)N * sizeof(float)) : NULL;
+  for (int64_t t = j->first; t < j->last; ++t) {
+    const uint8_t* arow = j->a + (size_t)j->rows[t] * (size_t)K;
+    for (int64_t n = 0; n < N; ++n) acc[n] = 0.0f;
+    if (absacc)
+      for (int64_t n = 0; n < N; ++n) absacc[n] = 0.0f;
+    for (int64_t k = 0; k < K; ++k) {
+      const float aik = oracle_e4m3_to_f32(arow[k]);
+      const float* brow = j->b32 + (size_t)k * (size_t)N;
+      for (int64_t n = 0; n < N; ++n) acc[n] = acc[n] + aik * brow[n];
+      if (absacc) {
+        const float aabs = fabsf(aik);
+        for (int64_t n = 0; n < N; ++n) absacc[n] = absacc[n] + aabs * fabsf(brow[n]);
+      }
+    }
+    for (int64_t n = 0; n < N; ++n) {
+      float v = acc[n] * j->scale;
+      if (j->bias) v = v + j->bias[n];
+      if (j->out_f32) j->out_f32[(size_t)t * N + n] = v;
+      if (j->out) j->out[(size_t)t * N + n] = oracle_f32_to_bf16(v);
+      if (absacc) j->abs_ab[(size_t)t * N + n] = absacc[n] * fabsf(j->scale);
+    }
+  }
+  free(acc);
+  free(absacc);
+  return NULL;
+}
+
+int oracle_gemm_rows_fp8(const uint8_t* a, int64_t M, int64_t K, const uint8_t* bt, int64_t N,
+                         float scale_a, float scale_b, const float* bias, const int64_t* rows,
+                         int64_t nrows, float* out_f32, uint16_t* out, float* abs_ab,
+                         int nthreads) {
+  (void)M;
+  if (nthreads <= 0) {
+    long c = sysconf(_SC_NPROCESSORS_ONLN);
+    nthreads = c > 0 ? (int)c : 1;
+  }
+  if (nthreads > nrows) nthreads = nrows > 0 ? (int)nrows : 1;
+  float* b32 = (float*)malloc((size_t)K * (size_t)N * sizeof(float));
+  for (int64_t n = 0; n < N; ++n)
+    for (int64_t k = 0; k < K; ++k)
+      b32[(size_t)k * N + n] = oracle_e4m3_to_f32(bt[(size_t)n * K + k]);
+  gemm8_job* jobs = (gemm8_job*)calloc((size_t)nthreads, sizeof(gemm8_job));
+  pthread_t* tids = (pthread_t*)calloc((size_t)nthreads, sizeof(pthread_t));
+  const float scale = scale_a * scale_b;
+  for (int t = 0; t < nthreads; ++t) {
+    gemm8_job* j = &jobs[t];
+    j->a = a; j->b32 = b32; j->bias = bias; j->rows = rows;
+    j->K = K; j->N = N; j->scale = scale;
+    j->out_f32 = out_f32; j->out = out; j->abs_ab = abs_ab;
+    j->first = nrows * t / nthreads;
+    j->last = nrows * (t + 1) / nthreads;
+    pthread_create(&tids[t], NULL, gemm8_worker, j);
   }
   for (int t = 0; t < nthreads; ++t) pthread_join(tids[t], NULL);
   free(tids);

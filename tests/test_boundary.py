@@ -44,7 +44,8 @@ def test_options_default_matches_header(lib):
     assert (o.dtype, o.layout, o.rank, o.k_per_flag, o.num_sms) == (0, 0, 0, 0, 0)
     assert o.inject_skip_flag == -1 and o.timeout_ns == 2_000_000_000
     assert not o.trace and o.trace_words == 0 and not o.workspace and o.workspace_bytes == 0
-    assert ctypes.sizeof(o) == 64
+    assert o.scale_a == 1.0 and o.scale_b == 1.0
+    assert ctypes.sizeof(o) == 72
 
 
 def test_status_strings(lib):
@@ -70,6 +71,10 @@ def test_workspace_size(lib):
     # automatic granularity, sized at 4 k-blocks per flag: K=384 has 6 k-blocks
     # -> 2 flags per row block (3 row blocks): 48 B -> 1 KiB
     assert agmm.workspace_size(8, 48, 384, 384) == 1024 + 1024
+    # FP8 (8-bit elements) is sized like the 16-bit problem with K/2 columns;
+    # K must be a multiple of 16 (16-byte rows)
+    assert agmm.workspace_size(8, 2048, 16384, 3584, dtype="fp8_e4m3") == 32768 + 15360
+    assert agmm.workspace_size(8, 2048, 8200, 3584, dtype="fp8_e4m3") == 0
     assert agmm.workspace_size(8, 48, 384, 384, k_per_flag=8) == 1024 + 1024
     assert agmm.workspace_size(0, 1, 8, 8) == 0
     assert agmm.workspace_size(1, 1, 12, 8) == 0
