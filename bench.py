@@ -266,7 +266,8 @@ def run_sweep(args):
     """Fused vs barrier device time (and host time per call) on the workloads of
     the parity configs: the two-shard case, the cube sweep, M=1024 at D=2/4/8,
     M=16384 (both layouts) and M=4096 with bias (m-contiguous); plus the
-    output-sharded M=16384 slice (N = 3584 / 8, both layouts)."""
+    output-sharded M=16384 slice (N = 3584 / 8, both layouts); plus FP8 E4M3
+    forms of M=16384, M=1024 and cube 4096 (an extension, k-contiguous)."""
     import torch
 
     import all_gather_gemm_gb300 as agmm
@@ -280,6 +281,12 @@ def run_sweep(args):
     # output-sharded variant: one rank's N/8 column slice of the M=16384 problem
     cases += [(inp.iris_m16384_colshard(), "k_contiguous"),
               (inp.iris_m16384_colshard(), "m_contiguous")]
+    cases += [(inp.fp8_m16384(), "k_contiguous"), (inp.fp8_m1024(8), "k_contiguous"),
+              (inp.fp8_cube(4096), "k_contiguous")]
+    if args.only:
+        keep = [t for t in args.only.split(",") if t]
+        cases = [c for c in cases if any(t in c[0].name for t in keep)]
+    peak16 = load_peaks()[0]
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
     steps = max(args.steps // 5, 5)
     for w, layout in cases:
@@ -287,14 +294,16 @@ def run_sweep(args):
         shards = [s.cuda() for s in x.shards]
         b = x.b.cuda()
         bias = x.bias.cuda() if x.bias is not None else None
+        fp8 = w.dtype == "fp8_e4m3"
         a_g = torch.empty((w.M, w.K), dtype=b.dtype, device="cuda")
-        out = torch.empty((w.M, w.N), dtype=b.dtype, device="cuda")
+        out = torch.empty((w.M, w.N), dtype=torch.bfloat16 if fp8 else b.dtype, device="cuda")
+        sc = {"scale_a": w.scale_a, "scale_b": w.scale_b} if fp8 else {}
         calls = {
             "fused": lambda: agmm.ag_matmul(shards, b, bias, a_gathered=a_g, out=out,
-                                            layout=layout),
+                                            layout=layout, **sc),
             "barrier": lambda: agmm.ag_then_matmul(shards, b, bias, a_gathered=a_g, out=out,
-                                                   layout=layout)}
-        if layout == "k_contiguous":
+                                                   layout=layout, **sc)}
+        if layout == "k_contiguous" and not fp8:
             calls["chunked"] = lambda: agmm.ag_chunked_matmul(shards, b, bias, chunks=CHUNKS,
                                                               a_gathered=a_g, out=out)
         for fn in calls.values():
@@ -322,6 +331,9 @@ def run_sweep(args):
                           "D": w.D, "dtype": w.dtype, "fused_us": f_us, "barrier_us": b_us,
                           "speedup_vs_barrier": b_us / f_us,
                           "fused_tflops": w.flops / (f_us * 1e-6) / 1e12,
+                          # FP8: the measured bf16 peak x 2, the nominal dense ratio
+                          "fused_frac_of_peak": w.flops / (f_us * 1e-6) / 1e12
+                          / (peak16 * (2.0 if fp8 else 1.0)),
                           "host_us_fused": statistics.median(host["fused"]),
                           "host_us_barrier": statistics.median(host["barrier"]),
                           "chunked_us": statistics.median(dev["chunked"]) if "chunked" in dev
@@ -350,6 +362,9 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the bench line: fused vs barrier on every workload of the "
                          "parity configs, one JSON line each")
+    ap.add_argument("--only", default="",
+                    help="with --sweep: comma-separated substrings; keep workloads whose "
+                         "name contains one")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
