@@ -94,25 +94,6 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
                : "memory");
 }
 
-// Relaxed arrive on an mbarrier given by its shared::cluster address.
-__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
-}
-
-// As mbar_test_wait, acquiring at cluster scope.
-__device__ __forceinline__ bool mbar_test_wait_cluster(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // As mbar_try_wait, acquiring at cluster scope (for arrivals from the peer CTA).
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
@@ -220,12 +201,6 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 
 // ------------------------------------------------------------------ flags
 
-__device__ __forceinline__ uint64_t ld_acquire_gpu(const uint64_t* p) {
-  uint64_t v;
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
-
 __device__ __forceinline__ uint64_t ld_relaxed_gpu(const uint64_t* p) {
   uint64_t v;
   asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
@@ -234,16 +209,6 @@ __device__ __forceinline__ uint64_t ld_relaxed_gpu(const uint64_t* p) {
 
 __device__ __forceinline__ void st_relaxed_gpu(uint64_t* p, uint64_t v) {
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
-__device__ __forceinline__ void st_release_cta_shared(uint32_t addr, uint32_t v) {
-  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ uint32_t ld_acquire_cta_shared(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
 }
 
 __device__ __forceinline__ void st_release_gpu(uint64_t* p, uint64_t v) {
@@ -277,15 +242,6 @@ __device__ __forceinline__ void red_release_add_gpu(uint64_t* p, uint64_t v) {
 // The acquire-only fence does not wait for this thread's earlier stores.
 __device__ __forceinline__ void fence_acquire_gpu() {
   asm volatile("fence.acquire.gpu;" ::: "memory");
-}
-
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
 }
 
 // 16-byte global load that bypasses L1 allocation (streamed once).
