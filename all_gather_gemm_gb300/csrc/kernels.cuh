@@ -4,37 +4,38 @@
 // for iris.ops" (ROCm/iris #346, section "New kernel") -- A tiles are staged
 // into an HBM buffer, per-tile ready flags are published, GEMM workers wait on
 // the flags and compute tiles as soon as their rows are staged -- and maps it
-// onto one persistent sm_103a CTA per SM with specialised warps:
+// onto persistent sm_103a CTA pairs (clusters of two; one CTA per SM) with
+// specialised warps:
 //
-//   warp 0      TMA issuer.  Every (row block, k-group) chunk has an owner:
-//               the column block whose tile starts its k-loop there (tiles
-//               of one row block start at evenly spread k-groups).  The
-//               owner loads the chunk straight from the shard that holds it
-//               and has it staged; the other tiles of the row block follow:
-//               they wait on the chunk's ready flag (acquire loads, read one
-//               chunk ahead) and load the staged copy.  Chunks of the local
-//               shard are always read straight from it, never waited on.
-//   warp 1      MMA issuer: tcgen05.mma 128x256x16 (bf16/fp16 in, fp32
-//               accumulate) into one of two TMEM accumulators.
-//   warps 2-5   epilogue: tcgen05.ld, + fp32 bias, round to 16 bits,
-//               128-byte-swizzled shared memory, TMA store of the out tile.
-//   warp 6      register fetcher (fused only): copies chunks that TMA cannot
+//   warp 0      A issuer: the A loads and the ready-flag protocol.  Every
+//               (row block, k-group) chunk has an owner: the column block
+//               whose tile starts its k-loop there (tiles of one row block
+//               start at evenly spread k-groups).  The owner has the chunk
+//               staged (a tile ahead, where it can) and loads it; the other
+//               tiles of the row block follow: they wait on the chunk's
+//               ready flag (read one chunk ahead) and load the staged copy.
+//               Chunks of the local shard are read straight from it and
+//               never waited on.
+//   warp 1      MMA issuer (the pair's even CTA): tcgen05.mma.cta_group::2
+//               256 x 256 x 16 (bf16/fp16; FP8 E4M3: x 32) with fp32
+//               accumulation into one of two TMEM accumulators.
+//   warps 2-5   epilogue: tcgen05.ld, (FP8: x scale) + fp32 bias, round to
+//               16 bits, 128-byte-swizzled shared memory, TMA store.
+//   warp 6      B loader: b's k-blocks in the A issuer's order.
+//   warp 7      register fetcher (fused only): copies chunks that TMA cannot
 //               load from a single shard (a row block straddling shards whose
 //               row count is not a multiple of 8) and publishes them.
-//   warps 7-10  copiers (fused only), off the MMA pipeline.  When the issuer
-//               starts a chunk it stages, it hands the chunk's record to the
-//               copiers through a ring in shared memory; they copy the chunk's
-//               boxes (spread over the four warps) from its shard into
-//               a_gathered (the k-contiguous staging) -- and, for the
-//               m-contiguous layout, transposed into the [K, M] staging, which
-//               is what followers then read -- with 16-byte global loads and
-//               stores, and the last of them to finish publishes the chunk.
-//               The issuer loads the same boxes into the pipeline for its own
-//               MMAs as usual, so the pipeline is the plain GEMM's.
+//   warps 8-11  copiers (fused only), off the MMA pipeline.  The A issuer
+//               hands a chunk's record to them through a ring in shared
+//               memory; they copy the chunk's boxes (spread over the four
+//               warps) from its shard into a_gathered (the k-contiguous
+//               staging) -- and, for the m-contiguous layout, transposed into
+//               the [K, M] staging, which is what followers then read -- with
+//               16-byte global loads and stores, and the last of them to
+//               finish publishes the chunk.
 //
-// Each staged box is therefore read from its shard once, by the CTA that also
-// multiplies it ("fetch once, write through"), and no atomic sits on the
-// issuer's path.  If a follower finds a chunk unpublished while its owner
+// Each staged box is therefore read from its shard once, and no atomic sits
+// on the issuer's path.  If a follower finds a chunk unpublished while its owner
 // tile has not started yet (its CTA is still busy with an earlier tile, or the
 // grid is small), it takes the chunk over: one atom.max decides between
 // competing followers, and the winner loads, stages and publishes it.  A chunk
@@ -78,8 +79,8 @@ enum Mode : int { kGemmK = 0, kGemmM = 1, kFusedK = 2, kFusedM = 3 };
 
 __host__ __device__ constexpr bool mode_fused(int m) { return m >= kFusedK; }
 __host__ __device__ constexpr bool mode_layout_m(int m) { return m == kGemmM || m == kFusedM; }
-// Warp roles: 0 A loads (and, fused, the ready-flag protocol), 1 MMA (pair
-// peer: relay), 2..5 epilogue, 6 B loads; fused: 7 register fetcher, 8..11
+// Warp roles: 0 A loads (and, fused, the ready-flag protocol), 1 MMA (pair:
+// the even CTA's), 2..5 epilogue, 6 B loads; fused: 7 register fetcher, 8..11
 // copiers.
 constexpr int kBWarp = 2 + kEpiWarps;
 constexpr int kRegWarp = 3 + kEpiWarps;
@@ -295,7 +296,7 @@ __device__ __forceinline__ int chunk_boxes(const GemmParams& p, int g) {
   return min(p.kpf, p.num_kb - g * p.kpf);
 }
 
-// Per-tile facts the TMA issuer needs for every chunk, computed once per tile.
+// Per-tile facts the A issuer needs for every chunk, computed once per tile.
 struct TileCtx {
   int mb, nb;
   int sd, sy;      // segmented barrier GEMM: segment and first row of the block in it
@@ -684,7 +685,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
   const uint32_t full_c = kPair ? mapa_shared(smem_u32(&full[0]), 0) : 0u;
 
   if (warp == 0) {
-    // ---------------------------------------------------------- TMA issuer
+    // ---------------------------------------------------------- A issuer
     if (lane == 0) {
       uint32_t issued_mask = 0, issued_parity = 0;
       bool aborted = false;
