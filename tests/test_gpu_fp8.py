@@ -74,6 +74,7 @@ RAGGED = [
     (5, 130, 1040, 520, True),
     (8, 16, 256, 264, False),
     (7, 100, 3008, 40, True),
+    (16, 40, 128, 72, False),  # the maximum shard count
 ]
 
 

@@ -165,6 +165,7 @@ RAGGED = [
     (8, 16, 64, 64, "fp16"),
     (1, 300, 128, 1000, "bf16"),
     (7, 100, 3000, 40, "fp16"),
+    (16, 24, 136, 72, "bf16"),   # the maximum shard count; 8-row boxes straddle shards
 ]
 
 
