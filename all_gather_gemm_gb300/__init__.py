@@ -245,14 +245,16 @@ def ag_then_matmul(shards, b, bias=None, *, a_gathered=None, out=None, stream=No
 
 
 def ag_chunked_matmul(shards, b, bias=None, *, chunks: int = 4, a_gathered=None, out=None,
-                      stream=None, num_sms: int = 0, timeout_ns: int = 0):
+                      stream=None, num_sms: int = 0, timeout_ns: int = 0, scale_a: float = 1.0,
+                      scale_b: float = 1.0):
     """Chunked pipeline: chunk s = the s-th sub-block of every shard; per chunk
     (four streams round-robin) gather it, then multiply its rows.  Returns
     (a_gathered, out); bitwise equal to ag_then_matmul's."""
     if chunks < 1:
         raise ValueError("chunks must be >= 1")
     return _call(False, shards, b, bias, a_gathered, out, stream, "k_contiguous", 0, 0,
-                 num_sms, timeout_ns, -1, None, None, chunks=chunks)
+                 num_sms, timeout_ns, -1, None, None, chunks=chunks, scale_a=scale_a,
+                 scale_b=scale_b)
 
 
 def device_error(stream=None):

@@ -643,7 +643,8 @@ int gemm_segments(DevState& ds, const Shape& s, int lo, int hi, const void* a_ga
   if ((st = make_map3(&p.tm_a, a_base, (uint64_t)s.K, (uint64_t)seg_rows, (uint64_t)s.D,
                       (uint64_t)s.mps, kBK, kBM)) != AG_OK)
     return st;
-  if ((st = make_map(&p.tm_b, b, (uint64_t)s.N, (uint64_t)s.K, 64, kBK)) != AG_OK) return st;
+  const bool fp8 = o.dtype == AG_DTYPE_FP8_E4M3;  // s.K counts 16-bit words (see run)
+  if (!fp8 && (st = make_map(&p.tm_b, b, (uint64_t)s.N, (uint64_t)s.K, 64, kBK)) != AG_OK) return st;
   if ((st = make_map3(&p.tm_out, out_base, (uint64_t)s.N, (uint64_t)seg_rows, (uint64_t)s.D,
                       (uint64_t)s.mps, kEpiCols, kEpiRows)) != AG_OK)
     return st;
@@ -668,6 +669,14 @@ int gemm_segments(DevState& ds, const Shape& s, int lo, int hi, const void* a_ga
   p.fp16 = o.dtype == AG_DTYPE_FP16 ? 1 : 0;
   p.inject_skip_flag = -1;
   const int grid = plan_launch(p, sc, cap, ds.pair_clusters, false, false, o.k_per_flag, 0);
+  if (fp8) {
+    if ((st = make_map(&p.tm_b, b, (uint64_t)s.K, (uint64_t)s.N, kBK, p.pair ? kBN / 2 : kBN)) !=
+        AG_OK)
+      return st;
+    p.scale_ab = o.scale_a * o.scale_b;
+    return p.pair ? launch<kGemmK, true, true>(grid, stream, p, "gemm kernel (chunk, fp8)")
+                  : launch<kGemmK, false, true>(grid, stream, p, "gemm kernel (chunk, fp8)");
+  }
   return p.pair ? launch<kGemmK, true>(grid, stream, p, "gemm kernel (chunk)")
                 : launch<kGemmK, false>(grid, stream, p, "gemm kernel (chunk)");
 }
@@ -678,7 +687,10 @@ int run_chunked(const void** a_shards, int D, int m_per_shard, int K, const void
   ag_options o;
   ag_options_default(&o);
   if (opt_in) o = *opt_in;
-  if (o.dtype == AG_DTYPE_FP8_E4M3) return AG_ERR_UNSUPPORTED;
+  if (o.dtype == AG_DTYPE_FP8_E4M3) {  // moved as K/2 16-bit words, as in run()
+    if (K < 16 || K % 16) return AG_ERR_INVALID_ARG;
+    K /= 2;
+  }
   Shape s;
   int st = validate(a_shards, D, m_per_shard, K, b, N, bias, a_gathered, out, o, false, &s);
   if (st != AG_OK) return st;
@@ -794,6 +806,12 @@ int noalloc_setup(NoAllocState& ns, int dev) {
   AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kFusedK, true, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Pipe<true>::kSmemBytes));
+  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kFusedK, false, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Pipe<false>::kSmemBytes));
+  AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kFusedK, true, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Pipe<true>::kSmemBytes));
   if (int st = query_pair_clusters(sms, &ns.pair_clusters)) return st;
   void* ptr = nullptr;
   AG_CK(cudaGetSymbolAddress(&ptr, g_noalloc_scratch));
@@ -830,8 +848,12 @@ int run_noalloc(const void** a_shards, int D, int m_per_shard, int K, const void
   ag_options_default(&o);
   if (opt_in) o = *opt_in;
   if (o.workspace) return AG_ERR_INVALID_ARG;  // the scratch is fixed
-  if (o.dtype == AG_DTYPE_FP8_E4M3) return AG_ERR_UNSUPPORTED;
   if (o.layout != AG_LAYOUT_K_CONTIGUOUS) return AG_ERR_UNSUPPORTED;
+  const bool fp8 = o.dtype == AG_DTYPE_FP8_E4M3;
+  if (fp8) {  // moved as K/2 16-bit words, as in run()
+    if (K < 16 || K % 16) return AG_ERR_INVALID_ARG;
+    K /= 2;
+  }
   Shape s;
   int st = validate(a_shards, D, m_per_shard, K, b, N, bias, a_gathered, out, o, true, &s);
   if (st != AG_OK) return st;
@@ -854,7 +876,7 @@ int run_noalloc(const void** a_shards, int D, int m_per_shard, int K, const void
   GemmParams p;
   memset(&p, 0, sizeof p);
   if ((st = make_map(&p.tm_a, a_gathered, (uint64_t)K, (uint64_t)s.M, kBK, kBM)) != AG_OK) return st;
-  if ((st = make_map(&p.tm_b, b, (uint64_t)N, (uint64_t)K, 64, kBK)) != AG_OK) return st;
+  if (!fp8 && (st = make_map(&p.tm_b, b, (uint64_t)N, (uint64_t)K, 64, kBK)) != AG_OK) return st;
   if ((st = make_map(&p.tm_out, out, (uint64_t)N, (uint64_t)s.M, kEpiCols, kEpiRows)) != AG_OK)
     return st;
   const bool straddle8 = D > 1 && (m_per_shard % kBM) != 0 && (m_per_shard % 8) == 0;
@@ -896,6 +918,14 @@ int run_noalloc(const void** a_shards, int D, int m_per_shard, int K, const void
   const int grid = plan_launch(p, s, cap, ns.pair_clusters, true, false, o.k_per_flag, o.rank);
   p.fp16 = o.dtype == AG_DTYPE_FP16 ? 1 : 0;
   p.inject_skip_flag = o.inject_skip_flag;
+  if (fp8) {
+    if ((st = make_map(&p.tm_b, b, (uint64_t)K, (uint64_t)N, kBK, p.pair ? kBN / 2 : kBN)) !=
+        AG_OK)
+      return st;
+    p.scale_ab = o.scale_a * o.scale_b;
+    return p.pair ? launch<kFusedK, true, true>(grid, stream, p, "fused kernel (no-alloc, fp8)")
+                  : launch<kFusedK, false, true>(grid, stream, p, "fused kernel (no-alloc, fp8)");
+  }
   return p.pair ? launch<kFusedK, true>(grid, stream, p, "fused kernel (no-alloc)")
                 : launch<kFusedK, false>(grid, stream, p, "fused kernel (no-alloc)");
 }

@@ -102,8 +102,8 @@ typedef enum ag_status {
  *   out          [M, N] bf16:  out = bf16(scale_a * scale_b * (a @ b) + bias),
  *                products and sums in fp32, the scale applied to the fp32 sum;
  *   K % 16 == 0 (16-byte rows), N % 8 == 0, layout k-contiguous only (the
- *   m-contiguous staging, ag_chunked_matmul_ex and ag_matmul_noalloc return
- *   AG_ERR_UNSUPPORTED for it). */
+ *   m-contiguous staging returns AG_ERR_UNSUPPORTED for it); every entry
+ *   point (fused, barrier, chunked, no-alloc) accepts it. */
 typedef enum ag_dtype { AG_DTYPE_BF16 = 0, AG_DTYPE_FP16 = 1, AG_DTYPE_FP8_E4M3 = 2 } ag_dtype;
 
 /* Layout of the staged A in HBM ("Fused all-gather+GEMM HBM-buffer kernel for

@@ -162,9 +162,6 @@ def test_fp8_rejections():
         agmm.ag_matmul(shards, bt, layout="m_contiguous")
     assert e.value.status == 2  # unsupported
     with pytest.raises(agmm.AgmmError) as e:
-        agmm.ag_chunked_matmul(shards, bt)
-    assert e.value.status == 2
-    with pytest.raises(agmm.AgmmError) as e:
         agmm.ag_matmul(shards, bt, scale_a=float("inf"))
     assert e.value.status == 1  # invalid
     odd = [torch.randn(64, 24, generator=g).to(torch.float8_e4m3fn).cuda() for _ in range(2)]
@@ -172,3 +169,20 @@ def test_fp8_rejections():
         agmm.ag_matmul(odd, torch.randn(64, 24, generator=g).to(torch.float8_e4m3fn).cuda())
     assert e.value.status == 1  # K % 16 != 0
     assert agmm.device_error() == (0, 0)
+
+
+@pytest.mark.parametrize("chunks", [1, 3])
+def test_fp8_chunked_pipeline_equals_barrier(oracle_mod, chunks):
+    """The chunked pipeline runs the barrier's GEMM core (k ascending) per chunk,
+    so its FP8 result is bitwise the barrier's."""
+    w = inp.Workload("fp8_chunked", D=3, m_per_shard=384, K=512, N=264, dtype="fp8_e4m3",
+                     a_dist="normal", b_dist="normal", b_scale="one", bias=True, scale_b=0.04)
+    x = inp.make_inputs(w)
+    shards = [s.cuda() for s in x.shards]
+    bias = x.bias.cuda()
+    a_c, o_c = agmm.ag_chunked_matmul(shards, x.b.cuda(), bias, chunks=chunks,
+                                      scale_a=w.scale_a, scale_b=w.scale_b)
+    assert agmm.device_error() == (0, 0)
+    a_b, o_b = run(x, fused=False)
+    assert torch.equal(o_c, o_b)
+    check(oracle_mod, x, [(a_c, o_c, f"chunked {chunks}")])

@@ -114,3 +114,31 @@ def test_noalloc_device_timeout_is_reported():
     assert agmm.device_error() == (0, 0)
     ref_a, ref_out = agmm.ag_matmul(shards, b, rank=1)
     assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+
+
+def test_noalloc_fp8_matches_ag_matmul():
+    """FP8 E4M3 (b given as [N, K], bf16 out) through the no-alloc entry: the
+    same fused kernel as ag_matmul, so the results are bitwise equal."""
+    w = inp.Workload("noalloc_fp8", D=4, m_per_shard=256, K=1024, N=768, dtype="fp8_e4m3",
+                     b_scale="one", bias=True, scale_b=0.03)
+    x = inp.make_inputs(w)
+    shards = [s.cuda() for s in x.shards]
+    bt, bias = x.b.cuda(), x.bias.cuda()
+    a_g = torch.empty(w.M, w.K, dtype=bt.dtype, device="cuda")
+    out = torch.empty(w.M, w.N, dtype=torch.bfloat16, device="cuda")
+    opt = agmm.default_options()
+    opt.dtype, opt.rank = agmm.DTYPES["fp8_e4m3"], 1
+    opt.scale_a, opt.scale_b = w.scale_a, w.scale_b
+    lib = agmm.library()
+    arr = (ctypes.c_void_p * w.D)(*[ctypes.c_void_p(s.data_ptr()) for s in shards])
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert lib.ag_matmul_noalloc(arr, w.D, w.m_per_shard, w.K, ctypes.c_void_p(bt.data_ptr()),
+                                 w.N, ctypes.c_void_p(bias.data_ptr()),
+                                 ctypes.c_void_p(a_g.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+                                 stream, ctypes.byref(opt)) == 0
+    assert agmm.device_error() == (0, 0)
+    ref_a, ref_out = agmm.ag_matmul(shards, bt, bias, rank=1, scale_a=w.scale_a,
+                                    scale_b=w.scale_b)
+    assert agmm.device_error() == (0, 0)
+    assert torch.equal(a_g.view(torch.uint8), ref_a.view(torch.uint8))
+    assert torch.equal(out, ref_out)
