@@ -1045,7 +1045,7 @@ const char* ag_status_string(int status) {
   switch (status) {
     case AG_OK: return "ok";
     case AG_ERR_INVALID_ARG: return "invalid argument";
-    case AG_ERR_UNSUPPORTED: return "unsupported by this build or device";
+    case AG_ERR_UNSUPPORTED: return "unsupported by the library or the device";
     case AG_ERR_CUDA: return t_cuda_msg;
     case AG_ERR_TIMEOUT: return "device-side wait timed out";
     case AG_ERR_WORKSPACE: return "caller workspace too small";

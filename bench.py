@@ -4,8 +4,8 @@ One step = one ag_matmul call over the whole workload: the fused persistent
 kernel gathers D row shards into a_gathered and computes out = a_gathered @ b.
 Default workload: M=16384 N=3584 K=8192 fp16 in 8 row shards of 2048x8192
 (the largest shape of the Iris HBM-buffer result tables), k-contiguous
-staging, local rank 0.  Inputs are synthetic and seeded (see
-all_gather_gemm_gb300/inputs.py).
+staging, local rank 0; --workload fp8_m16384_d8 runs its FP8 E4M3 form.
+Inputs are synthetic and seeded (see all_gather_gemm_gb300/inputs.py).
 
 Reported (one JSON line on rank 0):
   value        fused TFLOPS = 2*M*N*K / mean device time per step (CUDA events
@@ -13,14 +13,18 @@ Reported (one JSON line on rank 0):
   ms_per_step  that mean time; barrier_* keys give the gather-then-GEMM
                baseline (ag_then_matmul) timed the same way, interleaved
   roofline     achieved TFLOPS of the fused kernel against the measured bf16
-               tensor peak (fp16 runs at the same nominal rate)
+               burst tensor peak (fp16: the same nominal rate; FP8: x 2), the
+               fraction of the sustained peak beside it, and the kernel's DRAM
+               traffic from the committed ncu summary (null once the kernel
+               sources change)
   e2e          the same metric through the public API from pinned host
                buffers: H2D of the shards and b, the call, D2H of out
   cpu_baseline the CPU oracle (as it stands) on a bounded row sample
-  clocks       nvidia-smi samples taken during the timed region
+  clocks       nvidia-smi samples whose timestamps fall in the timed region
 
---impl reference times the CPU oracle instead (the reference arm of this
-build: there is no installable reference implementation).
+--sweep prints one line per parity workload (fused, barrier, chunked
+pipeline), --only narrows it.  --impl reference times the CPU oracle instead:
+the pages' method has no installable implementation to run.
 Multi-GPU: replicas only -- under torchrun each rank runs the same problem on
 its own GPU; value = all ranks' FLOPs / the slowest rank's time.
 """

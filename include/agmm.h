@@ -84,7 +84,7 @@ extern "C" {
 typedef enum ag_status {
   AG_OK = 0,
   AG_ERR_INVALID_ARG = 1, /* bad pointer, size, alignment, overlap or option value */
-  AG_ERR_UNSUPPORTED = 2, /* valid request this build cannot run (device, dtype/layout combo, D > AG_MAX_SHARDS) */
+  AG_ERR_UNSUPPORTED = 2, /* valid request the library cannot run (device, dtype/layout combo, D > AG_MAX_SHARDS) */
   AG_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed; see ag_status_string */
   AG_ERR_TIMEOUT = 4,     /* device-side: a bounded wait ran out (reported by ag_get_device_error) */
   AG_ERR_WORKSPACE = 5,   /* caller workspace smaller than ag_workspace_size() */
