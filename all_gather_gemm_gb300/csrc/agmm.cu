@@ -35,6 +35,7 @@ constexpr int64_t kDefaultTimeoutNs = 2000000000LL;
 // owners' longer first chunks are covered by staging ahead).
 constexpr int kAutoKpfOneWave = 4, kAutoKpfOneWaveMax = 8, kAutoKpfK = 8, kAutoKpfM = 16;
 
+
 // log2 of the row count of the boxes that load a row block straddling shards:
 // the largest of 64, 32, 16, 8 rows dividing m_per_shard (3 if none does; such
 // blocks are then copied by the register fetcher instead).
@@ -334,7 +335,29 @@ int plan_launch(GemmParams& p, const Shape& s, int cap, int pair_clusters, bool 
   p.mb_start = fused ? (int)(((int64_t)rank * s.mps) / kBM) >> p.pair : 0;
   p.ng = schedule_group(sched, units);
   p.w0 = std::min(p.ng, s.num_nb);
-  return std::max(1, std::min(units, sched.num_mb * s.num_nb)) << p.pair;
+  const int tiles = sched.num_mb * s.num_nb;  // tiles (pairs: pair tiles), one unit each
+  const int grid_units = std::max(1, std::min(units, tiles));
+  // Fetch prologue.  When a k-contiguous fused call takes two or three waves
+  // and the last one is partial, the units with one tile fewer than the rest
+  // have a tile's time to spare: their copier and epilogue warps stage all of
+  // A first (about 256 KB per CTA at most), in k-group order with ready
+  // flags, while the other units start their tiles and wait on those flags.
+  // No tile owns a window then (w0 = 0: k ascending, as in the barrier GEMM).
+  // m_per_shard % 8 == 0 keeps the register fetcher, which publishes its own
+  // chunks, out of it.  Measured on the cube workloads that qualify (n = 2176
+  // ... 3328, D = 8): the owner protocol's first wave waited about 8 us for
+  // chunks copied beside the GEMM's own loads.
+  p.pro_cta0 = -1;
+  if (fused && !layout_m && (s.mps % 8) == 0 && tiles > grid_units &&
+      tiles % grid_units != 0 && tiles <= 3 * grid_units) {
+    const int fetch_ctas = (grid_units - tiles % grid_units) << p.pair;
+    const int64_t a_bytes = s.M * (int64_t)s.num_kb * kBK * 2;
+    if (fetch_ctas >= 16 && a_bytes <= (int64_t)fetch_ctas * (256 << 10)) {
+      p.pro_cta0 = (tiles % grid_units) << p.pair;
+      p.w0 = 0;
+    }
+  }
+  return grid_units << p.pair;
 }
 
 // A 3-D view of D equal row segments, `rows` x `inner` each, `seg_stride`

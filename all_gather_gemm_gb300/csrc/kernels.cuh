@@ -70,6 +70,7 @@ constexpr int kEpiBufBytes = kEpiRows * kEpiCols * 2;  // 4 KB
 constexpr int kEpiBufs = 2;
 constexpr int kTmemCols = 2 * kBN;
 constexpr int kCopyWarps = 4;  // fused kernel: warps copying staged chunks
+constexpr int kProWarps = kCopyWarps + kEpiWarps;  // warps of the fetch prologue
 constexpr int kMaxShards = 16;
 constexpr int kFlagShift = 20;      // flag base = epoch << 20; boxes per chunk < 2^20
 
@@ -113,8 +114,8 @@ struct Pipe {
   static constexpr int kStageBytes = kAStageBytes + kBStageBytes;
   static constexpr int kData = kStages * kStageBytes + kEpiWarps * kEpiBufs * kEpiBufBytes;
   // full, empty [kStages]; tmem_full, tmem_empty [2]; drain; rfull, rfree
-  // [kRing]
-  static constexpr int kBars = 2 * kStages + 4 + 1 + 2 * kRing;
+  // [kRing]; pro (fetch prologue done)
+  static constexpr int kBars = 2 * kStages + 4 + 1 + 2 * kRing + 1;
   static constexpr int kSmemBytes =
       1024 + kData + 8 * kBars + 4 * kStages + 4 * kRing * kRingWords + 16 + 64;
   static_assert(kSmemBytes <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
@@ -124,7 +125,8 @@ struct Pipe {
 constexpr uint32_t kErrTimeout = 4;
 // Sites reported with a pipeline timeout (ready-flag timeouts report the flag index).
 constexpr uint32_t kSiteEmpty = 0xF00001, kSiteFull = 0xF00002, kSiteTmemEmpty = 0xF00003,
-                   kSiteTmemFull = 0xF00004, kSiteRing = 0xF00005, kSiteCopy = 0xF00006;
+                   kSiteTmemFull = 0xF00004, kSiteRing = 0xF00005, kSiteCopy = 0xF00006,
+                   kSitePro = 0xF00007;
 
 // Trace roles (see include/agmm.h).
 constexpr uint32_t kTraceClaim = 1, kTraceWait = 2, kTraceTile = 3, kTraceGather = 4,
@@ -164,6 +166,7 @@ struct GemmParams {
   int fp16;                 // 1: fp16, 0: bf16 (the output's type for FP8 inputs)
   float scale_ab;           // FP8 inputs: scale_a * scale_b, applied to the fp32 sum
   int inject_skip_flag;     // this flag index is never published (fault injection)
+  int pro_cta0;             // fetch prologue: CTAs from this index stage every chunk first (-1: off)
 };
 
 struct GatherParams {
@@ -459,6 +462,69 @@ __device__ __forceinline__ const uint16_t* shard_row(const uint16_t* const* shar
   return shards[s] + (int64_t)lr * K;
 }
 
+// Fetch prologue: copy box kb (64 columns) of row block mb from the shards
+// into a_gathered, one warp per box.  Lane = (row-group quarter, 16-byte
+// column chunk): four 8-row groups per lane, all 32 loads in flight before
+// the first store.  Needs m_per_shard % 8 == 0 (no 8-row group straddles).
+__device__ __forceinline__ void prologue_copy_box(const GemmParams& p, int mb, int kb, int lane) {
+  const int k = kb * kBK + (lane & 7) * 8;
+  if (k >= p.K) return;  // K % 8 == 0: a column chunk is all in or all out
+  uint4 v[4][8];
+  int m[4];
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    m[h] = mb * kBM + (4 * h + (lane >> 3)) * 8;
+    const int nrow = min(8, p.M - m[h]);
+    if (nrow > 0) {
+      const uint16_t* src = shard_row(p.shards, p.mps, p.K, m[h]) + k;
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+        if (r < nrow) v[h][r] = ld_stream_v4(src + (int64_t)r * p.K);
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    const int nrow = min(8, p.M - m[h]);
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+      if (r < nrow) st_v4(p.a_gathered + (int64_t)(m[h] + r) * p.K + k, v[h][r]);
+  }
+}
+
+// Fetch prologue (calls whose last wave is partial; p.pro_cta0 >= 0): the
+// CTAs with one tile fewer than the others stage every chunk of A before
+// their own tiles, k-group by k-group (the order in which the tiles read
+// them), chunk c by prologue CTA c mod (their number).  The copier and the
+// epilogue warps (pw = 0 .. kProWarps - 1) split a chunk's boxes; once all of
+// them are through (named barrier 1), one thread publishes it.  Nothing here
+// waits on another CTA, so every chunk is published whatever the pipelines
+// do.  Every one of those warps then arrives on pro_bar (all CTAs).
+__device__ __forceinline__ void fetch_prologue(const GemmParams& p, int pw, int lane,
+                                               uint64_t* pro_bar) {
+  if (p.pro_cta0 >= 0 && (int)blockIdx.x >= p.pro_cta0) {
+    const int nf = (int)gridDim.x - p.pro_cta0;
+    const int total = p.num_mb * p.G;
+    for (int c = (int)blockIdx.x - p.pro_cta0; c < total; c += nf) {
+      const uint64_t t0 = p.trace ? globaltimer_ns() : 0;
+      const int g = c / p.num_mb;
+      const int mb = c - g * p.num_mb;
+      const int nbox = chunk_boxes(p, g);
+      for (int j = pw; j < nbox; j += kProWarps) prologue_copy_box(p, mb, g * p.kpf + j, lane);
+      __threadfence();
+      fence_proxy_async_global();
+      named_bar_sync(1, kProWarps * 32);
+      if (pw == 0 && lane == 0) {
+        const int flag_idx = mb * p.G + g;
+        if (flag_idx != p.inject_skip_flag)
+          st_release_gpu(p.flags + flag_idx, p.fbase + (uint64_t)nbox);
+        if (p.trace) trace_rec(p.trace, p.trace_words, kTraceGather, mb, g, t0, globaltimer_ns());
+      }
+    }
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(pro_bar);
+}
+
 // ------------------------------------------------------------------ register fetcher
 
 // Stage one chunk of a row block TMA cannot load from the shards (it straddles
@@ -637,7 +703,8 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
   uint64_t* drain = tmem_empty + 2;          // [1] final MMA drain
   uint64_t* rfull = drain + 1;               // [kRing] fused: chunk record written
   uint64_t* rfree = rfull + kRing;           // [kRing] fused: every copier is done with it
-  uint32_t* info = reinterpret_cast<uint32_t*>(rfree + kRing);  // [kStages]
+  uint64_t* pro_bar = rfree + kRing;         // [1] fused: this CTA's fetch prologue is done
+  uint32_t* info = reinterpret_cast<uint32_t*>(pro_bar + 1);  // [kStages]
   uint32_t* ring = info + kStages;                // [kRing][kRingWords] chunk records
   volatile uint32_t* iseq = ring + kRing * kRingWords;  // issuer progress (chunks), a liveness signal
   uint32_t* tmem_slot = ring + kRing * kRingWords + 1;
@@ -657,6 +724,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
       mbar_init(&rfull[r], 1);
       mbar_init(&rfree[r], kCopyWarps);
     }
+    mbar_init(pro_bar, kProWarps);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tmem_full[b], 1);
       // one arrive per epilogue warp (pair: the leader's barrier takes both CTAs')
@@ -722,6 +790,11 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
         if (t + (int)gridDim.x < p.num_tiles) tile_ctx<kFused>(p, t + gridDim.x, nxt);
       }
       const int last_nbox = chunk_boxes(p, p.G - 1);
+      // A CTA that runs the fetch prologue loads nothing (A here, B in the B
+      // loader) before it is through (the copies have the SM to themselves).
+      if (kFused && !kLayoutM && p.pro_cta0 >= 0 && (int)blockIdx.x >= p.pro_cta0 &&
+          !wait_bar(p, pro_bar, 0u, abort_flag, kSitePro))
+        aborted = true;
       while (t < p.num_tiles && !aborted) {
         const uint64_t t_chunk = p.trace ? globaltimer_ns() : 0;
         if (kFused && gi == 0) {
@@ -778,8 +851,9 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
               fence_acquire_gpu();  // the relaxed read saw it published: make it an acquire
             } else {
               const uint64_t t0 = p.trace ? globaltimer_ns() : 0;
+              // (with the fetch prologue nobody owns a chunk: wait only)
               const int owner_tile =
-                  (kind == kDirect || (kAllStaged && kind == kLocal))
+                  p.pro_cta0 < 0 && (kind == kDirect || (kAllStaged && kind == kLocal))
                       ? tile_index(p, mb, owner_nb(p, g)) : -1;
               if (wait_or_take(p, flag_idx, target, owner_tile)) {
                 if constexpr (kAllStaged) {
@@ -1046,6 +1120,8 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
     __syncwarp();
   } else if (warp < 2 + kEpiWarps) {
     // ---------------------------------------------------------- epilogue
+    // (fetch prologue first: these warps have nothing to drain before it ends)
+    if constexpr (kFused && !kLayoutM) fetch_prologue(p, kCopyWarps + warp - 2, lane, pro_bar);
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     uint8_t* my_bufs = epi_smem + (warp - 2) * kEpiBufs * kEpiBufBytes;
     const uint32_t my_bufs_u32 = smem_u32(my_bufs);
@@ -1143,6 +1219,9 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
       bool aborted = false;
       int stage = 0;
       uint32_t phase = 0;
+      if (kFused && !kLayoutM && p.pro_cta0 >= 0 && (int)blockIdx.x >= p.pro_cta0 &&
+          !wait_bar(p, pro_bar, 0u, abort_flag, kSitePro))
+        aborted = true;
       for (int t = blockIdx.x; t < p.num_tiles && !aborted; t += gridDim.x) {
         int mb, nb;
         tile_coords(p, t, mb, nb);
@@ -1200,6 +1279,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
     // scope); the one that completes it publishes the chunk (release, GPU
     // scope), so the flag follows every copier's writes.
     const int w = warp - kCopyWarp0;
+    if constexpr (!kLayoutM) fetch_prologue(p, w, lane, pro_bar);
     const int ch = lane & 7;  // 16-byte column chunk of a 128-byte box row
     for (uint32_t n = 0;; ++n) {
       const int slot = (int)(n % kRing);

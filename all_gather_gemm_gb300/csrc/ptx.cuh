@@ -238,6 +238,11 @@ __device__ __forceinline__ void red_release_add_gpu(uint64_t* p, uint64_t v) {
   asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
+// Named barrier `id` over `count` threads (a multiple of 32) of the CTA.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Turns an earlier relaxed read of a flag into an acquire (fence pattern).
 // The acquire-only fence does not wait for this thread's earlier stores.
 __device__ __forceinline__ void fence_acquire_gpu() {

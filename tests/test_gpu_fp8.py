@@ -108,6 +108,20 @@ def test_fp8_small_grids(oracle_mod, num_sms):
                           (*run(x, fused=False, num_sms=num_sms), "barrier")])
 
 
+def test_fp8_fetch_prologue(oracle_mod):
+    """On 40 SMs this call takes two waves, the second partial: the CTAs with
+    one tile fewer stage all of A first (the fetch prologue).  k then runs in
+    ascending order, as in the barrier GEMM, so the two agree bitwise."""
+    w = inp.Workload("fp8_prologue", D=4, m_per_shard=384, K=1040, N=1024, dtype="fp8_e4m3",
+                     a_dist="uniform", b_dist="uniform", b_scale="one", bias=True,
+                     scale_a=0.75, scale_b=0.5)
+    x = inp.make_inputs(w)
+    a_f, o_f = run(x, rank=2, num_sms=40)
+    a_b, o_b = run(x, fused=False)
+    assert torch.equal(o_f, o_b), "fused (prologue) and barrier differ"
+    check(oracle_mod, x, [(a_f, o_f, "fused, fetch prologue"), (a_b, o_b, "barrier")])
+
+
 def test_fp8_integer_inputs_exact():
     """Integers in [-8, 8] and K=512: the fp32 sums are exact, so out must be
     the bf16 rounding of the exact integer result (scaled by 2 * 0.25)."""

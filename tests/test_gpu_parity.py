@@ -242,6 +242,49 @@ def test_small_grids_and_flag_granularity(oracle_mod, num_sms, kpf):
         check(oracle_mod, x, a_f, o_f, what=f"num_sms={num_sms} kpf={kpf} rank={rank}")
 
 
+# (D, m_per_shard, K, N, dtype, bias, rank): on 40 SMs (20 CTA pairs) each takes
+# between one and three waves with a partial last one, so the CTAs with one
+# tile fewer run the fetch prologue; ragged K and N, a half-empty last pair,
+# row blocks straddling shards (64- and 8-row boxes) and a non-zero rank.
+PROLOGUE = [
+    (4, 384, 520, 1024, "bf16", True, 0),
+    (8, 200, 256, 776, "fp16", False, 5),
+    (2, 704, 136, 1800, "bf16", False, 1),
+]
+
+
+@pytest.mark.parametrize("D,m,K,N,dt,bias,rank", PROLOGUE)
+def test_fetch_prologue(oracle_mod, D, m, K, N, dt, bias, rank):
+    """Calls with a partial last wave: the CTAs with fewer tiles stage every
+    chunk of A before their own tiles (trace role 4, each exactly once), the
+    others wait on those flags; results as the oracle (so are those of the
+    same call on all SMs: one wave, no prologue) and bitwise equal to the
+    barrier path (k ascending in both)."""
+    w = inp.Workload(f"prologue_{D}_{m}_{K}_{N}", D=D, m_per_shard=m, K=K, N=N, dtype=dt,
+                     a_dist="uniform", b_dist="uniform", bias=bias)
+    x = inp.make_inputs(w)
+    shards, b, bias_d = to_device(x)
+    tr = torch.zeros(1 + 4 * 16384, dtype=torch.int64, device="cuda")
+    a_f, o_f = agmm.ag_matmul(shards, b, bias_d, rank=rank, num_sms=40, trace=tr)
+    a_b, o_b = agmm.ag_then_matmul(shards, b, bias_d)
+    a_1, o_1 = agmm.ag_matmul(shards, b, bias_d, rank=rank)
+    torch.cuda.synchronize()
+    assert agmm.device_error() == (0, 0)
+    t = tr.cpu().numpy().view(np.uint64)
+    n = int(t[0])
+    assert n <= 16384
+    rec = t[1:1 + 4 * n].reshape(-1, 4)
+    pro = rec[(rec[:, 2] >> np.uint64(56)) == 4]
+    num_mb, num_kb = -(-w.M // 128), -(-K // 64)
+    G = -(-num_kb // 8)  # automatic k_per_flag for more than one wave: 8
+    keys = sorted((((pro[:, 2] >> np.uint64(20)) & np.uint64(0xFFFFF)) * np.uint64(G)
+                   + (pro[:, 2] & np.uint64(0xFFFFF))).tolist())
+    assert keys == list(range(num_mb * G)), "every chunk staged once by the prologue"
+    check(oracle_mod, x, a_f, o_f, what="fused, fetch prologue",
+          more=((a_b, o_b, "barrier"), (a_1, o_1, "fused, all SMs")))
+    assert_bitwise(o_f, o_b, "prologue vs barrier")
+
+
 @pytest.mark.parametrize("num_sms", [1, 2, 3, 7, 0])
 @pytest.mark.parametrize("layout", ["k_contiguous", "m_contiguous"])
 def test_barrier_small_grids_odd_row_blocks(oracle_mod, num_sms, layout):
