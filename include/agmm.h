@@ -20,10 +20,13 @@
  * from the shards into an HBM staging buffer and per-tile ready flags are
  * published, while tensor-core warps wait on those flags and compute each
  * output tile as soon as its A rows are staged -- no whole-gather barrier.
- * Here the first CTA that needs a chunk of A loads it from its shard with TMA
- * for its own MMA and stores that same shared-memory copy into the staging
- * buffer; the other CTAs wait on the chunk's flag and read the staged copy.
- * Tiles that lie inside the local shard (option `rank`) are read straight from
+ * Here every chunk of A (a 128-row block x k_per_flag k-blocks) has an owner
+ * tile, which loads it from its shard with TMA for its own MMA and hands it
+ * to its CTA's copier warps; they copy it into the staging buffer and publish
+ * its flag, and the other tiles wait on that flag and read the staged copy.
+ * When a call takes at most three waves and the last one is partial, the CTAs
+ * with one tile fewer copy all of A first instead, and every tile waits on the
+ * flags.  Tiles that lie inside the local shard (option `rank`) are read straight from
  * that shard without waiting (the local-tile shortcut described in the Helion
  * PR).  ag_then_matmul is the barrier baseline of the Iris result tables
  * ("Baseline" column): gather everything, then run the GEMM.
