@@ -26,10 +26,11 @@
  * its flag, and the other tiles wait on that flag and read the staged copy.
  * When a call takes at most three waves and the last one is partial, the CTAs
  * with one tile fewer copy all of A first instead, and every tile waits on the
- * flags.  Tiles that lie inside the local shard (option `rank`) are read straight from
- * that shard without waiting (the local-tile shortcut described in the Helion
- * PR).  ag_then_matmul is the barrier baseline of the Iris result tables
- * ("Baseline" column): gather everything, then run the GEMM.
+ * flags.  Tiles that lie inside the local shard (option `rank`) are read
+ * straight from that shard without waiting (the local-tile shortcut
+ * described in the Helion PR).  ag_then_matmul is the barrier baseline of the
+ * Iris result tables ("Baseline" column): gather everything, then run the
+ * GEMM.
  *
  * Common argument contract (every entry point below that takes these):
  *   a_shards      HOST array of D DEVICE pointers; shard r is row-major
