@@ -42,6 +42,11 @@
 // staged twice (owner and taker) is harmless: both write identical bytes and
 // publish the same value, and each publishes only after all of its own writes.
 //
+// Fetch prologue: when a k-contiguous call takes at most three waves and the
+// last is partial, the CTAs with one tile fewer first copy all of A (their
+// copier and epilogue warps, chunk by chunk in k-group order) and publish it;
+// no tile owns a chunk then, every tile runs k ascending and waits on flags.
+//
 // Flags are 64-bit.  A call with epoch e uses base = e << 20: a flag below base
 // is untouched by this call, base means taken over, base + boxes means
 // published (ready).  Nothing is cleared between calls.  Every wait is bounded
