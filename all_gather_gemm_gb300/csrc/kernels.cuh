@@ -172,6 +172,7 @@ struct GemmParams {
   float scale_ab;           // FP8 inputs: scale_a * scale_b, applied to the fp32 sum
   int inject_skip_flag;     // this flag index is never published (fault injection)
   int pro_cta0;             // fetch prologue: CTAs from this index stage every chunk first (-1: off)
+  int l2_prefetch;          // 1: each CTA prefetches its share of the shards into L2 at the start
 };
 
 struct GatherParams {
@@ -1269,6 +1270,25 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
     __syncwarp();
   } else if (kFused && warp == kRegWarp) {
     // ---------------------------------------------------------- register fetcher
+    if (p.l2_prefetch) {
+      // Small A (the host's choice): every CTA first asks L2 for its share of
+      // the shards' rows, so that the owners' and copiers' first reads of A
+      // hit L2, as the GEMM's do after the barrier path's gather.  Pieces of
+      // 32 KB, in bounds of each shard, 16-byte aligned (K % 8 == 0).
+      const int rows_per = (p.M + (int)gridDim.x - 1) / (int)gridDim.x;
+      int r0 = min(p.M, (int)blockIdx.x * rows_per);
+      const int r1 = min(p.M, r0 + rows_per);
+      while (r0 < r1) {
+        const int s = r0 / p.mps;
+        const int lr = r0 - s * p.mps;
+        const int n = min(r1 - r0, p.mps - lr);
+        const char* base = reinterpret_cast<const char*>(p.shards[s] + (int64_t)lr * p.K);
+        const int64_t bytes = (int64_t)n * p.K * 2;
+        for (int64_t off = (int64_t)lane * 32768; off < bytes; off += 32 * 32768)
+          prefetch_l2_bulk(base + off, (uint32_t)(bytes - off < 32768 ? bytes - off : 32768));
+        r0 += n;
+      }
+    }
     regfetch_loop(p, lane, kLayoutM);
     __syncwarp();
   } else if (kFused) {

@@ -249,6 +249,12 @@ __device__ __forceinline__ void fence_acquire_gpu() {
   asm volatile("fence.acquire.gpu;" ::: "memory");
 }
 
+// Bulk prefetch of `bytes` (a multiple of 16) starting at a 16-byte aligned
+// global address into L2; no completion is tracked.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // 16-byte global load that bypasses L1 allocation (streamed once).
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
   uint4 v;
