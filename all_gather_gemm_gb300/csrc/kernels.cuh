@@ -24,7 +24,8 @@
 //   warp 6      B loader: b's k-blocks in the A issuer's order.
 //   warp 7      register fetcher (fused only): copies chunks that TMA cannot
 //               load from a single shard (a row block straddling shards whose
-//               row count is not a multiple of 8) and publishes them.
+//               row count is not a multiple of 8) and publishes them.  When A
+//               is small it first asks L2 for the CTA's share of the shards.
 //   warps 8-11  copiers (fused only), off the MMA pipeline.  The A issuer
 //               hands a chunk's record to them through a ring in shared
 //               memory; they copy the chunk's boxes (spread over the four
