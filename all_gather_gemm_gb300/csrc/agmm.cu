@@ -39,7 +39,6 @@ constexpr int kAutoKpfOneWave = 4, kAutoKpfOneWaveMax = 8, kAutoKpfK = 8, kAutoK
 // at 16-34 MB (cube_2944, M=1024, cube_4096) it cost 0.7-2.6 us.
 constexpr int64_t kL2PrefetchMaxBytes = 12ll << 20;
 
-
 // log2 of the row count of the boxes that load a row block straddling shards:
 // the largest of 64, 32, 16, 8 rows dividing m_per_shard (3 if none does; such
 // blocks are then copied by the register fetcher instead).
@@ -341,6 +340,10 @@ int plan_launch(GemmParams& p, const Shape& s, int cap, int pair_clusters, bool 
   p.w0 = std::min(p.ng, s.num_nb);
   const int tiles = sched.num_mb * s.num_nb;  // tiles (pairs: pair tiles), one unit each
   const int grid_units = std::max(1, std::min(units, tiles));
+  p.pro_cta0 = -1;  // fetch prologue off unless chosen below
+  // A small enough to be read from L2 soon after the start: the fused kernel
+  // asks L2 for all of it first (see the register fetcher).
+  p.l2_prefetch = fused && s.M * (int64_t)s.num_kb * kBK * 2 <= kL2PrefetchMaxBytes ? 1 : 0;
   // Fetch prologue.  When a k-contiguous fused call takes two or three waves
   // and the last one is partial, the units with one tile fewer than the rest
   // have a tile's time to spare: their copier and epilogue warps stage all of
@@ -351,10 +354,6 @@ int plan_launch(GemmParams& p, const Shape& s, int cap, int pair_clusters, bool 
   // chunks, out of it.  Measured on the cube workloads that qualify (n = 2176
   // ... 3328, D = 8): the owner protocol's first wave waited about 8 us for
   // chunks copied beside the GEMM's own loads.
-  p.pro_cta0 = -1;
-  // A small enough to be read from L2 soon after the start: the fused kernel
-  // asks L2 for all of it first (see the register fetcher).
-  p.l2_prefetch = fused && s.M * (int64_t)s.num_kb * kBK * 2 <= kL2PrefetchMaxBytes ? 1 : 0;
   if (fused && !layout_m && (s.mps % 8) == 0 && tiles > grid_units &&
       tiles % grid_units != 0 && tiles <= 3 * grid_units) {
     const int fetch_ctas = (grid_units - tiles % grid_units) << p.pair;
