@@ -98,6 +98,9 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.ag_status_string.argtypes = [i32]
     lib.ag_status_string.restype = ctypes.c_char_p
     lib.ag_num_sms.argtypes = []
+    lib.ag_plan_fused.argtypes = [i32, i32, i32, i32, ctypes.POINTER(AgOptions), i32, i32,
+                                  ctypes.POINTER(AgPlan)]
+    lib.ag_plan_fused.restype = i32
     lib.ag_num_sms.restype = i32
     lib.ag_matmul_noalloc.argtypes = core + [ctypes.POINTER(AgOptions)]
     lib.ag_matmul_noalloc.restype = i32
@@ -280,6 +283,29 @@ def release_workspace() -> None:
     st = library().ag_release_workspace()
     if st != 0:
         raise AgmmError(st, "ag_release_workspace")
+
+
+class AgPlan(ctypes.Structure):
+    _fields_ = [("grid", ctypes.c_int32), ("cta_pairs", ctypes.c_int32),
+                ("tiles", ctypes.c_int32), ("k_per_flag", ctypes.c_int32),
+                ("prologue_cta0", ctypes.c_int32), ("l2_prefetch", ctypes.c_int32)]
+
+
+def plan_fused(D, m_per_shard, K, N, sms, pair_clusters, layout: str = "k_contiguous",
+               dtype: str = "bf16", rank: int = 0, k_per_flag: int = 0, num_sms: int = 0) -> dict:
+    """The launch plan of a fused call (ag_plan_fused): host arithmetic, no GPU needed."""
+    o = default_options()
+    o.layout = LAYOUTS[layout]
+    o.dtype = DTYPES[dtype]
+    o.rank = rank
+    o.k_per_flag = k_per_flag
+    o.num_sms = num_sms
+    plan = AgPlan()
+    st = library().ag_plan_fused(D, m_per_shard, K, N, ctypes.byref(o), sms, pair_clusters,
+                                 ctypes.byref(plan))
+    if st != 0:
+        raise AgmmError(st, "ag_plan_fused")
+    return {name: int(getattr(plan, name)) for name, _ in AgPlan._fields_}
 
 
 def num_sms() -> int:

@@ -125,11 +125,8 @@ bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
   return x < y + bn && y < x + an;
 }
 
-// Validation that needs no CUDA call.  Fills `sh`.
-int validate(const void** a_shards, int D, int m_per_shard, int K, const void* b, int N,
-             const void* bias, void* a_gathered, void* out, const ag_options& o, bool fused,
-             Shape* sh) {
-  if (!a_shards || !b || !a_gathered || !out) return AG_ERR_INVALID_ARG;
+// Sizes and options (no pointers, no CUDA call).  Fills `sh`.
+int shape_of(int D, int m_per_shard, int K, int N, const ag_options& o, Shape* sh) {
   if (D < 1 || m_per_shard < 1 || K < 8 || N < 8) return AG_ERR_INVALID_ARG;
   if (K % 8 || N % 8) return AG_ERR_INVALID_ARG;
   if (D > AG_MAX_SHARDS) return AG_ERR_UNSUPPORTED;
@@ -148,8 +145,31 @@ int validate(const void** a_shards, int D, int m_per_shard, int K, const void* b
       o.trace_words < 0 || o.workspace_bytes < 0)
     return AG_ERR_INVALID_ARG;
   if (o.trace && (o.trace_words < 1 || !aligned(o.trace, 8))) return AG_ERR_INVALID_ARG;
-  (void)fused;
   if (o.layout == AG_LAYOUT_M_CONTIGUOUS && (M % 8)) return AG_ERR_UNSUPPORTED;
+  sh->D = D;
+  sh->mps = m_per_shard;
+  sh->K = K;
+  sh->N = N;
+  sh->M = M;
+  sh->num_mb = (int)((M + kBM - 1) / kBM);
+  sh->num_nb = (N + kBN - 1) / kBN;
+  sh->num_kb = (K + kBK - 1) / kBK;
+  sh->kpf = o.k_per_flag ? o.k_per_flag : sizing_k_per_flag(sh->num_kb);
+  sh->G = (sh->num_kb + sh->kpf - 1) / sh->kpf;
+  if ((int64_t)sh->num_mb * sh->num_nb > INT32_MAX || (int64_t)sh->num_mb * sh->G > 0xFFFFFF)
+    return AG_ERR_UNSUPPORTED;
+  return AG_OK;
+}
+
+// Validation that needs no CUDA call.  Fills `sh`.
+int validate(const void** a_shards, int D, int m_per_shard, int K, const void* b, int N,
+             const void* bias, void* a_gathered, void* out, const ag_options& o, bool fused,
+             Shape* sh) {
+  (void)fused;
+  if (!a_shards || !b || !a_gathered || !out) return AG_ERR_INVALID_ARG;
+  int st = shape_of(D, m_per_shard, K, N, o, sh);
+  if (st != AG_OK) return st;
+  const int64_t M = sh->M;
   if (!aligned(b, 16) || !aligned(a_gathered, 16) || !aligned(out, 16)) return AG_ERR_INVALID_ARG;
   if (bias && !aligned(bias, 4)) return AG_ERR_INVALID_ARG;
   const size_t shard_bytes = (size_t)m_per_shard * K * 2;
@@ -167,18 +187,6 @@ int validate(const void** a_shards, int D, int m_per_shard, int K, const void* b
   if (bias && (overlaps(bias, bias_bytes, a_gathered, ag_bytes) ||
                overlaps(bias, bias_bytes, out, out_bytes)))
     return AG_ERR_INVALID_ARG;
-  sh->D = D;
-  sh->mps = m_per_shard;
-  sh->K = K;
-  sh->N = N;
-  sh->M = M;
-  sh->num_mb = (int)((M + kBM - 1) / kBM);
-  sh->num_nb = (N + kBN - 1) / kBN;
-  sh->num_kb = (K + kBK - 1) / kBK;
-  sh->kpf = o.k_per_flag ? o.k_per_flag : sizing_k_per_flag(sh->num_kb);
-  sh->G = (sh->num_kb + sh->kpf - 1) / sh->kpf;
-  if ((int64_t)sh->num_mb * sh->num_nb > INT32_MAX || (int64_t)sh->num_mb * sh->G > 0xFFFFFF)
-    return AG_ERR_UNSUPPORTED;
   return AG_OK;
 }
 
@@ -1088,6 +1096,32 @@ int ag_matmul_noalloc(const void** a_shards, int D, int m_per_shard, int K, cons
                       cudaStream_t stream, const ag_options* opt) {
   return run_noalloc(a_shards, D, m_per_shard, K, b, N, bias_or_null, a_gathered, out, stream,
                      opt);
+}
+
+int ag_plan_fused(int D, int m_per_shard, int K, int N, const ag_options* opt_in, int sms,
+                  int pair_clusters, ag_plan* plan) {
+  if (!plan || sms < 1 || pair_clusters < 0) return AG_ERR_INVALID_ARG;
+  ag_options o;
+  ag_options_default(&o);
+  if (opt_in) o = *opt_in;
+  if (o.dtype == AG_DTYPE_FP8_E4M3) {  // 16-bit words, as the calls count them
+    if (K < 16 || K % 16) return AG_ERR_INVALID_ARG;
+    K /= 2;
+  }
+  Shape s;
+  const int st = shape_of(D, m_per_shard, K, N, o, &s);
+  if (st != AG_OK) return st;
+  GemmParams p;
+  memset(&p, 0, sizeof p);
+  const int cap = o.num_sms ? std::min(o.num_sms, sms) : sms;
+  plan->grid = plan_launch(p, s, cap, pair_clusters, true, o.layout == AG_LAYOUT_M_CONTIGUOUS,
+                           o.k_per_flag, o.rank);
+  plan->cta_pairs = p.pair;
+  plan->tiles = p.num_tiles >> p.pair;
+  plan->k_per_flag = p.kpf;
+  plan->prologue_cta0 = p.pro_cta0;
+  plan->l2_prefetch = p.l2_prefetch;
+  return AG_OK;
 }
 
 int ag_num_sms(void) {

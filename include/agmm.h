@@ -217,6 +217,24 @@ const char* ag_status_string(int status);
  * device (0 if no device). */
 int ag_num_sms(void);
 
+/* The launch plan of a fused call (ag_matmul, ag_matmul_ex,
+ * ag_matmul_noalloc) with these sizes and options, on a device with `sms`
+ * SMs where `pair_clusters` clusters of two CTAs fit at once (0: single
+ * CTAs).  Host arithmetic only: no CUDA call and nothing launched, so it runs
+ * without a GPU too.  K counts elements (FP8: bytes), as in the calls.
+ * Returns AG_OK and fills *plan (caller-owned), or the status the calls
+ * would return for these sizes and options (pointers are not checked). */
+typedef struct ag_plan {
+  int32_t grid;           /* CTAs launched (even with CTA pairs) */
+  int32_t cta_pairs;      /* 1: 256 x 256 tiles on CTA pairs; 0: 128 x 256 on single CTAs */
+  int32_t tiles;          /* output tiles (pair tiles with CTA pairs) */
+  int32_t k_per_flag;     /* k-blocks (64 elements; FP8: 128 bytes) per ready flag */
+  int32_t prologue_cta0;  /* fetch prologue: CTAs from this index first stage all of A; -1: none */
+  int32_t l2_prefetch;    /* 1: the kernel first prefetches all of A into L2 */
+} ag_plan;
+int ag_plan_fused(int D, int m_per_shard, int K, int N, const ag_options* opt, int sms,
+                  int pair_clusters, ag_plan* plan);
+
 /* Size of the fixed device scratch that ag_matmul_noalloc uses (see below). */
 #define AG_NOALLOC_SCRATCH_BYTES (256 * 1024)
 

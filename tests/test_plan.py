@@ -1,0 +1,73 @@
+"""The launch plan of fused calls (ag_plan_fused), on the CPU: the fetch
+prologue, the L2 prefetch of small A, CTA pairs and k_per_flag are chosen as
+the library documents, for a GB300 (152 SMs, 76 co-resident CTA pairs)."""
+import pytest
+
+import all_gather_gemm_gb300 as agmm
+
+SMS, PAIRS = 152, 76
+
+
+def plan(D, m, K, N, **kw):
+    return agmm.plan_fused(D, m, K, N, SMS, PAIRS, **kw)
+
+
+def test_headline_shape_runs_neither_prologue_nor_prefetch():
+    p = plan(8, 2048, 8192, 3584, dtype="fp16")
+    assert p == {"grid": 152, "cta_pairs": 1, "tiles": 64 * 14, "k_per_flag": 8,
+                 "prologue_cta0": -1, "l2_prefetch": 0}
+
+
+@pytest.mark.parametrize("n", [2176, 2304, 2432, 2560, 2688, 2816, 3200, 3328])
+def test_cube_shapes_with_a_partial_last_wave_run_the_prologue(n):
+    # pair tiles T on 76 pairs: the last 76 - T % 76 pairs have one tile fewer
+    p = plan(8, n // 8, n, n)
+    T = -(-(-(-n // 128)) // 2) * -(-n // 256)
+    assert p["tiles"] == T and p["grid"] == 152
+    assert 76 < T <= 3 * 76 and T % 76
+    assert p["prologue_cta0"] == 2 * (T % 76)
+    assert p["l2_prefetch"] == (n * n * 2 <= 12 << 20)
+
+
+@pytest.mark.parametrize("n", [2944, 3072, 3456, 3584, 4096])
+def test_cube_shapes_without_prologue(n):
+    # 2944 / 3072: too few spare CTAs for A; 3456 ...: A too large per spare CTA
+    # or more than three waves
+    assert plan(8, n // 8, n, n)["prologue_cta0"] == -1
+
+
+@pytest.mark.parametrize("n", [256, 1024, 2048])
+def test_one_wave_cubes(n):
+    p = plan(8, n // 8, n, n)
+    T = (n // 256) * (n // 256)
+    assert p["tiles"] == T and p["grid"] == 2 * T and p["prologue_cta0"] == -1
+    assert p["l2_prefetch"] == 1
+    num_kb, num_nb = n // 64, n // 256
+    assert p["k_per_flag"] == min(num_kb, min(8, max(4, num_kb // num_nb)))
+
+
+def test_m_contiguous_and_fp8():
+    assert plan(8, 304, 2432, 2432, layout="m_contiguous")["prologue_cta0"] == -1
+    p = plan(8, 2048, 8192, 3584, dtype="fp8_e4m3")
+    assert p["tiles"] == 64 * 14 and p["k_per_flag"] == 8 and p["prologue_cta0"] == -1
+    # FP8 A of 8 MB (bytes) is prefetched
+    assert plan(8, 128, 8192, 3584, dtype="fp8_e4m3")["l2_prefetch"] == 1
+
+
+def test_restricted_grids():
+    p = plan(4, 384, 520, 1024, num_sms=40)  # 24 pair tiles on 20 pairs
+    assert p["grid"] == 40 and p["tiles"] == 24 and p["prologue_cta0"] == 8
+    p = plan(4, 160, 1024, 512, num_sms=1)
+    assert p["cta_pairs"] == 0 and p["grid"] == 1 and p["tiles"] == 10
+    assert agmm.plan_fused(4, 160, 1024, 512, SMS, 0)["cta_pairs"] == 0
+
+
+def test_rejections():
+    with pytest.raises(agmm.AgmmError):
+        plan(0, 128, 256, 256)
+    with pytest.raises(agmm.AgmmError):
+        plan(2, 128, 260, 256)  # K % 8
+    with pytest.raises(agmm.AgmmError):
+        plan(17, 128, 256, 256)  # more than AG_MAX_SHARDS
+    with pytest.raises(agmm.AgmmError):
+        agmm.plan_fused(2, 128, 256, 256, 0, 76)
