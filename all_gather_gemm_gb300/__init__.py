@@ -15,6 +15,11 @@ dtype; ``bias`` an optional fp32 [N].  ``a_gathered`` = concat(shards) and
 FP8 (``torch.float8_e4m3fn`` shards): ``b`` is given transposed, [N, K] e4m3,
 ``out`` is bf16 and ``out = scale_a * scale_b * (a_gathered @ b.T) + bias``
 (k-contiguous layout only).
+
+With the environment variable ``AGMM_VARIANT=debug`` set before the first
+call, the bounds-checked build ``libagmm_debug.so`` is loaded instead (every
+flag, per-tile word, shard-row and staging index checked on the device; a
+violation is reported by ``device_error()`` as AG_ERR_BOUNDS).
 """
 from __future__ import annotations
 
@@ -30,7 +35,8 @@ __all__ = [
 ]
 
 STATUS = {0: "AG_OK", 1: "AG_ERR_INVALID_ARG", 2: "AG_ERR_UNSUPPORTED", 3: "AG_ERR_CUDA",
-          4: "AG_ERR_TIMEOUT", 5: "AG_ERR_WORKSPACE", 6: "AG_ERR_TOO_LARGE"}
+          4: "AG_ERR_TIMEOUT", 5: "AG_ERR_WORKSPACE", 6: "AG_ERR_TOO_LARGE", 7: "AG_ERR_BUSY",
+          8: "AG_ERR_BOUNDS"}
 LAYOUTS = {"k_contiguous": 0, "m_contiguous": 1}
 DTYPES = {"bf16": 0, "fp16": 1, "fp8_e4m3": 2}
 EXPORTS = ("ag_options_default", "ag_matmul", "ag_then_matmul", "ag_matmul_ex",
@@ -61,22 +67,39 @@ class AgOptions(ctypes.Structure):
         ("workspace_bytes", ctypes.c_int64),
         ("scale_a", ctypes.c_float),
         ("scale_b", ctypes.c_float),
+        ("inject_delay_ns", ctypes.c_int64),
+        ("block_m", ctypes.c_int32),
+        ("block_n", ctypes.c_int32),
+        ("block_k", ctypes.c_int32),
+        ("stages", ctypes.c_int32),
+        ("producer_warps", ctypes.c_int32),
     ]
 
 
 _lib = None
 
 
+def variant() -> str:
+    """The library variant this process loads: "release", or "debug" (the
+    bounds-checked build) when AGMM_VARIANT=debug."""
+    v = os.environ.get("AGMM_VARIANT", "release") or "release"
+    if v not in _build.VARIANTS:
+        raise ValueError(f"AGMM_VARIANT must be one of {sorted(_build.VARIANTS)}, not {v!r}")
+    return v
+
+
 def library(build_if_missing: bool = True) -> ctypes.CDLL:
-    """Load libagmm.so (building it first if it is missing or stale)."""
+    """Load libagmm.so, or libagmm_debug.so under AGMM_VARIANT=debug (building
+    it first if it is missing or stale)."""
     global _lib
     if _lib is not None:
         return _lib
-    path = _build.LIB_PATH
-    if build_if_missing and _build.is_stale():
-        _build.build()
+    v = variant()
+    path = _build.VARIANTS[v][0]
+    if build_if_missing and _build.is_stale(path):
+        _build.build(variants=(v,))
     if not os.path.exists(path):
-        raise RuntimeError(f"libagmm.so not found at {path}; build it with "
+        raise RuntimeError(f"{os.path.basename(path)} not found at {path}; build it with "
                            "__graft_entry__.build() (nvcc, sm_103a)")
     lib = ctypes.CDLL(path)
     vp, i32 = ctypes.c_void_p, ctypes.c_int
@@ -162,8 +185,12 @@ def ag_matmul_raw(fused: bool, shard_ptrs, D, m_per_shard, K, b_ptr, N, bias_ptr
     return fn(*args, ctypes.byref(options))
 
 
+TILE_OPTIONS = ("block_m", "block_n", "block_k", "stages", "producer_warps")
+
+
 def _call(fused, shards, b, bias, a_gathered, out, stream, layout, rank, k_per_flag, num_sms,
-          timeout_ns, inject_skip_flag, trace, workspace, chunks=0, scale_a=1.0, scale_b=1.0):
+          timeout_ns, inject_skip_flag, trace, workspace, chunks=0, scale_a=1.0, scale_b=1.0,
+          inject_delay_ns=0, tile=None):
     import torch
     if not shards:
         raise ValueError("need at least one shard")
@@ -203,6 +230,11 @@ def _call(fused, shards, b, bias, a_gathered, out, stream, layout, rank, k_per_f
     o.inject_skip_flag = inject_skip_flag
     o.scale_a = scale_a
     o.scale_b = scale_b
+    o.inject_delay_ns = inject_delay_ns
+    for name, value in (tile or {}).items():
+        if name not in TILE_OPTIONS:
+            raise TypeError(f"unknown tile option {name!r}; one of {TILE_OPTIONS}")
+        setattr(o, name, value)
     if trace is not None:
         o.trace = trace.data_ptr()
         o.trace_words = trace.numel()
@@ -231,20 +263,26 @@ def _call(fused, shards, b, bias, a_gathered, out, stream, layout, rank, k_per_f
 def ag_matmul(shards, b, bias=None, *, a_gathered=None, out=None, stream=None,
               layout: str = "k_contiguous", rank: int = 0, k_per_flag: int = 0,
               num_sms: int = 0, timeout_ns: int = 0, inject_skip_flag: int = -1, trace=None,
-              workspace=None, scale_a: float = 1.0, scale_b: float = 1.0):
+              workspace=None, scale_a: float = 1.0, scale_b: float = 1.0,
+              inject_delay_ns: int = 0, **tile):
     """Fused all-gather matmul (one persistent kernel).  Returns (a_gathered, out).
-    ``scale_a``/``scale_b``: FP8 per-tensor scales (ignored for 16-bit inputs)."""
+    ``scale_a``/``scale_b``: FP8 per-tensor scales (ignored for 16-bit inputs).
+    ``inject_delay_ns``: stress testing, publishers of ready flags wait up to
+    this long before publishing.  ``tile``: block_m, block_n, block_k, stages,
+    producer_warps (ag_options; 0 = automatic)."""
     return _call(True, shards, b, bias, a_gathered, out, stream, layout, rank, k_per_flag,
                  num_sms, timeout_ns, inject_skip_flag, trace, workspace,
-                 scale_a=scale_a, scale_b=scale_b)
+                 scale_a=scale_a, scale_b=scale_b, inject_delay_ns=inject_delay_ns, tile=tile)
 
 
 def ag_then_matmul(shards, b, bias=None, *, a_gathered=None, out=None, stream=None,
                    layout: str = "k_contiguous", k_per_flag: int = 0, num_sms: int = 0,
-                   timeout_ns: int = 0, trace=None, scale_a: float = 1.0, scale_b: float = 1.0):
+                   timeout_ns: int = 0, trace=None, scale_a: float = 1.0, scale_b: float = 1.0,
+                   **tile):
     """Barrier baseline: gather kernel, then GEMM kernel.  Returns (a_gathered, out)."""
     return _call(False, shards, b, bias, a_gathered, out, stream, layout, 0, k_per_flag,
-                 num_sms, timeout_ns, -1, trace, None, scale_a=scale_a, scale_b=scale_b)
+                 num_sms, timeout_ns, -1, trace, None, scale_a=scale_a, scale_b=scale_b,
+                 tile=tile)
 
 
 def ag_chunked_matmul(shards, b, bias=None, *, chunks: int = 4, a_gathered=None, out=None,
@@ -288,11 +326,13 @@ def release_workspace() -> None:
 class AgPlan(ctypes.Structure):
     _fields_ = [("grid", ctypes.c_int32), ("cta_pairs", ctypes.c_int32),
                 ("tiles", ctypes.c_int32), ("k_per_flag", ctypes.c_int32),
-                ("prologue_cta0", ctypes.c_int32), ("l2_prefetch", ctypes.c_int32)]
+                ("prologue_cta0", ctypes.c_int32), ("l2_prefetch", ctypes.c_int32),
+                ("block_m", ctypes.c_int32), ("stages", ctypes.c_int32)]
 
 
 def plan_fused(D, m_per_shard, K, N, sms, pair_clusters, layout: str = "k_contiguous",
-               dtype: str = "bf16", rank: int = 0, k_per_flag: int = 0, num_sms: int = 0) -> dict:
+               dtype: str = "bf16", rank: int = 0, k_per_flag: int = 0, num_sms: int = 0,
+               **tile) -> dict:
     """The launch plan of a fused call (ag_plan_fused): host arithmetic, no GPU needed."""
     o = default_options()
     o.layout = LAYOUTS[layout]
@@ -300,6 +340,10 @@ def plan_fused(D, m_per_shard, K, N, sms, pair_clusters, layout: str = "k_contig
     o.rank = rank
     o.k_per_flag = k_per_flag
     o.num_sms = num_sms
+    for name, value in tile.items():
+        if name not in TILE_OPTIONS:
+            raise TypeError(f"unknown tile option {name!r}; one of {TILE_OPTIONS}")
+        setattr(o, name, value)
     plan = AgPlan()
     st = library().ag_plan_fused(D, m_per_shard, K, N, ctypes.byref(o), sms, pair_clusters,
                                  ctypes.byref(plan))

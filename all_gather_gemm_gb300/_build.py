@@ -1,7 +1,11 @@
 """Build libagmm.so (the C-ABI library) in-tree with nvcc for sm_103a.
 
 Cross-compiles without a GPU.  One translation unit, one -gencode, static
-cudart; the result lands next to this file and is git-ignored.
+cudart; the result lands next to this file and is git-ignored.  The
+bounds-checked variant libagmm_debug.so (-DAGMM_DEBUG: every flag, per-tile
+word, shard-row and staging index is checked against its buffer; a violation
+is recorded as AG_ERR_BOUNDS and the access skipped) is compiled alongside it,
+in parallel, from the same sources.
 """
 from __future__ import annotations
 
@@ -14,6 +18,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(PKG, "libagmm.so")
+DEBUG_LIB_PATH = os.path.join(PKG, "libagmm_debug.so")
+VARIANTS = {"release": (LIB_PATH, ()), "debug": (DEBUG_LIB_PATH, ("-DAGMM_DEBUG",))}
 SOURCES = [os.path.join(CSRC, f) for f in ("agmm.cu", "kernels.cuh", "ptx.cuh")] + [
     os.path.join(INCLUDE, "agmm.h")]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -31,26 +37,39 @@ def nvcc_command(out: str, extra=()) -> list:
             "-shared", "-I", INCLUDE, *extra, "-o", out, os.path.join(CSRC, "agmm.cu")]
 
 
-def is_stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+def is_stale(path: str = LIB_PATH) -> bool:
+    if not os.path.exists(path):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     return any(os.path.getmtime(s) > t for s in SOURCES)
 
 
-def build(force: bool = False, verbose: bool = False, extra=()) -> str:
-    """Compile if missing or older than its sources.  Returns the library path."""
-    if not force and not extra and not is_stale():
-        return LIB_PATH
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = nvcc_command(tmp, extra)
-    res = subprocess.run(cmd, capture_output=True, text=True)
-    if verbose or res.returncode != 0:
-        print(" ".join(cmd))
-        print(res.stdout, res.stderr)
-    if res.returncode != 0:
-        raise RuntimeError(f"nvcc failed with exit code {res.returncode}")
-    os.replace(tmp, LIB_PATH)
+def build(force: bool = False, verbose: bool = False, extra=(),
+          variants=("release", "debug")) -> str:
+    """Compile the variants that are missing or older than their sources (all
+    of them with `force` or `extra` flags), in parallel.  Returns the release
+    library's path."""
+    jobs = []
+    for v in variants:
+        path, flags = VARIANTS[v]
+        if not force and not extra and not is_stale(path):
+            continue
+        tmp = path + f".tmp{os.getpid()}"
+        cmd = nvcc_command(tmp, (*flags, *extra))
+        proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True)
+        jobs.append((v, path, tmp, cmd, proc))
+    failed = []
+    for v, path, tmp, cmd, proc in jobs:
+        out, err = proc.communicate()
+        if verbose or proc.returncode != 0:
+            print(" ".join(cmd))
+            print(out, err)
+        if proc.returncode != 0:
+            failed.append((v, proc.returncode))
+            continue
+        os.replace(tmp, path)
+    if failed:
+        raise RuntimeError(f"nvcc failed: {failed}")
     return LIB_PATH
 
 

@@ -104,6 +104,11 @@ struct DevState {
   uint16_t* staging = nullptr;
   size_t staging_cap = 0;  // elements
   uint64_t reported_epoch = 0;
+  // Overlap detection on the library workspace: the stream of the last call
+  // that used it and an event recorded on that stream after the call.
+  cudaEvent_t ws_done = nullptr;
+  cudaStream_t ws_stream = nullptr;
+  bool ws_used = false;
 };
 
 std::mutex g_mu;
@@ -123,6 +128,26 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
   uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
   return x < y + bn && y < x + an;
+}
+
+// Tile options: only the compiled shapes.  128-row tiles run on single CTAs
+// with 4 stages, 256-row tiles on CTA pairs with 6 (Pipe<>), both 256 columns
+// wide, 64 16-bit elements (128 FP8 bytes) per stage, 4 copier warps.
+constexpr int kStagesSingle = 4, kStagesPair = 6;
+static_assert(Pipe<false>::kStages == kStagesSingle && Pipe<true>::kStages == kStagesPair,
+              "tile options and compiled pipelines differ");
+int check_tile_options(const ag_options& o) {
+  if (o.block_m < 0 || o.block_n < 0 || o.block_k < 0 || o.stages < 0 || o.producer_warps < 0)
+    return AG_ERR_INVALID_ARG;
+  const int bk = o.dtype == AG_DTYPE_FP8_E4M3 ? 2 * kBK : kBK;
+  if ((o.block_m && o.block_m != kBM && o.block_m != 2 * kBM) || (o.block_n && o.block_n != kBN) ||
+      (o.block_k && o.block_k != bk) || (o.producer_warps && o.producer_warps != kCopyWarps))
+    return AG_ERR_UNSUPPORTED;
+  if (o.stages && o.stages != kStagesSingle && o.stages != kStagesPair) return AG_ERR_UNSUPPORTED;
+  if (o.stages && o.block_m &&
+      (o.stages == kStagesPair) != (o.block_m == 2 * kBM))
+    return AG_ERR_UNSUPPORTED;
+  return AG_OK;
 }
 
 // Sizes and options (no pointers, no CUDA call).  Fills `sh`.
@@ -145,6 +170,10 @@ int shape_of(int D, int m_per_shard, int K, int N, const ag_options& o, Shape* s
       o.trace_words < 0 || o.workspace_bytes < 0)
     return AG_ERR_INVALID_ARG;
   if (o.trace && (o.trace_words < 1 || !aligned(o.trace, 8))) return AG_ERR_INVALID_ARG;
+  if (o.inject_delay_ns < 0 ||
+      o.inject_delay_ns > (o.timeout_ns ? o.timeout_ns : kDefaultTimeoutNs) / 16)
+    return AG_ERR_INVALID_ARG;
+  if (int st = check_tile_options(o)) return st;
   if (o.layout == AG_LAYOUT_M_CONTIGUOUS && (M % 8)) return AG_ERR_UNSUPPORTED;
   sh->D = D;
   sh->mps = m_per_shard;
@@ -292,10 +321,45 @@ int device_init(DevState& ds, int dev) {
   AG_CK(cudaFuncSetAttribute(agmm_gemm_kernel<kFusedK, true, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem2));
   if (int st = query_pair_clusters(sms, &ds.pair_clusters)) return st;
+  AG_CK(cudaEventCreateWithFlags(&ds.ws_done, cudaEventDisableTiming));
   AG_CK(cudaMalloc(&ds.err, 2 * sizeof(unsigned long long)));
   AG_CK(cudaMemset(ds.err, 0, 2 * sizeof(unsigned long long)));
   ds.init = true;
   ds.supported = true;
+  return AG_OK;
+}
+
+// A call about to use the library workspace on `stream`: AG_ERR_BUSY while
+// the last call that used it was made on another stream and has not finished
+// (its event has not completed).  Same-stream calls are ordered by the stream.
+// While `stream` is being captured nothing runs, so nothing is checked or
+// recorded.
+bool capturing(cudaStream_t stream) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return cs != cudaStreamCaptureStatusNone;
+}
+
+int check_busy(DevState& ds, cudaStream_t stream) {
+  if (!ds.ws_used || ds.ws_stream == stream || capturing(stream)) return AG_OK;
+  const cudaError_t q = cudaEventQuery(ds.ws_done);
+  if (q == cudaErrorNotReady) {
+    cudaGetLastError();
+    return AG_ERR_BUSY;
+  }
+  if (q != cudaSuccess) return cuda_fail(q, "cudaEventQuery (workspace in use?)");
+  return AG_OK;
+}
+
+// After a successful launch that used the library workspace.
+int mark_busy(DevState& ds, cudaStream_t stream) {
+  if (capturing(stream)) return AG_OK;
+  AG_CK(cudaEventRecord(ds.ws_done, stream));
+  ds.ws_stream = stream;
+  ds.ws_used = true;
   return AG_OK;
 }
 
@@ -326,12 +390,20 @@ int grow_workspace(DevState& ds, const Shape& s, bool need_flags, bool need_stag
 }
 
 // The launch plan shared by every entry point: CTA pairs (256 x 256 tiles)
-// whenever two SMs are allowed; the schedule; the automatic k_per_flag (the
-// workspace is sized for s.G, which is >= the automatic choice's G).  Fills
-// the schedule fields of p and returns the grid (CTAs; even for pairs).
+// whenever two SMs are allowed, unless the tile options ask for 128-row
+// tiles; the schedule; the automatic k_per_flag (the workspace is sized for
+// s.G, which is >= the automatic choice's G).  Fills the schedule fields of p
+// and *grid (CTAs; even for pairs).  The options were checked by
+// check_tile_options; 256-row tiles on a grid without a CTA pair are
+// AG_ERR_UNSUPPORTED.
 int plan_launch(GemmParams& p, const Shape& s, int cap, int pair_clusters, bool fused,
-                bool layout_m, int k_per_flag, int rank) {
-  const bool pair = cap >= 2 && pair_clusters >= 1;
+                bool layout_m, const ag_options& o, int* grid) {
+  const int k_per_flag = o.k_per_flag, rank = o.rank;
+  const bool want_single = o.block_m == kBM || o.stages == kStagesSingle;
+  const bool want_pair = o.block_m == 2 * kBM || o.stages == kStagesPair;
+  const bool can_pair = cap >= 2 && pair_clusters >= 1;
+  if (want_pair && !can_pair) return AG_ERR_UNSUPPORTED;
+  const bool pair = can_pair && !want_single;
   Shape sched = s;
   sched.num_mb = pair ? (s.num_mb + 1) / 2 : s.num_mb;
   const int units = pair ? std::min(cap / 2, pair_clusters) : cap;  // CTAs, or CTA pairs
@@ -371,7 +443,10 @@ int plan_launch(GemmParams& p, const Shape& s, int cap, int pair_clusters, bool 
       p.w0 = 0;
     }
   }
-  return grid_units << p.pair;
+  p.flag_words = (int64_t)s.num_mb * p.G;
+  p.started_words = p.num_tiles;
+  *grid = grid_units << p.pair;
+  return AG_OK;
 }
 
 // A 3-D view of D equal row segments, `rows` x `inner` each, `seg_stride`
@@ -516,10 +591,29 @@ int run(bool fused, const void** a_shards, int D, int m_per_shard, int K, const 
   if (bias && (st = check_device_ptr(bias, dev)) != AG_OK) return st;
   if (o.trace && (st = check_device_ptr(o.trace, dev)) != AG_OK) return st;
 
-  // Workspace: flags (fused) and the [K, M] staging (m-contiguous layout).
   const bool layout_m = o.layout == AG_LAYOUT_M_CONTIGUOUS;
+  const int cap = o.num_sms ? std::min(o.num_sms, ds.sms) : ds.sms;
+  // The launch plan first: it can still refuse the tile options, and nothing
+  // may be enqueued before every check has passed.
+  GemmParams p;
+  memset(&p, 0, sizeof p);
+  p.M = (int)s.M;
+  p.N = N;
+  p.K = K;
+  p.D = D;
+  p.mps = m_per_shard;
+  p.rank = fused ? o.rank : 0;
+  p.num_mb = s.num_mb;
+  p.num_nb = s.num_nb;
+  p.num_kb = s.num_kb;
+  int grid = 0;
+  if ((st = plan_launch(p, s, cap, ds.pair_clusters, fused, layout_m, o, &grid)) != AG_OK)
+    return st;
+
+  // Workspace: flags (fused) and the [K, M] staging (m-contiguous layout).
   uint64_t* flags = nullptr;
   uint16_t* staging = nullptr;
+  bool library_ws = false;
   if (fused && o.workspace) {
     const size_t need = flags_bytes(s) + (layout_m ? (size_t)s.K * s.M * 2 : 0);
     if ((size_t)o.workspace_bytes < need) return AG_ERR_WORKSPACE;
@@ -530,14 +624,63 @@ int run(bool fused, const void** a_shards, int D, int m_per_shard, int K, const 
                                                      flags_bytes(s))
                        : nullptr;
   } else if (fused || layout_m) {
+    library_ws = true;
+    if ((st = check_busy(ds, stream)) != AG_OK) return st;
     if ((st = grow_workspace(ds, s, fused, layout_m, stream)) != AG_OK) return st;
     flags = fused ? ds.flags : nullptr;
     staging = layout_m ? ds.staging : nullptr;
   }
 
+  if ((st = make_map(&p.tm_a, a_gathered, (uint64_t)K, (uint64_t)s.M, kBK, kBM)) != AG_OK) return st;
+  const bool pair = p.pair != 0;
+  if (fp8) {
+    // b is [N, K] (K-major): boxes of this CTA's b columns (pair: 128 of the
+    // tile's 256) x 128 bytes of K.
+    if ((st = make_map(&p.tm_b, b, (uint64_t)K, (uint64_t)N, kBK, pair ? kBN / 2 : kBN)) != AG_OK)
+      return st;
+  } else if ((st = make_map(&p.tm_b, b, (uint64_t)N, (uint64_t)K, 64, kBK)) != AG_OK) {
+    return st;
+  }
+  if ((st = make_map(&p.tm_out, out, (uint64_t)N, (uint64_t)s.M, kEpiCols, kEpiRows)) != AG_OK)
+    return st;
+  if (layout_m &&
+      (st = make_map(&p.tm_a_mk, staging, (uint64_t)s.M, (uint64_t)K, 64, kBK)) != AG_OK)
+    return st;
+  if (fused) {
+    // Row blocks that straddle shards are loaded in boxes of 2^sh_log2 rows
+    // (the largest of 64, 32, 16, 8 that divides m_per_shard) when the shard
+    // boundaries fall on multiples of 8 rows.
+    const bool straddle8 = D > 1 && (m_per_shard % kBM) != 0 && (m_per_shard % 8) == 0;
+    p.sh_log2 = straddle_log2(m_per_shard);
+    for (int r = 0; r < D; ++r) {
+      if ((st = make_map(&p.tm_shard[r], a_shards[r], (uint64_t)K, (uint64_t)m_per_shard, kBK,
+                         kBM)) != AG_OK)
+        return st;
+      if (straddle8 && (st = make_map(&p.tm_shard8[r], a_shards[r], (uint64_t)K,
+                                      (uint64_t)m_per_shard, kBK, 1u << p.sh_log2)) != AG_OK)
+        return st;
+    }
+  }
+
   const uint64_t epoch = g_epoch.fetch_add(1) + 1;
   const int64_t timeout = o.timeout_ns ? o.timeout_ns : kDefaultTimeoutNs;
-  const int cap = o.num_sms ? std::min(o.num_sms, ds.sms) : ds.sms;
+  for (int r = 0; r < D; ++r) p.shards[r] = static_cast<const uint16_t*>(a_shards[r]);
+  p.a_gathered = static_cast<uint16_t*>(a_gathered);
+  p.staging_mk = staging;
+  p.bias = static_cast<const float*>(bias);
+  p.flags = flags;
+  p.started = flags ? flags + flags_region(s) / 8 : nullptr;
+  p.err = ds.err;
+  p.trace = o.trace;
+  p.trace_words = o.trace_words;
+  p.epoch = epoch;
+  p.fbase = epoch << kFlagShift;
+  p.timeout_ns = timeout;
+  p.pipe_timeout_ns = 4 * timeout + 2000000000LL;
+  p.inject_delay_ns = fused ? o.inject_delay_ns : 0;
+  p.fp16 = o.dtype == AG_DTYPE_FP16 ? 1 : 0;  // FP8 writes bf16
+  p.inject_skip_flag = fused ? o.inject_skip_flag : -1;
+  if (fp8) p.scale_ab = o.scale_a * o.scale_b;
 
   if (!fused) {
     GatherParams gp;
@@ -569,80 +712,26 @@ int run(bool fused, const void** a_shards, int D, int m_per_shard, int K, const 
     if (e != cudaSuccess) return cuda_fail(e, "gather kernel launch");
   }
 
-  GemmParams p;
-  memset(&p, 0, sizeof p);
-  if ((st = make_map(&p.tm_a, a_gathered, (uint64_t)K, (uint64_t)s.M, kBK, kBM)) != AG_OK) return st;
-  if (!fp8 && (st = make_map(&p.tm_b, b, (uint64_t)N, (uint64_t)K, 64, kBK)) != AG_OK) return st;
-  if ((st = make_map(&p.tm_out, out, (uint64_t)N, (uint64_t)s.M, kEpiCols, kEpiRows)) != AG_OK)
-    return st;
-  if (layout_m &&
-      (st = make_map(&p.tm_a_mk, staging, (uint64_t)s.M, (uint64_t)K, 64, kBK)) != AG_OK)
-    return st;
-  if (fused) {
-    // Row blocks that straddle shards are loaded in boxes of 2^sh_log2 rows
-    // (the largest of 64, 32, 16, 8 that divides m_per_shard) when the shard
-    // boundaries fall on multiples of 8 rows.
-    const bool straddle8 = D > 1 && (m_per_shard % kBM) != 0 && (m_per_shard % 8) == 0;
-    p.sh_log2 = straddle_log2(m_per_shard);
-    for (int r = 0; r < D; ++r) {
-      if ((st = make_map(&p.tm_shard[r], a_shards[r], (uint64_t)K, (uint64_t)m_per_shard, kBK,
-                         kBM)) != AG_OK)
-        return st;
-      if (straddle8 && (st = make_map(&p.tm_shard8[r], a_shards[r], (uint64_t)K,
-                                      (uint64_t)m_per_shard, kBK, 1u << p.sh_log2)) != AG_OK)
-        return st;
-    }
-  }
-  for (int r = 0; r < D; ++r) p.shards[r] = static_cast<const uint16_t*>(a_shards[r]);
-  p.a_gathered = static_cast<uint16_t*>(a_gathered);
-  p.staging_mk = staging;
-  p.bias = static_cast<const float*>(bias);
-  p.flags = flags;
-  p.started = flags ? flags + flags_region(s) / 8 : nullptr;
-  p.err = ds.err;
-  p.trace = o.trace;
-  p.trace_words = o.trace_words;
-  p.epoch = epoch;
-  p.fbase = epoch << kFlagShift;
-  p.timeout_ns = timeout;
-  p.pipe_timeout_ns = 4 * timeout + 2000000000LL;
-  p.M = (int)s.M;
-  p.N = N;
-  p.K = K;
-  p.D = D;
-  p.mps = m_per_shard;
-  p.rank = fused ? o.rank : 0;
-  p.num_mb = s.num_mb;
-  p.num_nb = s.num_nb;
-  p.num_kb = s.num_kb;
-  const int grid = plan_launch(p, s, cap, ds.pair_clusters, fused, layout_m, o.k_per_flag,
-                               fused ? o.rank : 0);
-  p.fp16 = o.dtype == AG_DTYPE_FP16 ? 1 : 0;  // FP8 writes bf16
-  p.inject_skip_flag = fused ? o.inject_skip_flag : -1;
-  const bool pair = p.pair != 0;
-  if (fp8) {
-    // b is [N, K] (K-major): boxes of this CTA's b columns (pair: 128 of the
-    // tile's 256) x 128 bytes of K.
-    if ((st = make_map(&p.tm_b, b, (uint64_t)K, (uint64_t)N, kBK, pair ? kBN / 2 : kBN)) != AG_OK)
-      return st;
-    p.scale_ab = o.scale_a * o.scale_b;
-    if (fused)
-      return pair ? launch<kFusedK, true, true>(grid, stream, p, "fused kernel (fp8)")
-                  : launch<kFusedK, false, true>(grid, stream, p, "fused kernel (fp8)");
-    return pair ? launch<kGemmK, true, true>(grid, stream, p, "gemm kernel (fp8)")
-                : launch<kGemmK, false, true>(grid, stream, p, "gemm kernel (fp8)");
-  }
-  if (fused && layout_m)
-    return pair ? launch<kFusedM, true>(grid, stream, p, "fused kernel")
-                : launch<kFusedM, false>(grid, stream, p, "fused kernel");
-  if (fused)
-    return pair ? launch<kFusedK, true>(grid, stream, p, "fused kernel")
-                : launch<kFusedK, false>(grid, stream, p, "fused kernel");
-  if (layout_m)
-    return pair ? launch<kGemmM, true>(grid, stream, p, "gemm kernel")
-                : launch<kGemmM, false>(grid, stream, p, "gemm kernel");
-  return pair ? launch<kGemmK, true>(grid, stream, p, "gemm kernel")
+  if (fp8 && fused)
+    st = pair ? launch<kFusedK, true, true>(grid, stream, p, "fused kernel (fp8)")
+              : launch<kFusedK, false, true>(grid, stream, p, "fused kernel (fp8)");
+  else if (fp8)
+    st = pair ? launch<kGemmK, true, true>(grid, stream, p, "gemm kernel (fp8)")
+              : launch<kGemmK, false, true>(grid, stream, p, "gemm kernel (fp8)");
+  else if (fused && layout_m)
+    st = pair ? launch<kFusedM, true>(grid, stream, p, "fused kernel")
+              : launch<kFusedM, false>(grid, stream, p, "fused kernel");
+  else if (fused)
+    st = pair ? launch<kFusedK, true>(grid, stream, p, "fused kernel")
+              : launch<kFusedK, false>(grid, stream, p, "fused kernel");
+  else if (layout_m)
+    st = pair ? launch<kGemmM, true>(grid, stream, p, "gemm kernel")
+              : launch<kGemmM, false>(grid, stream, p, "gemm kernel");
+  else
+    st = pair ? launch<kGemmK, true>(grid, stream, p, "gemm kernel")
               : launch<kGemmK, false>(grid, stream, p, "gemm kernel");
+  if (st == AG_OK && library_ws) st = mark_busy(ds, stream);
+  return st;
 }
 
 }  // namespace
@@ -705,7 +794,8 @@ int gemm_segments(DevState& ds, const Shape& s, int lo, int hi, const void* a_ga
   p.seg_rows = seg_rows;
   p.fp16 = o.dtype == AG_DTYPE_FP16 ? 1 : 0;
   p.inject_skip_flag = -1;
-  const int grid = plan_launch(p, sc, cap, ds.pair_clusters, false, false, o.k_per_flag, 0);
+  int grid = 0;
+  if ((st = plan_launch(p, sc, cap, ds.pair_clusters, false, false, o, &grid)) != AG_OK) return st;
   if (fp8) {
     if ((st = make_map(&p.tm_b, b, (uint64_t)s.K, (uint64_t)s.N, kBK, p.pair ? kBN / 2 : kBN)) !=
         AG_OK)
@@ -863,21 +953,6 @@ int noalloc_setup(NoAllocState& ns, int dev) {
   return AG_OK;
 }
 
-// Newest unreported error recorded by ag_matmul_noalloc on `dev` (code 0 if
-// none).  The caller holds g_mu and has synchronised the stream.
-int noalloc_take_error(int dev, int* code, int* info) {
-  NoAllocState& ns = g_noalloc[dev];
-  if (!ns.scratch) return AG_OK;
-  unsigned long long host[2];
-  AG_CK(cudaMemcpy(host, ns.scratch, sizeof host, cudaMemcpyDeviceToHost));
-  if (host[0] > ns.reported_epoch) {
-    ns.reported_epoch = host[0];
-    if (code) *code = (int)(host[1] >> 32);
-    if (info) *info = (int)(host[1] & 0xFFFFFFFFull);
-  }
-  return AG_OK;
-}
-
 int run_noalloc(const void** a_shards, int D, int m_per_shard, int K, const void* b, int N,
                 const void* bias, void* a_gathered, void* out, cudaStream_t stream,
                 const ag_options* opt_in) {
@@ -952,7 +1027,9 @@ int run_noalloc(const void** a_shards, int D, int m_per_shard, int K, const void
   p.num_nb = s.num_nb;
   p.num_kb = s.num_kb;
   const int cap = o.num_sms ? std::min(o.num_sms, ns.sms) : ns.sms;
-  const int grid = plan_launch(p, s, cap, ns.pair_clusters, true, false, o.k_per_flag, o.rank);
+  int grid = 0;
+  if ((st = plan_launch(p, s, cap, ns.pair_clusters, true, false, o, &grid)) != AG_OK) return st;
+  p.inject_delay_ns = o.inject_delay_ns;
   p.fp16 = o.dtype == AG_DTYPE_FP16 ? 1 : 0;
   p.inject_skip_flag = o.inject_skip_flag;
   if (fp8) {
@@ -1049,17 +1126,28 @@ int ag_get_device_error(cudaStream_t stream, int* code, int* info) {
   AG_CK(cudaStreamSynchronize(stream));
   std::lock_guard<std::mutex> lock(g_mu);
   if (dev < 0 || dev >= kMaxDevices) return AG_OK;
-  if (!g_dev[dev].err) return noalloc_take_error(dev, code, info);
+  // Both error words carry epochs of the one process-wide counter, so the
+  // later call's error is the one with the larger epoch; the other word keeps
+  // its error for the next report.
+  unsigned long long lib[2] = {0, 0}, na[2] = {0, 0};
   DevState& ds = g_dev[dev];
-  unsigned long long host[2];
-  AG_CK(cudaMemcpy(host, ds.err, sizeof host, cudaMemcpyDeviceToHost));
-  if (host[0] > ds.reported_epoch) {
-    ds.reported_epoch = host[0];
-    if (code) *code = (int)(host[1] >> 32);
-    if (info) *info = (int)(host[1] & 0xFFFFFFFFull);
-    return AG_OK;
+  NoAllocState& ns = g_noalloc[dev];
+  if (ds.err) AG_CK(cudaMemcpy(lib, ds.err, sizeof lib, cudaMemcpyDeviceToHost));
+  if (ns.scratch) AG_CK(cudaMemcpy(na, ns.scratch, sizeof na, cudaMemcpyDeviceToHost));
+  const bool lib_new = lib[0] > ds.reported_epoch, na_new = na[0] > ns.reported_epoch;
+  const unsigned long long* w = nullptr;
+  if (lib_new && (!na_new || lib[0] > na[0])) {
+    ds.reported_epoch = lib[0];
+    w = lib;
+  } else if (na_new) {
+    ns.reported_epoch = na[0];
+    w = na;
   }
-  return noalloc_take_error(dev, code, info);
+  if (w) {
+    if (code) *code = (int)(w[1] >> 32);
+    if (info) *info = (int)(w[1] & 0xFFFFFFFFull);
+  }
+  return AG_OK;
 }
 
 int ag_release_workspace(void) {
@@ -1114,8 +1202,13 @@ int ag_plan_fused(int D, int m_per_shard, int K, int N, const ag_options* opt_in
   GemmParams p;
   memset(&p, 0, sizeof p);
   const int cap = o.num_sms ? std::min(o.num_sms, sms) : sms;
-  plan->grid = plan_launch(p, s, cap, pair_clusters, true, o.layout == AG_LAYOUT_M_CONTIGUOUS,
-                           o.k_per_flag, o.rank);
+  int grid = 0;
+  const int pst =
+      plan_launch(p, s, cap, pair_clusters, true, o.layout == AG_LAYOUT_M_CONTIGUOUS, o, &grid);
+  if (pst != AG_OK) return pst;
+  plan->grid = grid;
+  plan->block_m = p.pair ? 2 * kBM : kBM;
+  plan->stages = p.pair ? kStagesPair : kStagesSingle;
   plan->cta_pairs = p.pair;
   plan->tiles = p.num_tiles >> p.pair;
   plan->k_per_flag = p.kpf;

@@ -127,8 +127,12 @@ struct Pipe {
   static_assert(kSmemBytes <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
 };
 
-// Error code written to the device error word (matches ag_status).
+// Error codes written to the device error word (match ag_status).
 constexpr uint32_t kErrTimeout = 4;
+constexpr uint32_t kErrBounds = 8;  // AGMM_DEBUG builds: info = site << 24 | index
+// Sites of a bounds violation (AGMM_DEBUG builds).
+constexpr uint32_t kDbgFlag = 1, kDbgStarted = 2, kDbgShardRow = 3, kDbgGathered = 4,
+                   kDbgStaging = 5, kDbgTile = 6;
 // Sites reported with a pipeline timeout (ready-flag timeouts report the flag index).
 constexpr uint32_t kSiteEmpty = 0xF00001, kSiteFull = 0xF00002, kSiteTmemEmpty = 0xF00003,
                    kSiteTmemFull = 0xF00004, kSiteRing = 0xF00005, kSiteCopy = 0xF00006,
@@ -174,6 +178,9 @@ struct GemmParams {
   int inject_skip_flag;     // this flag index is never published (fault injection)
   int pro_cta0;             // fetch prologue: CTAs from this index stage every chunk first (-1: off)
   int l2_prefetch;          // 1: each CTA prefetches its share of the shards into L2 at the start
+  int64_t inject_delay_ns;  // stress testing: publishers wait up to this long before a release
+  int64_t flag_words;       // bounds of flags / started (checked in AGMM_DEBUG builds only)
+  int64_t started_words;
 };
 
 struct GatherParams {
@@ -197,6 +204,43 @@ __device__ __forceinline__ void record_error(const unsigned long long* err_c, ui
   if (prev < epoch) {
     atomicExch(err + 1, ((unsigned long long)code << 32) | info);
     __threadfence();
+  }
+}
+
+// Bounds check of the bounds-checked build (-DAGMM_DEBUG, libagmm_debug.so):
+// false when `ok` does not hold, after recording AG_ERR_BOUNDS with the site
+// and the low 24 bits of the index; the caller then skips the access.  The
+// release build compiles it to `true`.
+__device__ __forceinline__ bool dbg_ok(const GemmParams& p, bool ok, uint32_t site, int64_t idx) {
+#ifdef AGMM_DEBUG
+  if (!ok) {
+    record_error(p.err, p.epoch, kErrBounds, (site << 24) | ((uint32_t)idx & 0xFFFFFFu));
+    return false;
+  }
+#else
+  (void)p, (void)ok, (void)site, (void)idx;
+#endif
+  return true;
+}
+
+__device__ __forceinline__ bool flag_ok(const GemmParams& p, int64_t idx) {
+  return dbg_ok(p, idx >= 0 && idx < p.flag_words, kDbgFlag, idx);
+}
+
+// Stress testing (ag_options.inject_delay_ns): a publisher waits a
+// pseudo-random 0 .. inject_delay_ns (a hash of the flag index and the call's
+// epoch) between its copies and the release store that publishes them, so
+// that readers meet publishers late and in shuffled order.  The wait is
+// bounded by time and by an iteration count.
+__device__ __forceinline__ void inject_delay(const GemmParams& p, int flag_idx) {
+  if (p.inject_delay_ns <= 0) return;
+  uint32_t h = (uint32_t)flag_idx * 0x9E3779B1u ^ (uint32_t)p.epoch * 0x85EBCA77u;
+  h ^= h >> 15;
+  h *= 0xC2B2AE3Du;
+  h ^= h >> 13;
+  const uint64_t d = (uint64_t)p.inject_delay_ns * (h & 1023u) / 1023u;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0; it < (1u << 26) && globaltimer_ns() - t0 < d; ++it) {
   }
 }
 
@@ -320,6 +364,9 @@ struct TileCtx {
 template <bool kFused>
 __device__ __forceinline__ void tile_ctx(const GemmParams& p, int t, TileCtx& c) {
   tile_coords(p, t, c.mb, c.nb);
+  if (!dbg_ok(p, c.mb >= 0 && c.mb < p.num_mb + p.pair && c.nb >= 0 && c.nb < p.num_nb, kDbgTile,
+              t))
+    c.mb = p.num_mb + p.pair;  // (bounds-checked build) treated as rows past M
   // Fused: the owned window first (chunk_at).  The barrier GEMM has nothing
   // to own and runs k in ascending order, which keeps the tiles of a row
   // block reading the same A k-block at about the same time.
@@ -416,6 +463,9 @@ __device__ __forceinline__ bool wait_handoff(const GemmParams& p, uint64_t* bar,
 // and returns false; the caller then proceeds, so the pipeline always drains.
 __device__ __forceinline__ bool wait_or_take(const GemmParams& p, int flag_idx, uint64_t target,
                                              int owner_tile) {
+  if (!flag_ok(p, flag_idx)) return false;
+  if (owner_tile >= 0 && !dbg_ok(p, owner_tile < p.started_words, kDbgStarted, owner_tile))
+    owner_tile = -1;
   uint64_t* f = p.flags + flag_idx;
   const uint64_t t0 = globaltimer_ns();
   // Once the owner tile is seen started it stays started for this call, so
@@ -482,7 +532,7 @@ __device__ __forceinline__ void prologue_copy_box(const GemmParams& p, int mb, i
   for (int h = 0; h < 4; ++h) {
     m[h] = mb * kBM + (4 * h + (lane >> 3)) * 8;
     const int nrow = min(8, p.M - m[h]);
-    if (nrow > 0) {
+    if (nrow > 0 && dbg_ok(p, m[h] >= 0 && k + 8 <= p.K, kDbgShardRow, m[h])) {
       const uint16_t* src = shard_row(p.shards, p.mps, p.K, m[h]) + k;
 #pragma unroll
       for (int r = 0; r < 8; ++r)
@@ -492,6 +542,7 @@ __device__ __forceinline__ void prologue_copy_box(const GemmParams& p, int mb, i
 #pragma unroll
   for (int h = 0; h < 4; ++h) {
     const int nrow = min(8, p.M - m[h]);
+    if (!dbg_ok(p, m[h] >= 0 && k + 8 <= p.K, kDbgGathered, m[h])) continue;
 #pragma unroll
     for (int r = 0; r < 8; ++r)
       if (r < nrow) st_v4(p.a_gathered + (int64_t)(m[h] + r) * p.K + k, v[h][r]);
@@ -522,8 +573,10 @@ __device__ __forceinline__ void fetch_prologue(const GemmParams& p, int pw, int 
       named_bar_sync(1, kProWarps * 32);
       if (pw == 0 && lane == 0) {
         const int flag_idx = mb * p.G + g;
-        if (flag_idx != p.inject_skip_flag)
+        if (flag_idx != p.inject_skip_flag && flag_ok(p, flag_idx)) {
+          inject_delay(p, flag_idx);
           st_release_gpu(p.flags + flag_idx, p.fbase + (uint64_t)nbox);
+        }
         if (p.trace) trace_rec(p.trace, p.trace_words, kTraceGather, mb, g, t0, globaltimer_ns());
       }
     }
@@ -557,8 +610,10 @@ __device__ __noinline__ void regfetch_chunk(const GemmParams& p, int mb, int g, 
         if (idx < total) {
           const int r = idx / nv;
           const int cv = idx - r * nv;
-          v[u] = ld_stream_v4(shard_row(p.shards, p.mps, p.K, row0 + r) + c0 + cv * 8);
-          dst[u] = (int64_t)(row0 + r) * p.K + c0 + cv * 8;
+          if (dbg_ok(p, row0 + r < p.M && c0 + cv * 8 + 8 <= p.K, kDbgShardRow, row0 + r)) {
+            v[u] = ld_stream_v4(shard_row(p.shards, p.mps, p.K, row0 + r) + c0 + cv * 8);
+            dst[u] = (int64_t)(row0 + r) * p.K + c0 + cv * 8;
+          }
         }
       }
 #pragma unroll
@@ -573,6 +628,8 @@ __device__ __noinline__ void regfetch_chunk(const GemmParams& p, int mb, int g, 
   for (int idx = lane; idx < total; idx += 32) {
     const int rg = idx % nrg, cg = idx / nrg;
     const int col = c0 + cg * 8;
+    if (!dbg_ok(p, row0 + rg * 8 + 8 <= p.M && col + 8 <= p.K, kDbgStaging, row0 + rg * 8))
+      continue;
     uint4 v[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
@@ -596,7 +653,7 @@ __device__ __forceinline__ void regfetch_loop(const GemmParams& p, int lane, boo
       const int idx = mb * p.G + g;
       uint64_t* f = p.flags + idx;
       int won = 0;
-      if (lane == 0) {
+      if (lane == 0 && flag_ok(p, idx)) {
         const uint64_t v = ld_relaxed_gpu(f);
         if (v < p.fbase)
           won = atomicCAS(reinterpret_cast<unsigned long long*>(f), (unsigned long long)v,
@@ -610,7 +667,10 @@ __device__ __forceinline__ void regfetch_loop(const GemmParams& p, int lane, boo
       fence_proxy_async_global();
       __syncwarp();
       if (lane == 0) {
-        if (idx != p.inject_skip_flag) red_release_add_gpu(f, (uint64_t)chunk_boxes(p, g));
+        if (idx != p.inject_skip_flag) {
+          inject_delay(p, idx);
+          red_release_add_gpu(f, (uint64_t)chunk_boxes(p, g));
+        }
         if (p.trace) trace_rec(p.trace, p.trace_words, kTraceRegFetch, mb, g, t0, globaltimer_ns());
       }
     }
@@ -793,7 +853,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
         const int g0 = chunk_at(0, cur.ws, cur.we);
         if (kAllStaged ? cur.kind != kEmpty
                        : (cur.kind != kLocal && cur.kind != kEmpty && !cur.owns(g0)))
-          cur_peek = ld_relaxed_gpu(p.flags + cur.mb * p.G + g0);
+          if (flag_ok(p, cur.mb * p.G + g0)) cur_peek = ld_relaxed_gpu(p.flags + cur.mb * p.G + g0);
         if (t + (int)gridDim.x < p.num_tiles) tile_ctx<kFused>(p, t + gridDim.x, nxt);
       }
       const int last_nbox = chunk_boxes(p, p.G - 1);
@@ -831,7 +891,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
             }
             if (aborted) break;
           }
-          st_relaxed_gpu(p.started + t, p.epoch);
+          if (dbg_ok(p, t < p.started_words, kDbgStarted, t)) st_relaxed_gpu(p.started + t, p.epoch);
         }
         const int g = chunk_at(gi, cur.ws, cur.we);
         const int mb = cur.mb;
@@ -933,7 +993,8 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
                                   : (n_kind != kLocal && n_kind != kEmpty &&
                                      !(n_kind == kDirect && ng >= n_ws && ng < n_we &&
                                        ng - n_ws >= n_pre));
-          if (nxt_follow) nxt_peek = ld_relaxed_gpu(p.flags + n_mb * p.G + ng);
+          if (nxt_follow && flag_ok(p, n_mb * p.G + ng))
+            nxt_peek = ld_relaxed_gpu(p.flags + n_mb * p.G + ng);
         }
 
         const int r0 = cur.r0;
@@ -1008,7 +1069,9 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
             rslot = 0;
             rphase ^= 1u;
           }
-          if (++pre == nxt.we - nxt.ws) st_relaxed_gpu(p.started + t + gridDim.x, p.epoch);
+          if (++pre == nxt.we - nxt.ws &&
+              dbg_ok(p, t + (int)gridDim.x < p.started_words, kDbgStarted, t + (int)gridDim.x))
+            st_relaxed_gpu(p.started + t + gridDim.x, p.epoch);
         }
         t = nt;
         gi = ngi;
@@ -1332,7 +1395,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
             // a row block inside one shard) the group is inside one shard.
             m[h] = row0 + (4 * (b + h) + (lane >> 3)) * 8;
             const int nrow = min(8, p.M - m[h]);
-            if (nrow > 0) {
+            if (nrow > 0 && dbg_ok(p, m[h] >= 0, kDbgShardRow, m[h])) {
               const uint16_t* src = shard_row(p.shards, p.mps, p.K, m[h]) + k;
 #pragma unroll
               for (int r = 0; r < 8; ++r)
@@ -1342,10 +1405,12 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int nrow = min(8, p.M - m[h]);
+            if (!dbg_ok(p, m[h] >= 0 && k + 8 <= p.K, kDbgGathered, m[h])) continue;
 #pragma unroll
             for (int r = 0; r < 8; ++r)
               if (r < nrow) st_v4(p.a_gathered + (int64_t)(m[h] + r) * p.K + k, v[h][r]);
-            if (publish_m && nrow == 8) {  // M % 8 == 0 for this layout
+            if (publish_m && nrow == 8 &&
+                dbg_ok(p, m[h] + 8 <= p.M, kDbgStaging, m[h])) {  // M % 8 == 0 for this layout
 #pragma unroll
               for (int c = 0; c < 8; ++c)
                 st_v4(p.staging_mk + (int64_t)(k + c) * p.M + m[h], transpose_col(v[h], c));
@@ -1357,8 +1422,11 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
       if (lane == 0) {
         if ((bits & kInfoPublish) && j0 < nbox) {
           const uint32_t done = atom_add_acq_rel_cta_shared(smem_u32(rec + 6), 1u) + 1u;
-          if (done == (uint32_t)min(nbox, kCopyWarps) && flag_idx != p.inject_skip_flag)
+          if (done == (uint32_t)min(nbox, kCopyWarps) && flag_idx != p.inject_skip_flag &&
+              flag_ok(p, flag_idx)) {
+            inject_delay(p, flag_idx);
             st_release_gpu(p.flags + flag_idx, p.fbase + (uint64_t)nbox);
+          }
         }
         mbar_arrive(&rfree[slot]);
       }

@@ -64,11 +64,18 @@
  *
  * Workspace: the fused path needs ready flags (8 bytes per (128-row block,
  * k-group)) and one word per output tile (8 bytes per 128 x 256 tile); both
- * paths need a [K, M] staging buffer for the m-contiguous layout.  By default the library owns them (one set per device,
- * grown on demand; growing synchronises the device).  Calls that use the
- * library workspace on the same device must be ordered (same stream, or
- * ordered by events); calls that may overlap on the GPU need separate
- * caller workspaces (ag_options.workspace).
+ * paths need a [K, M] staging buffer for the m-contiguous layout.  By default
+ * the library owns them (one set per device, grown on demand; growing
+ * synchronises the device).  Calls on one workspace must not overlap on the
+ * GPU.  For the library workspace this is checked: the library remembers the
+ * stream of the last call that used it and an event recorded after that
+ * call; a call on another stream while that event has not completed returns
+ * AG_ERR_BUSY and enqueues nothing (the library cannot see an ordering that
+ * the caller set up between streams with events, so such a call is refused
+ * rather than allowed to race).  Calls on the same stream are ordered by the
+ * stream and never busy.  Work that must overlap on several streams passes a
+ * caller workspace per stream (ag_options.workspace); the library does not
+ * track those.
  */
 #ifndef AGMM_H_
 #define AGMM_H_
@@ -92,7 +99,12 @@ typedef enum ag_status {
   AG_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed; see ag_status_string */
   AG_ERR_TIMEOUT = 4,     /* device-side: a bounded wait ran out (reported by ag_get_device_error) */
   AG_ERR_WORKSPACE = 5,   /* caller workspace smaller than ag_workspace_size() */
-  AG_ERR_TOO_LARGE = 6    /* problem needs more than ag_matmul_noalloc's fixed scratch */
+  AG_ERR_TOO_LARGE = 6,   /* problem needs more than ag_matmul_noalloc's fixed scratch */
+  AG_ERR_BUSY = 7,        /* the library workspace is in use by an unfinished call on another
+                             stream; nothing was enqueued (see "Workspace" above) */
+  AG_ERR_BOUNDS = 8       /* device-side, bounds-checked build only (libagmm_debug.so): an
+                             index fell outside its buffer; the access was skipped
+                             (reported by ag_get_device_error; info = site << 24 | index) */
 } ag_status;
 
 /* Storage types.  AG_DTYPE_FP8_E4M3 is an extension the pages do not cover:
@@ -142,6 +154,24 @@ typedef struct ag_options {
   int64_t workspace_bytes;  /* its size; must be >= ag_workspace_size() */
   float scale_a;            /* AG_DTYPE_FP8_E4M3: per-tensor scale of A (default 1); ignored otherwise */
   float scale_b;            /* AG_DTYPE_FP8_E4M3: per-tensor scale of b (default 1); must be finite */
+  int64_t inject_delay_ns;  /* stress testing (fused calls): every publisher of a ready flag
+                               waits a pseudo-random 0 .. inject_delay_ns after its copies and
+                               before the release store that publishes them, so readers meet
+                               late publishers.  0 = off (default); at most timeout_ns / 16
+                               (the default 2 s timeout allows 125 ms), else
+                               AG_ERR_INVALID_ARG.  Results are unchanged. */
+  /* Tile and pipeline shape.  The pages' tunables ("Fused all-gather+GEMM
+   * HBM-buffer kernel for iris.ops", the defaults table: block sizes,
+   * num_stages, fetch SMs).  0 = automatic (default).  Only the shapes the
+   * library is compiled for are accepted; any other positive value is
+   * AG_ERR_UNSUPPORTED, a negative one AG_ERR_INVALID_ARG. */
+  int32_t block_m;          /* output rows per tile: 256 (a CTA pair per tile; automatic when at
+                               least two SMs are allowed) or 128 (one CTA per tile) */
+  int32_t block_n;          /* output columns per tile: 256 */
+  int32_t block_k;          /* K per pipeline stage, in elements: 64 (16-bit) or 128 (FP8) */
+  int32_t stages;           /* pipeline depth: 6 with block_m 256, 4 with block_m 128 (a value
+                               alone also selects block_m) */
+  int32_t producer_warps;   /* copier warps per CTA that stage A chunks: 4 */
 } ag_options;
 
 /* Fill `opt` with the defaults listed above.  Never fails (NULL is ignored). */
@@ -159,10 +189,11 @@ int ag_then_matmul(const void** a_shards, int D, int m_per_shard, int K, const v
                    const void* bias_or_null, void* a_gathered, void* out, cudaStream_t stream);
 
 /* As above with options (opt may be NULL for the defaults).  ag_then_matmul_ex
- * honours dtype, layout, num_sms, timeout_ns and trace: with the m-contiguous
- * layout its gather kernel also writes the [K, M] staging (library-owned) and
- * the GEMM reads A from there.  It ignores rank, k_per_flag, inject_skip_flag
- * and the caller workspace. */
+ * honours dtype, layout, num_sms, timeout_ns, trace and the tile options
+ * (block_m ... producer_warps): with the m-contiguous layout its gather kernel
+ * also writes the [K, M] staging (library-owned) and the GEMM reads A from
+ * there.  It ignores rank, k_per_flag, inject_skip_flag, inject_delay_ns and
+ * the caller workspace. */
 int ag_matmul_ex(const void** a_shards, int D, int m_per_shard, int K, const void* b, int N,
                  const void* bias_or_null, void* a_gathered, void* out, cudaStream_t stream,
                  const ag_options* opt);
@@ -200,9 +231,12 @@ int ag_chunked_matmul_ex(const void** a_shards, int D, int m_per_shard, int K, c
 size_t ag_workspace_size(int D, int m_per_shard, int K, int N, const ag_options* opt);
 
 /* Synchronises `stream`, then reports the newest device-side error recorded
- * on the current device by a call made since the previous report.  *code is
- * AG_OK when there is none; *info is the flag index or pipeline site that
- * timed out.  Either pointer may be NULL.  Returns AG_OK or AG_ERR_CUDA. */
+ * on the current device by a call made since the previous report.  Errors are
+ * kept in two places -- the library's error word and ag_matmul_noalloc's
+ * scratch -- and when both hold an unreported error, the one of the later
+ * call is reported and the other stays for the next report.  *code is AG_OK
+ * when there is none; *info is the flag index or pipeline site that timed
+ * out.  Either pointer may be NULL.  Returns AG_OK or AG_ERR_CUDA. */
 int ag_get_device_error(cudaStream_t stream, int* code, int* info);
 
 /* Frees the library-owned workspace of the current device (synchronises the
@@ -231,6 +265,8 @@ typedef struct ag_plan {
   int32_t k_per_flag;     /* k-blocks (64 elements; FP8: 128 bytes) per ready flag */
   int32_t prologue_cta0;  /* fetch prologue: CTAs from this index first stage all of A; -1: none */
   int32_t l2_prefetch;    /* 1: the kernel first prefetches all of A into L2 */
+  int32_t block_m;        /* output rows per tile (256: CTA pairs, 128: single CTAs) */
+  int32_t stages;         /* pipeline depth */
 } ag_plan;
 int ag_plan_fused(int D, int m_per_shard, int K, int N, const ag_options* opt, int sms,
                   int pair_clusters, ag_plan* plan);
@@ -274,10 +310,12 @@ int ag_plan_fused(int D, int m_per_shard, int K, int N, const ag_options* opt, i
  * streams without ordering) race on the array and give wrong results; order
  * them on one stream or with events.
  *
- * Set-up: the first call on each device (with that device current) looks up
- * the array's device address once and sets the kernel's shared-memory limit;
- * make that first call before any stream capture begins.  The call itself
- * performs no device allocation or free. */
+ * Set-up: the first call on each device, made with that device current, does
+ * one-time set-up: it looks up the array's device address (the array's name
+ * in host code is only a stand-in for it) and sets the kernel's shared-memory
+ * limit.  Those are CUDA runtime calls that should not run while a stream is
+ * being captured, so make that first call before any stream capture begins.
+ * No call performs a device allocation or free. */
 int ag_matmul_noalloc(const void** a_shards, int D, int m_per_shard, int K, const void* b, int N,
                       const void* bias_or_null, void* a_gathered, void* out,
                       cudaStream_t stream, const ag_options* opt);

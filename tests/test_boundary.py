@@ -45,11 +45,13 @@ def test_options_default_matches_header(lib):
     assert o.inject_skip_flag == -1 and o.timeout_ns == 2_000_000_000
     assert not o.trace and o.trace_words == 0 and not o.workspace and o.workspace_bytes == 0
     assert o.scale_a == 1.0 and o.scale_b == 1.0
-    assert ctypes.sizeof(o) == 72
+    assert o.inject_delay_ns == 0
+    assert (o.block_m, o.block_n, o.block_k, o.stages, o.producer_warps) == (0, 0, 0, 0, 0)
+    assert ctypes.sizeof(o) == 104
 
 
 def test_status_strings(lib):
-    for code in range(6):
+    for code in range(9):
         s = lib.ag_status_string(code)
         assert isinstance(s, bytes) and s
     assert lib.ag_status_string(99) == b"unknown status"
@@ -126,6 +128,44 @@ def test_invalid_arguments_are_rejected_before_cuda(lib, fused):
     D = 17  # one more than AG_MAX_SHARDS
     assert _call(lib, fused, D=D, m=1, shards=[BASE + (r << 24) for r in range(D)]) == UNSUPPORTED
     assert _call(lib, fused, opt=opts(k_per_flag=65537)) == INVALID
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_tile_options_accept_only_compiled_shapes(lib, fused):
+    """block_m / block_n / block_k / stages / producer_warps: the pages'
+    tunables; only the compiled shapes pass validation (a valid one then
+    reaches the first CUDA call, CUDA or UNSUPPORTED without a GPU)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("this check is for hosts without a GPU")
+    for kw in ({"block_m": 64}, {"block_m": 512}, {"block_n": 128}, {"block_k": 32},
+               {"block_k": 128}, {"stages": 5}, {"stages": 8}, {"producer_warps": 8},
+               {"block_m": 128, "stages": 6}, {"block_m": 256, "stages": 4}):
+        assert _call(lib, fused, opt=opts(**kw)) == UNSUPPORTED, kw
+    for kw in ({"block_m": -1}, {"block_n": -256}, {"block_k": -64}, {"stages": -6},
+               {"producer_warps": -4}):
+        assert _call(lib, fused, opt=opts(**kw)) == INVALID, kw
+    for kw in ({"block_m": 128}, {"block_m": 256}, {"block_n": 256}, {"block_k": 64},
+               {"stages": 4}, {"stages": 6}, {"producer_warps": 4},
+               {"block_m": 256, "block_n": 256, "block_k": 64, "stages": 6, "producer_warps": 4}):
+        assert _call(lib, fused, opt=opts(**kw)) in (CUDA, UNSUPPORTED), kw
+    # FP8 counts block_k in 8-bit elements: 128 per stage
+    assert _call(lib, fused, opt=opts(dtype=2, block_k=64)) == UNSUPPORTED
+    assert _call(lib, fused, opt=opts(dtype=2, block_k=128)) in (CUDA, UNSUPPORTED)
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_inject_delay_is_bounded_by_the_timeout(lib, fused):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("this check is for hosts without a GPU")
+    assert _call(lib, fused, opt=opts(inject_delay_ns=-1)) == INVALID
+    # at most timeout_ns / 16: 125 ms with the default 2 s
+    assert _call(lib, fused, opt=opts(inject_delay_ns=125_000_001)) == INVALID
+    assert _call(lib, fused, opt=opts(inject_delay_ns=125_000_000)) in (CUDA, UNSUPPORTED)
+    assert _call(lib, fused, opt=opts(timeout_ns=16_000, inject_delay_ns=1001)) == INVALID
+    assert _call(lib, fused, opt=opts(timeout_ns=16_000, inject_delay_ns=1000)) in (CUDA,
+                                                                                   UNSUPPORTED)
 
 
 @pytest.mark.parametrize("fused", [True, False])

@@ -150,22 +150,13 @@ def test_fp8_identity_b_returns_gathered_a():
     assert torch.equal(out.cpu(), torch.cat(shards).cpu().float().to(torch.bfloat16))
 
 
-def _sample_rows(w, n_random=24):
-    M, m = w.M, w.m_per_shard
-    rows = {0, M - 1}
-    for r in range(w.D):
-        rows |= {r * m, r * m + m - 1}
-    rows |= set(int(v) for v in np.random.default_rng(3).integers(0, M, size=n_random))
-    return np.array(sorted(rows), np.int64)
-
-
 @pytest.mark.parametrize("make", [lambda: inp.fp8_m1024(8), inp.fp8_m16384],
                          ids=["fp8_m1024_d8", "fp8_m16384_d8"])
-def test_fp8_iris_shapes_sampled(oracle_mod, make):
+def test_fp8_iris_shapes_full(oracle_mod, make):
+    """Every output element of the Iris shapes in FP8, fused and barrier."""
     w = make()
     x = inp.make_inputs(w)
-    rows = _sample_rows(w)
-    check(oracle_mod, x, [(*run(x), "fused"), (*run(x, fused=False), "barrier")], rows=rows)
+    check(oracle_mod, x, [(*run(x), "fused"), (*run(x, fused=False), "barrier")])
 
 
 def test_fp8_rejections():

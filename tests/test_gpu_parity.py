@@ -3,10 +3,10 @@
 a_gathered must be bit-exact; out must satisfy, elementwise,
     |out_gpu - out_ref_f32| <= 1e-2 * (|a|.|b|)_ij + 1e-3
 where out_ref_f32 is the oracle's fp32 sum (+ bias) and (|a|.|b|)_ij the sum
-of |a_ik||b_kj|.  At the full benchmark sizes the oracle computes sampled
-rows (shard and tile boundaries plus random rows); everything smaller is
-checked in full.  Both the fused kernel and the barrier baseline are checked
-against the oracle.  The fused kernel's k order is fixed per tile, so its
+of |a_ik||b_kj|.  Every output element is checked, at every size (the
+oracle takes about 6 s for the largest workload, M=16384 N=3584 K=8192, on
+the 16 host cores of a GB300 machine).  Both the fused kernel and the barrier
+baseline are checked against the oracle.  The fused kernel's k order is fixed per tile, so its
 outputs must be bitwise equal for every choice of local rank and staging
 layout; the barrier GEMM runs k in ascending order (a different fp32
 summation order), so it is bitwise equal to itself across layouts.
@@ -39,19 +39,6 @@ def to_device(x: inp.Inputs):
     b = x.b.cuda()
     bias = x.bias.cuda() if x.bias is not None else None
     return shards, b, bias
-
-
-def sample_rows(w: inp.Workload, n_random: int = 24, seed: int = 0) -> np.ndarray:
-    M, m = w.M, w.m_per_shard
-    rows = {0, M - 1}
-    for r in range(w.D):
-        rows |= {r * m, r * m + m - 1, min(M - 1, r * m + m // 2)}
-    for t in (127, 128, 255, 256, M - 128, M - 129):
-        if 0 <= t < M:
-            rows.add(t)
-    rng = np.random.default_rng(seed)
-    rows |= set(int(v) for v in rng.integers(0, M, size=n_random))
-    return np.array(sorted(rows), np.int64)
 
 
 def check(oracle, x: inp.Inputs, a_dev, out_dev, rows=None, what="", more=()):
@@ -102,8 +89,7 @@ def test_cube_sweep(oracle_mod, n):
     w = inp.cube(n)
     x = inp.make_inputs(w)
     (a_f, o_f), (a_b, o_b) = run_both(x)
-    rows = None if n <= 768 else sample_rows(w, seed=n)
-    check(oracle_mod, x, a_f, o_f, rows, what=f"fused cube {n}",
+    check(oracle_mod, x, a_f, o_f, what=f"fused cube {n}",
           more=((a_b, o_b, f"barrier cube {n}"),))
 
 
@@ -112,7 +98,7 @@ def test_iris_m1024(oracle_mod, D):
     w = inp.iris_m1024(D)
     x = inp.make_inputs(w)
     (a_f, o_f), (a_b, o_b) = run_both(x)
-    check(oracle_mod, x, a_f, o_f, sample_rows(w, 64, seed=D), what=f"m1024 D={D}",
+    check(oracle_mod, x, a_f, o_f, what=f"m1024 D={D}",
           more=((a_b, o_b, f"barrier m1024 D={D}"),))
 
 
@@ -120,13 +106,12 @@ def test_iris_m16384_both_layouts(oracle_mod):
     w = inp.iris_m16384()
     x = inp.make_inputs(w)
     shards, b, _ = to_device(x)
-    rows = sample_rows(w, 24, seed=16384)
     a_k, o_k = agmm.ag_matmul(shards, b, layout="k_contiguous")
     a_m, o_m = agmm.ag_matmul(shards, b, layout="m_contiguous")
     a_b, o_b = agmm.ag_then_matmul(shards, b)
     a_bm, o_bm = agmm.ag_then_matmul(shards, b, layout="m_contiguous")
     assert agmm.device_error() == (0, 0)
-    check(oracle_mod, x, a_k, o_k, rows, what="k_contiguous",
+    check(oracle_mod, x, a_k, o_k, what="k_contiguous",
           more=((a_b, o_b, "barrier k_contiguous"),))
     assert_bitwise(a_m, a_k, "a_gathered m vs k")
     assert_bitwise(o_m, o_k, "out m_contiguous vs k_contiguous")
@@ -142,7 +127,7 @@ def test_output_sharded_slice(oracle_mod, layout):
     w = inp.iris_m16384_colshard()
     x = inp.make_inputs(w)
     (a_f, o_f), (a_b, o_b) = run_both(x, layout=layout)
-    check(oracle_mod, x, a_f, o_f, sample_rows(w, 24, seed=448), what=f"colshard {layout}",
+    check(oracle_mod, x, a_f, o_f, what=f"colshard {layout}",
           more=((a_b, o_b, f"barrier colshard {layout}"),))
 
 
@@ -150,7 +135,7 @@ def test_iris_m4096_bias_m_contiguous(oracle_mod):
     w = inp.iris_m4096_bias()
     x = inp.make_inputs(w)
     (a_f, o_f), (a_b, o_b) = run_both(x, layout="m_contiguous")
-    check(oracle_mod, x, a_f, o_f, sample_rows(w, 48, seed=4096), what="bias m_contiguous",
+    check(oracle_mod, x, a_f, o_f, what="bias m_contiguous",
           more=((a_b, o_b, "barrier bias m_contiguous"),))
 
 
@@ -226,7 +211,7 @@ def test_rank_invariance(oracle_mod):
             assert agmm.device_error() == (0, 0)
             assert_bitwise(a_r, ref_a, f"a_gathered rank {rank} {layout}")
             assert_bitwise(o_r, ref_o, f"out rank {rank} {layout}")
-    check(oracle_mod, x, ref_a, ref_o, sample_rows(w, 16), what="cube 1024 rank 0")
+    check(oracle_mod, x, ref_a, ref_o, what="cube 1024 rank 0")
 
 
 @pytest.mark.parametrize("num_sms,kpf", [(1, 16), (3, 1), (7, 4), (0, 2)])
@@ -306,7 +291,7 @@ def test_chunked_pipeline(oracle_mod, name, chunks):
     """The chunked pipeline (chunk s = the s-th sub-block of every shard,
     gathered then multiplied, chunks round-robin over four streams) gives
     a_gathered bitwise and the barrier's out bitwise (same GEMM core and k
-    order), which the oracle checks on sampled rows."""
+    order), which the oracle checks in full."""
     w = {"two_shard": inp.small_two_shard(), "cube_1280": inp.cube(1280),
          "m1024_d8": inp.iris_m1024(8), "m16384_d8": inp.iris_m16384(),
          "ragged": inp.Workload("ragged_chunk", D=3, m_per_shard=37, K=200, N=136, dtype="bf16",
@@ -324,8 +309,7 @@ def test_chunked_pipeline(oracle_mod, name, chunks):
     assert agmm.device_error() == (0, 0)
     assert_bitwise(a_c, a_b, "chunked a_gathered")
     assert_bitwise(o_c, o_b, "chunked out vs barrier")
-    rows = None if w.M <= 1024 else sample_rows(w, 16, seed=chunks)
-    check(oracle_mod, x, a_c, o_c, rows, what=f"chunked {name} S={chunks}")
+    check(oracle_mod, x, a_c, o_c, what=f"chunked {name} S={chunks}")
 
 
 def test_repeat_calls_are_deterministic():

@@ -15,7 +15,7 @@ def plan(D, m, K, N, **kw):
 def test_headline_shape_runs_neither_prologue_nor_prefetch():
     p = plan(8, 2048, 8192, 3584, dtype="fp16")
     assert p == {"grid": 152, "cta_pairs": 1, "tiles": 64 * 14, "k_per_flag": 8,
-                 "prologue_cta0": -1, "l2_prefetch": 0}
+                 "prologue_cta0": -1, "l2_prefetch": 0, "block_m": 256, "stages": 6}
 
 
 @pytest.mark.parametrize("n", [2176, 2304, 2432, 2560, 2688, 2816, 3200, 3328])
@@ -60,6 +60,31 @@ def test_restricted_grids():
     p = plan(4, 160, 1024, 512, num_sms=1)
     assert p["cta_pairs"] == 0 and p["grid"] == 1 and p["tiles"] == 10
     assert agmm.plan_fused(4, 160, 1024, 512, SMS, 0)["cta_pairs"] == 0
+
+
+def test_tile_options_choose_the_compiled_variant():
+    """block_m 128 (or stages 4) selects single CTAs with 128 x 256 tiles,
+    block_m 256 (or stages 6) CTA pairs; 256-row tiles need a CTA pair."""
+    for kw in ({"block_m": 128}, {"stages": 4}, {"block_m": 128, "stages": 4}):
+        p = plan(8, 2048, 8192, 3584, dtype="fp16", **kw)
+        assert (p["cta_pairs"], p["block_m"], p["stages"], p["grid"]) == (0, 128, 4, 152), kw
+        assert p["tiles"] == 128 * 14
+    for kw in ({"block_m": 256}, {"stages": 6}, {"block_n": 256, "block_k": 64,
+                                                 "producer_warps": 4}):
+        p = plan(8, 2048, 8192, 3584, dtype="fp16", **kw)
+        assert (p["cta_pairs"], p["block_m"], p["stages"]) == (1, 256, 6), kw
+    with pytest.raises(agmm.AgmmError) as e:
+        plan(4, 160, 1024, 512, num_sms=1, block_m=256)
+    assert e.value.status == 2
+    with pytest.raises(agmm.AgmmError) as e:
+        agmm.plan_fused(4, 160, 1024, 512, SMS, 0, stages=6)
+    assert e.value.status == 2
+    for kw in ({"block_m": 192}, {"stages": 3}, {"block_n": 128}, {"producer_warps": 2},
+               {"block_m": 128, "stages": 6}):
+        with pytest.raises(agmm.AgmmError) as e:
+            plan(8, 2048, 8192, 3584, **kw)
+        assert e.value.status == 2, kw
+    assert plan(8, 2048, 16384, 3584, dtype="fp8_e4m3", block_k=128)["block_m"] == 256
 
 
 def test_rejections():

@@ -142,3 +142,38 @@ def test_noalloc_fp8_matches_ag_matmul():
     assert agmm.device_error() == (0, 0)
     assert torch.equal(a_g.view(torch.uint8), ref_a.view(torch.uint8))
     assert torch.equal(out, ref_out)
+
+
+@pytest.mark.parametrize("name", ["multi_wave", "fetch_prologue"])
+def test_noalloc_multi_wave_and_prologue_match_ag_matmul(name):
+    """Calls of more than one wave on the shared scratch: M=4096 N=3584
+    K=8192 over 8 shards takes three waves of CTA pairs, where per-tile words
+    left by the previous call decide between waiting for a chunk's owner and
+    taking the chunk over; cube 2432 takes 1.3 waves and its CTAs with a tile
+    fewer first stage all of A (the fetch prologue).  Two calls in a row each,
+    bitwise equal to ag_matmul (the same kernel and launch plan)."""
+    w = {"multi_wave": inp.Workload("noalloc_mw", D=8, m_per_shard=512, K=8192, N=3584,
+                                    dtype="bf16", bias=True),
+         "fetch_prologue": inp.cube(2432)}[name]
+    sms = agmm.num_sms()
+    plan = agmm.plan_fused(w.D, w.m_per_shard, w.K, w.N, sms, sms // 2)
+    assert plan["tiles"] > plan["grid"] // 2
+    if name == "fetch_prologue":
+        assert plan["prologue_cta0"] >= 0
+    x = inp.make_inputs(w)
+    shards = [s.cuda() for s in x.shards]
+    b = x.b.cuda()
+    bias = x.bias.cuda() if x.bias is not None else None
+    ref_a, ref_out = agmm.ag_matmul(shards, b, bias, rank=1)
+    ref_a, ref_out = ref_a.clone(), ref_out.clone()
+    assert agmm.device_error() == (0, 0)
+    for call in range(2):
+        a_g = torch.full_like(ref_a, float("nan"))
+        out = torch.full_like(ref_out, float("nan"))
+        opt = agmm.default_options()
+        opt.rank = 1
+        assert _noalloc(shards, b, bias, a_g, out, opt) == 0
+        assert agmm.device_error() == (0, 0)
+        assert torch.equal(a_g.view(torch.int16), ref_a.view(torch.int16)), f"call {call}"
+        assert _within(out, ref_out, ref_a, b)
+        assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16)), f"call {call}"
