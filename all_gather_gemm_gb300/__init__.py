@@ -327,7 +327,8 @@ class AgPlan(ctypes.Structure):
     _fields_ = [("grid", ctypes.c_int32), ("cta_pairs", ctypes.c_int32),
                 ("tiles", ctypes.c_int32), ("k_per_flag", ctypes.c_int32),
                 ("prologue_cta0", ctypes.c_int32), ("l2_prefetch", ctypes.c_int32),
-                ("block_m", ctypes.c_int32), ("stages", ctypes.c_int32)]
+                ("block_m", ctypes.c_int32), ("stages", ctypes.c_int32),
+                ("k_ascending", ctypes.c_int32)]
 
 
 def plan_fused(D, m_per_shard, K, N, sms, pair_clusters, layout: str = "k_contiguous",

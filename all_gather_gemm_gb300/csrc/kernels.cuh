@@ -177,6 +177,8 @@ struct GemmParams {
   float scale_ab;           // FP8 inputs: scale_a * scale_b, applied to the fp32 sum
   int inject_skip_flag;     // this flag index is never published (fault injection)
   int pro_cta0;             // fetch prologue: CTAs from this index stage every chunk first (-1: off)
+  int k_asc;                // 1: every tile visits its k-groups in ascending order
+  int stage_from;           // staging ahead starts at this position of the current tile's k-loop
   int l2_prefetch;          // 1: each CTA prefetches its share of the shards into L2 at the start
   int64_t inject_delay_ns;  // stress testing: publishers wait up to this long before a release
   int64_t flag_words;       // bounds of flags / started (checked in AGMM_DEBUG builds only)
@@ -327,6 +329,15 @@ __device__ __forceinline__ int chunk_at(int i, int ws, int we) {
   if (i < wlen) return ws + i;
   const int j = i - wlen;
   return j < ws ? j : j + wlen;
+}
+
+// k-group visited at position i of a tile: k ascending when the launch plan
+// says so (p.k_asc: calls of four or more waves, where a CTA's next window is
+// staged while it works on the current tile, so every tile of a row block can
+// read A in the same order as its neighbours and the barrier GEMM, sharing
+// each k-slice in L2), else the owned window first (chunk_at).
+__device__ __forceinline__ int order_at(const GemmParams& p, int i, int ws, int we) {
+  return p.k_asc ? i : chunk_at(i, ws, we);
 }
 
 // The column block whose tiles own k-group g: the nb < w0 with
@@ -698,6 +709,16 @@ __device__ __forceinline__ void stage_load_2d(void* dst, const CUtensorMap* m, u
 }
 
 template <bool kPair>
+__device__ __forceinline__ void stage_load_2d_hint(void* dst, const CUtensorMap* m, uint64_t* bar,
+                                                   uint32_t bar_c, int32_t x, int32_t y,
+                                                   uint64_t pol) {
+  if constexpr (kPair)
+    tma_load_2d_pair_hint(dst, m, bar_c, x, y, pol);
+  else
+    tma_load_2d_hint(dst, m, bar, x, y, pol);
+}
+
+template <bool kPair>
 __device__ __forceinline__ void stage_load_3d(void* dst, const CUtensorMap* m, uint64_t* bar,
                                               uint32_t bar_c, int32_t x, int32_t y, int32_t z) {
   if constexpr (kPair)
@@ -841,6 +862,9 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
       // followers in other CTAs find those chunks published early.  `pre`
       // counts the chunks of nxt handed so far (window order), `cur_pre`
       // those of the current tile, which it then loads without staging.  The
+      // hand-off starts at position p.stage_from of the current tile (the
+      // plan sets it half-way through for calls of four or more waves), so
+      // the staged copy is still in L2 when the next wave reads it.  The
       // next tile is marked started only once its whole window is handed:
       // until then a follower may still take its chunks over, as for any
       // tile that has not started.
@@ -850,7 +874,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
       uint64_t cur_peek = 0;
       if (t < p.num_tiles) {
         tile_ctx<kFused>(p, t, cur);
-        const int g0 = chunk_at(0, cur.ws, cur.we);
+        const int g0 = order_at(p, 0, cur.ws, cur.we);
         if (kAllStaged ? cur.kind != kEmpty
                        : (cur.kind != kLocal && cur.kind != kEmpty && !cur.owns(g0)))
           if (flag_ok(p, cur.mb * p.G + g0)) cur_peek = ld_relaxed_gpu(p.flags + cur.mb * p.G + g0);
@@ -893,7 +917,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
           }
           if (dbg_ok(p, t < p.started_words, kDbgStarted, t)) st_relaxed_gpu(p.started + t, p.epoch);
         }
-        const int g = chunk_at(gi, cur.ws, cur.we);
+        const int g = order_at(p, gi, cur.ws, cur.we);
         const int mb = cur.mb;
         const int flag_idx = mb * p.G + g;
         const int nbox = g == p.G - 1 ? last_nbox : p.kpf;
@@ -988,7 +1012,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
         uint64_t nxt_peek = 0;
         bool nxt_follow = false;
         if (kFused && nt < p.num_tiles) {
-          const int ng = chunk_at(ngi, n_ws, n_we);
+          const int ng = order_at(p, ngi, n_ws, n_we);
           nxt_follow = kAllStaged ? n_kind != kEmpty
                                   : (n_kind != kLocal && n_kind != kEmpty &&
                                      !(n_kind == kDirect && ng >= n_ws && ng < n_we &&
@@ -1055,6 +1079,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
                     t_chunk, globaltimer_ns());
         if (kFused && !aborted && !new_tile && t + (int)gridDim.x < p.num_tiles &&
             (nxt.kind == kLocal || nxt.kind == kDirect) && pre < nxt.we - nxt.ws &&
+            gi >= p.stage_from &&
             mbar_test_wait(&rfree[rslot], rphase ^ 1u)) {
           // Stage ahead: one chunk of the next tile's window.
           const int pg = nxt.ws + pre;
@@ -1299,7 +1324,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
         const int we = kFused ? chunk_end(p, nb) : 0;
         const int n0 = nb * kBN + (int)rank * P::kBCols;  // this CTA's columns (pair: the rank's half)
         for (int gi = 0; gi < p.G && !aborted; ++gi) {
-          const int g = chunk_at(gi, ws, we);
+          const int g = order_at(p, gi, ws, we);
           const int nbox = chunk_boxes(p, g);
           for (int j = 0; j < nbox; ++j) {
             const int kb = g * p.kpf + j;

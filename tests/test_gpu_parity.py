@@ -117,6 +117,11 @@ def test_iris_m16384_both_layouts(oracle_mod):
     assert_bitwise(o_m, o_k, "out m_contiguous vs k_contiguous")
     assert_bitwise(a_bm, a_k, "a_gathered barrier m")
     assert_bitwise(o_bm, o_b, "out barrier m_contiguous vs barrier k_contiguous")
+    # twelve waves: the plan runs every fused tile k ascending, as the barrier GEMM
+    sms = agmm.num_sms()
+    assert agmm.plan_fused(w.D, w.m_per_shard, w.K, w.N, sms, sms // 2,
+                           dtype="fp16")["k_ascending"] == 1
+    assert_bitwise(o_k, o_b, "fused (k ascending) vs barrier")
 
 
 @pytest.mark.parametrize("layout", ["k_contiguous", "m_contiguous"])

@@ -15,7 +15,8 @@ def plan(D, m, K, N, **kw):
 def test_headline_shape_runs_neither_prologue_nor_prefetch():
     p = plan(8, 2048, 8192, 3584, dtype="fp16")
     assert p == {"grid": 152, "cta_pairs": 1, "tiles": 64 * 14, "k_per_flag": 8,
-                 "prologue_cta0": -1, "l2_prefetch": 0, "block_m": 256, "stages": 6}
+                 "prologue_cta0": -1, "l2_prefetch": 0, "block_m": 256, "stages": 6,
+                 "k_ascending": 1}
 
 
 @pytest.mark.parametrize("n", [2176, 2304, 2432, 2560, 2688, 2816, 3200, 3328])
@@ -60,6 +61,20 @@ def test_restricted_grids():
     p = plan(4, 160, 1024, 512, num_sms=1)
     assert p["cta_pairs"] == 0 and p["grid"] == 1 and p["tiles"] == 10
     assert agmm.plan_fused(4, 160, 1024, 512, SMS, 0)["cta_pairs"] == 0
+
+
+@pytest.mark.parametrize("D,m,K,N,waves4", [(8, 2048, 8192, 3584, True), (8, 512, 8192, 3584, False),
+                                            (8, 512, 4096, 4096, False), (8, 128, 8192, 3584, False),
+                                            (8, 1024, 8192, 7168, True)])
+def test_k_order_by_wave_count(D, m, K, N, waves4):
+    """k-contiguous calls of four or more waves run every tile k ascending;
+    fewer waves, and the m-contiguous layout, keep each tile's owned k-range
+    first (the fetch prologue, which owns nothing, runs k ascending without
+    this flag)."""
+    p = plan(D, m, K, N, dtype="fp16")
+    assert (p["tiles"] >= 4 * p["grid"] // 2) == waves4
+    assert p["k_ascending"] == int(waves4)
+    assert plan(D, m, K, N, layout="m_contiguous")["k_ascending"] == 0
 
 
 def test_tile_options_choose_the_compiled_variant():
