@@ -709,16 +709,6 @@ __device__ __forceinline__ void stage_load_2d(void* dst, const CUtensorMap* m, u
 }
 
 template <bool kPair>
-__device__ __forceinline__ void stage_load_2d_hint(void* dst, const CUtensorMap* m, uint64_t* bar,
-                                                   uint32_t bar_c, int32_t x, int32_t y,
-                                                   uint64_t pol) {
-  if constexpr (kPair)
-    tma_load_2d_pair_hint(dst, m, bar_c, x, y, pol);
-  else
-    tma_load_2d_hint(dst, m, bar, x, y, pol);
-}
-
-template <bool kPair>
 __device__ __forceinline__ void stage_load_3d(void* dst, const CUtensorMap* m, uint64_t* bar,
                                               uint32_t bar_c, int32_t x, int32_t y, int32_t z) {
   if constexpr (kPair)
