@@ -443,22 +443,23 @@ int plan_launch(GemmParams& p, const Shape& s, int cap, int pair_clusters, bool 
       p.w0 = 0;
     }
   }
-  // k-contiguous calls of four or more waves: every tile runs k ascending
-  // (the tiles of a row block then read each A k-slice at about the same
-  // time, as in the barrier GEMM, and share it in L2), and a CTA hands its
-  // next tile's window to the copiers from half-way through the current tile,
-  // so that staged chunks are still in L2 when the next wave reads them.
-  // Measured at M=16384 N=3584 K=8192 (ncu, per fused launch): DRAM reads
-  // 1293 -> 1069 MB, 589 -> 579 us; interleaved timing 609 -> 601 us.  On one
-  // to three waves ascending order cost 2-7 us (the first wave waits on the
-  // owners' copiers) and the later hand-off 2 us at cube 4096; with the
-  // m-contiguous staging neither helped.  Those keep the owned window first.
-  // The choice depends on the shape only, so every rank of a call gets the
-  // same per-tile order (and, with k ascending, the barrier GEMM's results
-  // bit for bit).
-  if (fused && !layout_m && p.w0 > 0 && tiles >= 4 * grid_units) {
+  // Calls of four or more waves: every tile runs k ascending (the tiles of a
+  // row block then read each A k-slice at about the same time, as in the
+  // barrier GEMM, and share it in L2); with the k-contiguous staging a CTA
+  // also hands its next tile's window to the copiers from half-way through
+  // the current tile, so that staged chunks are still in L2 when the next
+  // wave reads them.  Measured at M=16384 N=3584 K=8192 (ncu, per fused
+  // launch): DRAM reads 1293 -> 1069 MB, 589 -> 579 us; interleaved timing
+  // 609 -> 601 us.  On one to three waves ascending order cost 2-7 us (the
+  // first wave waits on the owners' copiers) and the later hand-off 2 us at
+  // cube 4096, and with the m-contiguous staging the later hand-off did not
+  // help: those keep the owned window first / hand off at once.  The order
+  // depends on the shape only, so every rank and both layouts of a call get
+  // the same per-tile order (and, with k ascending, the barrier GEMM's
+  // results bit for bit).
+  if (fused && p.w0 > 0 && tiles >= 4 * grid_units) {
     p.k_asc = 1;
-    p.stage_from = p.G / 2;
+    if (!layout_m) p.stage_from = p.G / 2;
   }
   p.flag_words = (int64_t)s.num_mb * p.G;
   p.started_words = p.num_tiles;

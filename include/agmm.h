@@ -267,10 +267,10 @@ typedef struct ag_plan {
   int32_t l2_prefetch;    /* 1: the kernel first prefetches all of A into L2 */
   int32_t block_m;        /* output rows per tile (256: CTA pairs, 128: single CTAs) */
   int32_t stages;         /* pipeline depth */
-  int32_t k_ascending;    /* 1: every tile runs k ascending (k-contiguous calls of four or
-                             more waves; the results then equal ag_then_matmul_ex's with the
-                             same tile options bit for bit); 0: each tile starts at the
-                             k-range it owns */
+  int32_t k_ascending;    /* 1: every tile runs k ascending (calls of four or more waves; the
+                             results then equal ag_then_matmul_ex's with the same tile
+                             options bit for bit); 0: each tile starts at the k-range it
+                             owns */
 } ag_plan;
 int ag_plan_fused(int D, int m_per_shard, int K, int N, const ag_options* opt, int sms,
                   int pair_clusters, ag_plan* plan);

@@ -67,14 +67,13 @@ def test_restricted_grids():
                                             (8, 512, 4096, 4096, False), (8, 128, 8192, 3584, False),
                                             (8, 1024, 8192, 7168, True)])
 def test_k_order_by_wave_count(D, m, K, N, waves4):
-    """k-contiguous calls of four or more waves run every tile k ascending;
-    fewer waves, and the m-contiguous layout, keep each tile's owned k-range
-    first (the fetch prologue, which owns nothing, runs k ascending without
-    this flag)."""
+    """Calls of four or more waves run every tile k ascending, in both
+    layouts; fewer waves keep each tile's owned k-range first (the fetch
+    prologue, which owns nothing, runs k ascending without this flag)."""
     p = plan(D, m, K, N, dtype="fp16")
     assert (p["tiles"] >= 4 * p["grid"] // 2) == waves4
     assert p["k_ascending"] == int(waves4)
-    assert plan(D, m, K, N, layout="m_contiguous")["k_ascending"] == 0
+    assert plan(D, m, K, N, layout="m_contiguous")["k_ascending"] == int(waves4)
 
 
 def test_tile_options_choose_the_compiled_variant():
