@@ -360,6 +360,38 @@ def run_sweep(args):
                           "device_error": code}), flush=True)
 
 
+def run_cublas(args):
+    """Context only, not the product path: cuBLAS (torch.matmul) on the
+    workload's gathered A and b, timed like the bench (CUDA events, L2 flushed
+    between calls), to compare this library's GEMM core with a library GEMM of
+    the same shape.  16-bit workloads only."""
+    import torch
+
+    from all_gather_gemm_gb300 import inputs as inp
+    w = headline_workload(args.workload)
+    if w.dtype not in ("bf16", "fp16"):
+        raise SystemExit("--cublas compares 16-bit workloads only")
+    x = inp.make_inputs(w)
+    a = torch.cat([s.cuda() for s in x.shards])
+    b = x.b.cuda()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
+    for _ in range(max(args.warmup, 3)):
+        torch.matmul(a, b)
+    ts = []
+    for i in range(args.steps):
+        flush.fill_(i)
+        s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s_.record()
+        torch.matmul(a, b)
+        e_.record()
+        torch.cuda.synchronize()
+        ts.append(s_.elapsed_time(e_) * 1e3)
+    print(json.dumps({"cublas_context": w.name, "M": w.M, "N": w.N, "K": w.K, "dtype": w.dtype,
+                      "us_median": statistics.median(ts), "us_mean": statistics.fmean(ts),
+                      "tflops": w.flops / (statistics.median(ts) * 1e-6) / 1e12,
+                      "steps": args.steps, "l2": "flushed between calls"}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -378,6 +410,9 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the bench line: fused vs barrier on every workload of the "
                          "parity configs, one JSON line each")
+    ap.add_argument("--cublas", action="store_true",
+                    help="context only: time cuBLAS (torch.matmul) on the workload's gathered A "
+                         "and b instead of the bench line")
     ap.add_argument("--only", default="",
                     help="with --sweep: comma-separated substrings; keep workloads whose "
                          "name contains one")
@@ -390,6 +425,9 @@ def main():
 
     if args.sweep:
         run_sweep(args)
+        return
+    if args.cublas:
+        run_cublas(args)
         return
     if args.impl == "reference":
         run_reference(args, w, rank, world)
