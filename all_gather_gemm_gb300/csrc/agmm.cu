@@ -1193,6 +1193,8 @@ const char* ag_status_string(int status) {
     case AG_ERR_TIMEOUT: return "device-side wait timed out";
     case AG_ERR_WORKSPACE: return "caller workspace too small";
     case AG_ERR_TOO_LARGE: return "problem needs more than the fixed no-alloc scratch";
+    case AG_ERR_BUSY: return "library workspace in use by an unfinished call on another stream";
+    case AG_ERR_BOUNDS: return "device-side index outside its buffer (bounds-checked build)";
     default: return "unknown status";
   }
 }

@@ -51,10 +51,14 @@ def test_options_default_matches_header(lib):
 
 
 def test_status_strings(lib):
+    unknown = lib.ag_status_string(99)
+    assert unknown == b"unknown status"
     for code in range(9):
         s = lib.ag_status_string(code)
-        assert isinstance(s, bytes) and s
-    assert lib.ag_status_string(99) == b"unknown status"
+        assert isinstance(s, bytes) and s and s != unknown, code
+    assert b"busy" in lib.ag_status_string(7) or b"in use" in lib.ag_status_string(7)
+    assert b"bounds" in lib.ag_status_string(8) or b"outside" in lib.ag_status_string(8)
+    assert set(agmm.STATUS) == set(range(9))
 
 
 def test_workspace_size(lib):
