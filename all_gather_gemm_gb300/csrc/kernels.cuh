@@ -178,6 +178,8 @@ struct GemmParams {
   int inject_skip_flag;     // this flag index is never published (fault injection)
   int pro_cta0;             // fetch prologue: CTAs from this index stage every chunk first (-1: off)
   int k_asc;                // 1: every tile visits its k-groups in ascending order
+  int local_direct;         // 1 (fused m-contiguous pairs): pairs wholly in the local shard read it
+                            // K-major, unstaged
   int stage_from;           // staging ahead starts at this position of the current tile's k-loop
   int l2_prefetch;          // 1: each CTA prefetches its share of the shards into L2 at the start
   int64_t inject_delay_ns;  // stress testing: publishers wait up to this long before a release
@@ -369,6 +371,9 @@ struct TileCtx {
   int r0;          // shard holding the block's first row
   bool one_shard;  // every row of the block lies in shard r0
   int ws, we;      // owned window of k-groups [ws, we); ws is also the k-loop start
+  bool pair_local; // CTA pairs with p.local_direct: every row of the pair's two blocks is in
+                   // the local shard (or past M), so the pair reads A straight from the
+                   // shard, even with the m-contiguous staging
   __device__ __forceinline__ bool owns(int g) const { return g >= ws && g < we; }
 };
 
@@ -386,6 +391,12 @@ __device__ __forceinline__ void tile_ctx(const GemmParams& p, int t, TileCtx& c)
   if (!kFused && p.seg_blocks) {
     c.sd = c.mb / p.seg_blocks;
     c.sy = (c.mb - c.sd * p.seg_blocks) * kBM;
+  }
+  c.pair_local = false;
+  if (kFused && p.pair && p.local_direct) {
+    const int m0 = c.mb & ~1;
+    const int k1 = m0 + 1 < p.num_mb ? block_kind(p, m0 + 1) : (int)kEmpty;
+    c.pair_local = m0 < p.num_mb && block_kind(p, m0) == kLocal && (k1 == kLocal || k1 == kEmpty);
   }
   if (c.mb >= p.num_mb) {
     c.kind = kEmpty;
@@ -767,7 +778,10 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
   constexpr bool kLayoutM = mode_layout_m(kMode);
   // Fused m-contiguous on CTA pairs: every A tile is read from the [K, M]
   // staging (MN-major) -- the owner's window and local rows included, once
-  // published -- because one pair MMA reads both CTAs' A with one major-ness.
+  // published -- because one pair MMA reads both CTAs' A with one major-ness;
+  // except in pairs whose rows all lie in the local shard (TileCtx::pair_local):
+  // both CTAs read those K-major from the shard, nobody waits for them, and
+  // their chunks go to a_gathered only (no reader needs them transposed).
   constexpr bool kAllStaged = kFused && kLayoutM && kPair;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -865,8 +879,9 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
       if (t < p.num_tiles) {
         tile_ctx<kFused>(p, t, cur);
         const int g0 = order_at(p, 0, cur.ws, cur.we);
-        if (kAllStaged ? cur.kind != kEmpty
-                       : (cur.kind != kLocal && cur.kind != kEmpty && !cur.owns(g0)))
+        if ((kAllStaged && !cur.pair_local)
+                ? cur.kind != kEmpty
+                : (cur.kind != kLocal && cur.kind != kEmpty && !cur.owns(g0)))
           if (flag_ok(p, cur.mb * p.G + g0)) cur_peek = ld_relaxed_gpu(p.flags + cur.mb * p.G + g0);
         if (t + (int)gridDim.x < p.num_tiles) tile_ctx<kFused>(p, t + gridDim.x, nxt);
       }
@@ -886,7 +901,8 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
           // with CTA pairs that pipeline also waits on the partner CTA.
           if (cur.kind == kLocal || cur.kind == kDirect) {
             const uint32_t wbits =
-                (cur.kind == kDirect || kAllStaged) ? (kInfoStage | kInfoPublish) : kInfoStage;
+                (cur.kind == kDirect || (kAllStaged && !cur.pair_local)) ? (kInfoStage | kInfoPublish)
+                                                                         : kInfoStage;
             for (int wg = cur.ws + cur_pre; wg < cur.we; ++wg) {
               if (!wait_bar(p, &rfree[rslot], rphase ^ 1u, abort_flag, kSiteRing)) {
                 aborted = true;
@@ -920,7 +936,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
           // the shard.
           // (Owned chunks were handed to the copiers at the tile start.)
           const bool staged_ahead = cur.owns(g) && g - cur.ws < cur_pre;
-          if (kind == kLocal && !kAllStaged) {
+          if (kind == kLocal && (!kAllStaged || cur.pair_local)) {
             direct = true;
           } else if (kind == kEmpty) {
             // rows past M: the gathered copy's maps read zeros there
@@ -997,14 +1013,16 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
         const int n_kind = new_tile ? nxt.kind : cur.kind;
         const int n_ws = new_tile ? nxt.ws : cur.ws;
         const int n_we = new_tile ? nxt.we : cur.we;
+        const bool n_pl = new_tile ? nxt.pair_local : cur.pair_local;
         // (staging ahead does not run on a tile's last chunk, so pre is final here)
         const int n_pre = new_tile ? pre : cur_pre;
         uint64_t nxt_peek = 0;
         bool nxt_follow = false;
         if (kFused && nt < p.num_tiles) {
           const int ng = order_at(p, ngi, n_ws, n_we);
-          nxt_follow = kAllStaged ? n_kind != kEmpty
-                                  : (n_kind != kLocal && n_kind != kEmpty &&
+          nxt_follow = (kAllStaged && !n_pl)
+                           ? n_kind != kEmpty
+                           : (n_kind != kLocal && n_kind != kEmpty &&
                                      !(n_kind == kDirect && ng >= n_ws && ng < n_we &&
                                        ng - n_ws >= n_pre));
           if (nxt_follow && flag_ok(p, n_mb * p.G + ng))
@@ -1074,7 +1092,8 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
           // Stage ahead: one chunk of the next tile's window.
           const int pg = nxt.ws + pre;
           hand_chunk(ring + rslot * kRingWords, &rfull[rslot],
-                     kInfoStage | ((nxt.kind == kDirect || kAllStaged) ? kInfoPublish : 0u), nxt.mb, pg,
+                     kInfoStage | ((nxt.kind == kDirect || (kAllStaged && !nxt.pair_local))
+                                       ? kInfoPublish : 0u), nxt.mb, pg,
                      chunk_boxes(p, pg), nxt.mb * p.G + pg, seq, p);
           if (p.trace) {
             const uint64_t now = globaltimer_ns();
@@ -1120,8 +1139,10 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
       const uint32_t idesc_k = kF8 ? idesc_e4m3_f32(kM, kBN) : idesc_f16_f32(ab_bf16, 0, 1, kM, kBN);
       const uint32_t idesc_mn = idesc_f16_f32(ab_bf16, 1, 1, kM, kBN);
       // A's major-ness: K-major for the k-contiguous layout, MN-major for the
-      // [K, M] staging; only the single-CTA fused m-contiguous kernel mixes
-      // the two (shard rows K-major), and reads it from the stage record.
+      // [K, M] staging.  The single-CTA fused m-contiguous kernel mixes the two
+      // per chunk (shard rows K-major) and reads it from the stage record; the
+      // pair kernel decides per tile (K-major only for pairs wholly in the
+      // local shard), so its loop reads no shared memory for it.
       constexpr int kAMajor = !kLayoutM ? 0 : (kFused && !kPair) ? 2 : 1;
       bool aborted = false;
       int stage = 0;
@@ -1139,6 +1160,14 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
       for (int j = 0; j < my_tiles && !aborted; ++j) {
         const int buf = j & 1;
         const uint32_t use = (uint32_t)(j >> 1);
+        bool tile_mn = kAMajor == 1;
+        if constexpr (kAllStaged) {
+          if (p.local_direct) {
+            TileCtx tc;
+            tile_ctx<true>(p, blockIdx.x + j * gridDim.x, tc);
+            tile_mn = !tc.pair_local;
+          }
+        }
         if (!wait_bar<kPair>(p, &tmem_empty[buf], (use & 1u) ^ 1u, abort_flag, kSiteTmemEmpty)) {
           aborted = true;
           break;
@@ -1155,7 +1184,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
           const uint32_t ph1 = stage + 1 == kStages ? phase ^ 1u : phase;
           const bool more = done + 1 < total;
           const bool t_full = more && mbar_test_wait(&full[s1], ph1);
-          const bool a_mn = kAMajor == 2 ? (info[stage] & kInfoAmn) != 0 : kAMajor == 1;
+          const bool a_mn = kAMajor == 2 ? (info[stage] & kInfoAmn) != 0 : tile_mn;
           const uint32_t idesc = a_mn ? idesc_mn : idesc_k;
           const uint32_t a_addr = smem_u32(smem + stage * kStageBytes);
           const uint32_t b_addr = a_addr + kAStageBytes;

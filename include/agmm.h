@@ -270,7 +270,8 @@ typedef struct ag_plan {
   int32_t k_ascending;    /* 1: every tile runs k ascending (calls of four or more waves; the
                              results then equal ag_then_matmul_ex's with the same tile
                              options bit for bit); 0: each tile starts at the k-range it
-                             owns */
+                             owns.  With the m-contiguous layout on CTA pairs, such calls
+                             also read pairs wholly in the local shard straight from it */
 } ag_plan;
 int ag_plan_fused(int D, int m_per_shard, int K, int N, const ag_options* opt, int sms,
                   int pair_clusters, ag_plan* plan);

@@ -100,6 +100,9 @@ STRESS = [
                                 dtype="bf16", a_dist="uniform", b_dist="uniform",
                                 bias=True), "k_contiguous"),  # owners' copiers, take-overs
     ("m4096_d8_bias_m", inp.iris_m4096_bias(), "m_contiguous"),  # every chunk via [K, M]
+    # twelve waves, m-contiguous: k ascending, and pairs wholly in the (rotating) local
+    # shard read it directly while every other chunk goes through the [K, M] staging
+    ("m16384_d8_m", inp.iris_m16384(), "m_contiguous"),
     ("regfetch", inp.Workload("stress_regfetch", D=5, m_per_shard=130, K=2048, N=1280,
                               dtype="fp16", bias=True), "k_contiguous"),  # register fetcher
 ]
