@@ -1148,12 +1148,13 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
       int stage = 0;
       uint32_t phase = 0;
       // The MMA issue queue is shallow: whatever this thread waits on between
-      // two stages' MMAs idles the tensor pipe.  So the next stage's barriers
-      // are tested (without blocking) before this stage's MMAs are issued,
-      // and the result is used after them; a blocking wait happens only when
-      // that stage had not landed yet.  A completed phase stays completed
-      // until the stage is refilled, which needs this thread's commit, so a
-      // positive test also holds across a tile boundary.
+      // two stages' MMAs idles the tensor pipe.  So the next stage's barrier
+      // is tested (without blocking) right after this stage's MMAs and commit
+      // are issued -- its latency then overlaps the queued MMAs -- and a
+      // blocking wait happens only when that stage had not landed yet.  A
+      // completed phase stays completed until the stage is refilled, which
+      // needs this thread's commit, so a positive test also holds across a
+      // tile boundary.
       bool ready = false;  // stage `stage` (phase `phase`) is known to have landed
       const int total = my_tiles * p.num_kb;
       int done = 0;
@@ -1183,21 +1184,25 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
           const int s1 = stage + 1 == kStages ? 0 : stage + 1;
           const uint32_t ph1 = stage + 1 == kStages ? phase ^ 1u : phase;
           const bool more = done + 1 < total;
-          const bool t_full = more && mbar_test_wait(&full[s1], ph1);
           const bool a_mn = kAMajor == 2 ? (info[stage] & kInfoAmn) != 0 : tile_mn;
           const uint32_t idesc = a_mn ? idesc_mn : idesc_k;
           const uint32_t a_addr = smem_u32(smem + stage * kStageBytes);
           const uint32_t b_addr = a_addr + kAStageBytes;
+          const uint64_t a_desc0 = a_mn ? smem_desc_sw128(a_addr, kMnChunkBytes, 1024)
+                                        : smem_desc_sw128(a_addr, 16, 1024);
+          const uint64_t b_desc0 = kF8 ? smem_desc_sw128(b_addr, 16, 1024)
+                                       : smem_desc_sw128(b_addr, kMnChunkBytes, 1024);
+          // Each k-slice of 16 elements moves a descriptor's start address by
+          // 32 bytes (K-major: inside the swizzle row) or 2048 bytes (MN-major:
+          // two 1024-byte groups of 8 k-rows), i.e. its address field
+          // (address >> 4, 14 bits, no carry within the stage) by 2 or 128:
+          // one add per MMA instead of rebuilding the descriptor.
+          const uint64_t a_step = a_mn ? 128u : 2u;
+          constexpr uint64_t b_step = kF8 ? 2u : 128u;
 #pragma unroll
           for (int ks = 0; ks < kBK / kUmmaK; ++ks) {
-            // K-major A: advance 16 elements (32 bytes) inside the swizzle row.
-            // MN-major A/B: advance 16 k-rows (2 x 1024-byte groups).
-            const uint64_t a_desc =
-                a_mn ? smem_desc_sw128(a_addr + ks * 2048, kMnChunkBytes, 1024)
-                     : smem_desc_sw128(a_addr + ks * 32, 16, 1024);
-            // B: MN-major 16-bit [K, N] boxes, or (FP8) K-major rows of [N, K].
-            const uint64_t b_desc = kF8 ? smem_desc_sw128(b_addr + ks * 32, 16, 1024)
-                                        : smem_desc_sw128(b_addr + ks * 2048, kMnChunkBytes, 1024);
+            const uint64_t a_desc = a_desc0 + a_step * ks;
+            const uint64_t b_desc = b_desc0 + b_step * ks;
             const uint32_t acc = (kb | ks) != 0 ? 1u : 0u;
             if constexpr (kF8 && kPair)
               umma_f8_pair(d_tmem, a_desc, b_desc, idesc, acc);
@@ -1212,6 +1217,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
             umma_commit_pair_mc(&empty[stage], 3);  // frees the stage in both CTAs
           else
             umma_commit(&empty[stage]);
+          const bool t_full = more && mbar_test_wait(&full[s1], ph1);
           stage = s1;
           phase = ph1;
           ready = t_full;
