@@ -134,6 +134,7 @@ bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
 // with 4 stages, 256-row tiles on CTA pairs with 6 (Pipe<>), both 256 columns
 // wide, 64 16-bit elements (128 FP8 bytes) per stage, 4 copier warps.
 constexpr int kStagesSingle = 4, kStagesPair = 6;
+constexpr int kSingleMaxKb = 32;  // automatic single CTAs: K up to 32 k-blocks, one wave
 static_assert(Pipe<false>::kStages == kStagesSingle && Pipe<true>::kStages == kStagesPair,
               "tile options and compiled pipelines differ");
 int check_tile_options(const ag_options& o) {
@@ -403,7 +404,17 @@ int plan_launch(GemmParams& p, const Shape& s, int cap, int pair_clusters, bool 
   const bool want_pair = o.block_m == 2 * kBM || o.stages == kStagesPair;
   const bool can_pair = cap >= 2 && pair_clusters >= 1;
   if (want_pair && !can_pair) return AG_ERR_UNSUPPORTED;
-  const bool pair = can_pair && !want_single;
+  // Automatic tile shape: CTA pairs, except for short calls -- K of at most
+  // kSingleMaxKb k-blocks with every 128-row tile in one wave of the grid --
+  // which run on single CTAs: there the start-up of a cluster launch weighs
+  // more than the pair's halved B traffic.  Measured (means, L2 flushed), on
+  // the one-wave cubes n = 256 ... 2048 single CTAs were 1.5-2 us faster for
+  // the fused call and the barrier GEMM alike (cube_1024: fused 21.3 -> 19.6,
+  // barrier 22.0 -> 19.9 us); at M=1024 N=3584 K=8192 (one wave either way)
+  // pairs stayed faster (fused 57.7 vs 62.3 us).
+  const bool short_one_wave =
+      s.num_kb <= kSingleMaxKb && (int64_t)s.num_mb * s.num_nb <= (int64_t)cap;
+  const bool pair = can_pair && !want_single && (want_pair || !short_one_wave);
   Shape sched = s;
   sched.num_mb = pair ? (s.num_mb + 1) / 2 : s.num_mb;
   const int units = pair ? std::min(cap / 2, pair_clusters) : cap;  // CTAs, or CTA pairs

@@ -165,8 +165,10 @@ typedef struct ag_options {
    * num_stages, fetch SMs).  0 = automatic (default).  Only the shapes the
    * library is compiled for are accepted; any other positive value is
    * AG_ERR_UNSUPPORTED, a negative one AG_ERR_INVALID_ARG. */
-  int32_t block_m;          /* output rows per tile: 256 (a CTA pair per tile; automatic when at
-                               least two SMs are allowed) or 128 (one CTA per tile) */
+  int32_t block_m;          /* output rows per tile: 256 (a CTA pair per tile) or 128 (one CTA
+                               per tile).  Automatic: 256 when at least two SMs are allowed,
+                               except calls with K of at most 32 k-blocks (2048 16-bit
+                               elements) whose 128-row tiles all fit one wave: 128 */
   int32_t block_n;          /* output columns per tile: 256 */
   int32_t block_k;          /* K per pipeline stage, in elements: 64 (16-bit) or 128 (FP8) */
   int32_t stages;           /* pipeline depth: 6 with block_m 256, 4 with block_m 128 (a value

@@ -39,12 +39,34 @@ def test_cube_shapes_without_prologue(n):
 
 @pytest.mark.parametrize("n", [256, 1024, 2048])
 def test_one_wave_cubes(n):
+    """K of at most 32 k-blocks and every 128-row tile in one wave: single
+    CTAs (128 x 256 tiles), one per tile."""
     p = plan(8, n // 8, n, n)
-    T = (n // 256) * (n // 256)
-    assert p["tiles"] == T and p["grid"] == 2 * T and p["prologue_cta0"] == -1
+    T = (n // 128) * (n // 256)
+    assert (p["cta_pairs"], p["block_m"], p["stages"]) == (0, 128, 4)
+    assert p["tiles"] == T and p["grid"] == T and p["prologue_cta0"] == -1
     assert p["l2_prefetch"] == 1
     num_kb, num_nb = n // 64, n // 256
     assert p["k_per_flag"] == min(num_kb, min(8, max(4, num_kb // num_nb)))
+    # the tile options still force CTA pairs
+    q = plan(8, n // 8, n, n, block_m=256)
+    assert q["cta_pairs"] == 1 and q["tiles"] == (n // 256) * (n // 256) and q["grid"] == 2 * q["tiles"]
+
+
+@pytest.mark.parametrize("D,m,K,N,single", [
+    (8, 256, 2048, 2048, True),     # cube 2048: 32 k-blocks, 128 tiles
+    (8, 272, 2176, 2176, False),    # cube 2176: 34 k-blocks
+    (8, 128, 8192, 3584, False),    # M=1024 K=8192: one wave, long K
+    (8, 2048, 2048, 3584, False),   # K short but 128 x 14 tiles: more than one wave
+    (2, 128, 256, 256, True),       # the two-shard case
+])
+def test_automatic_tile_shape(D, m, K, N, single):
+    p = plan(D, m, K, N)
+    assert p["cta_pairs"] == (0 if single else 1)
+    assert p["block_m"] == (128 if single else 256)
+    # FP8 counts K in bytes: the same rule on K/2 16-bit words
+    if K % 16 == 0:
+        assert plan(D, m, 2 * K, N, dtype="fp8_e4m3")["cta_pairs"] == (0 if single else 1)
 
 
 def test_m_contiguous_and_fp8():
