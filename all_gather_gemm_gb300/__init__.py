@@ -16,8 +16,9 @@ FP8 (``torch.float8_e4m3fn`` shards): ``b`` is given transposed, [N, K] e4m3,
 ``out`` is bf16 and ``out = scale_a * scale_b * (a_gathered @ b.T) + bias``
 (k-contiguous layout only).
 
-With the environment variable ``AGMM_VARIANT=debug`` set before the first
-call, the bounds-checked build ``libagmm_debug.so`` is loaded instead (every
+With the environment variable ``AGMM_VARIANT=debug`` (or ``AGMM_DEBUG=1``) set
+before the first call, the bounds-checked build ``libagmm_debug.so`` is loaded
+instead (every
 flag, per-tile word, shard-row and staging index checked on the device; a
 violation is reported by ``device_error()`` as AG_ERR_BOUNDS).
 """
@@ -81,8 +82,10 @@ _lib = None
 
 def variant() -> str:
     """The library variant this process loads: "release", or "debug" (the
-    bounds-checked build) when AGMM_VARIANT=debug."""
-    v = os.environ.get("AGMM_VARIANT", "release") or "release"
+    bounds-checked build) when AGMM_VARIANT=debug or AGMM_DEBUG=1."""
+    v = os.environ.get("AGMM_VARIANT", "") or ""
+    if not v:
+        v = "debug" if os.environ.get("AGMM_DEBUG", "0") not in ("", "0") else "release"
     if v not in _build.VARIANTS:
         raise ValueError(f"AGMM_VARIANT must be one of {sorted(_build.VARIANTS)}, not {v!r}")
     return v

@@ -212,3 +212,19 @@ def test_python_binding_fails_loudly_without_cuda_tensors():
     s = [torch.zeros(4, 8, dtype=torch.bfloat16)]
     with pytest.raises((ValueError, RuntimeError)):
         agmm.ag_matmul(s, torch.zeros(8, 8, dtype=torch.bfloat16))
+
+
+def test_library_variant_selection(monkeypatch):
+    """AGMM_VARIANT=debug or AGMM_DEBUG=1 select the bounds-checked build;
+    anything else unknown is refused."""
+    for env, want in (({}, "release"), ({"AGMM_DEBUG": "1"}, "debug"),
+                      ({"AGMM_DEBUG": "0"}, "release"), ({"AGMM_VARIANT": "debug"}, "debug"),
+                      ({"AGMM_VARIANT": "release", "AGMM_DEBUG": "1"}, "release")):
+        monkeypatch.delenv("AGMM_VARIANT", raising=False)
+        monkeypatch.delenv("AGMM_DEBUG", raising=False)
+        for k, v in env.items():
+            monkeypatch.setenv(k, v)
+        assert agmm.variant() == want, env
+    monkeypatch.setenv("AGMM_VARIANT", "fast")
+    with pytest.raises(ValueError):
+        agmm.variant()
