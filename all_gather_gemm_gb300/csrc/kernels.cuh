@@ -1133,7 +1133,9 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
     // count their bytes on the leader's barriers themselves.
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // The whole warp runs this loop in step (waits are voted, so every lane
+    // takes the same branch); one elected lane issues each MMA and commit.
+    {
       const uint32_t ab_bf16 = p.fp16 ? 0u : 1u;
       constexpr uint32_t kM = kPair ? 2 * kBM : kBM;
       const uint32_t idesc_k = kF8 ? idesc_e4m3_f32(kM, kBN) : idesc_f16_f32(ab_bf16, 0, 1, kM, kBN);
@@ -1147,13 +1149,13 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
       bool aborted = false;
       int stage = 0;
       uint32_t phase = 0;
-      // The MMA issue queue is shallow: whatever this thread waits on between
+      // The MMA issue queue is shallow: whatever this warp waits on between
       // two stages' MMAs idles the tensor pipe.  So the next stage's barrier
       // is tested (without blocking) right after this stage's MMAs and commit
       // are issued -- its latency then overlaps the queued MMAs -- and a
       // blocking wait happens only when that stage had not landed yet.  A
       // completed phase stays completed until the stage is refilled, which
-      // needs this thread's commit, so a positive test also holds across a
+      // needs this warp's commit, so a positive test also holds across a
       // tile boundary.
       bool ready = false;  // stage `stage` (phase `phase`) is known to have landed
       const int total = my_tiles * p.num_kb;
@@ -1169,14 +1171,16 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
             tile_mn = !tc.pair_local;
           }
         }
-        if (!wait_bar<kPair>(p, &tmem_empty[buf], (use & 1u) ^ 1u, abort_flag, kSiteTmemEmpty)) {
+        if (!__all_sync(0xffffffffu, wait_bar<kPair>(p, &tmem_empty[buf], (use & 1u) ^ 1u,
+                                                     abort_flag, kSiteTmemEmpty))) {
           aborted = true;
           break;
         }
         tcgen05_fence_after_sync();
         const uint32_t d_tmem = tmem_base + (uint32_t)(buf * kBN);
         for (int kb = 0; kb < p.num_kb; ++kb, ++done) {
-          if (!ready && !wait_bar(p, &full[stage], phase, abort_flag, kSiteFull)) {
+          if (!ready &&
+              !__all_sync(0xffffffffu, wait_bar(p, &full[stage], phase, abort_flag, kSiteFull))) {
             aborted = true;
             break;
           }
@@ -1217,7 +1221,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
             umma_commit_pair_mc(&empty[stage], 3);  // frees the stage in both CTAs
           else
             umma_commit(&empty[stage]);
-          const bool t_full = more && mbar_test_wait(&full[s1], ph1);
+          const bool t_full = __all_sync(0xffffffffu, more && mbar_test_wait(&full[s1], ph1));
           stage = s1;
           phase = ph1;
           ready = t_full;
@@ -1228,7 +1232,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
         else
           umma_commit(&tmem_full[buf]);
       }
-      // All MMAs issued by this thread complete before TMEM is released.
+      // All MMAs issued by this warp complete before TMEM is released.
       if constexpr (kPair)
         umma_commit_pair(drain);
       else
