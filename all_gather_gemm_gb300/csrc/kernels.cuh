@@ -26,6 +26,10 @@
 //               load from a single shard (a row block straddling shards whose
 //               row count is not a multiple of 8) and publishes them.  When A
 //               is small it first asks L2 for the CTA's share of the shards.
+//               Then it works out, a tile ahead of the A issuer, when every
+//               flag of the issuer's next tile is published (readiness_loop),
+//               so that the issuer reads such a tile with no flag reads or
+//               fences of its own.
 //   warps 8-11  copiers (fused only), off the MMA pipeline.  The A issuer
 //               hands a chunk's record to them through a ring in shared
 //               memory; they copy the chunk's boxes (spread over the four
@@ -122,8 +126,10 @@ struct Pipe {
   // full, empty [kStages]; tmem_full, tmem_empty [2]; drain; rfull, rfree
   // [kRing]; pro (fetch prologue done)
   static constexpr int kBars = 2 * kStages + 4 + 1 + 2 * kRing + 1;
+  // (+ the issuer's progress word, the TMEM address, the abort word, the two
+  // tile-readiness words and the issuer's tile counter: 32 bytes)
   static constexpr int kSmemBytes =
-      1024 + kData + 8 * kBars + 4 * kStages + 4 * kRing * kRingWords + 16 + 64;
+      1024 + kData + 8 * kBars + 4 * kStages + 4 * kRing * kRingWords + 32 + 64;
   static_assert(kSmemBytes <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
 };
 
@@ -699,6 +705,78 @@ __device__ __forceinline__ void regfetch_loop(const GemmParams& p, int lane, boo
   }
 }
 
+// Tile readiness, worked out ahead of the A issuer (fused kernels, the
+// register-fetch warp once its own chunks are done).  For each of the CTA's
+// tiles in order, the warp polls every ready flag the issuer could wait on in
+// that tile -- all non-empty chunks of the tile's row block except the
+// local-shard ones it reads straight from the shard (m-contiguous pairs: all
+// but those of pairs wholly in the local shard), the tile's own window
+// included -- until all are published, then takes them with an acquire fence
+// and tells the issuer with ready[j & 1] = j + 1 (release, CTA scope).  The
+// issuer, seeing that (acquire), issues one proxy fence and reads the rest of
+// the tile's chunks with no flag reads or fences of its own.  The warp works
+// on tile j only once the issuer has reached tile j - 1 (`itile`; one word per
+// tile parity, so it never overwrites the word of a tile still in use), and
+// gives up on a tile the issuer has already left behind.  Every exit decision
+// is voted, so the warp stays converged; every wait is bounded, and whatever
+// the warp does not report the issuer checks chunk by chunk itself.
+template <bool kAllStaged>
+__device__ __forceinline__ void readiness_loop(const GemmParams& p, int lane, int my_tiles,
+                                               uint32_t* ready, volatile uint32_t* itile,
+                                               volatile int* abort_flag) {
+  for (int j = 0; j < my_tiles; ++j) {
+    // Throttle: until the issuer is at tile j - 1 (bounded; the limit restarts
+    // whenever the issuer moves on).
+    uint32_t seen = *itile;
+    uint64_t t0 = globaltimer_ns();
+    for (;;) {
+      const uint32_t now_tile = __shfl_sync(0xffffffffu, *itile, 0);
+      if (now_tile + 1 >= (uint32_t)j) break;
+      bool stop = false;
+      if (lane == 0) {
+        const uint64_t now = globaltimer_ns();
+        if (now_tile != seen) {
+          seen = now_tile;
+          t0 = now;
+        }
+        stop = *abort_flag != 0 || now - t0 > (uint64_t)p.pipe_timeout_ns;
+      }
+      if (__shfl_sync(0xffffffffu, stop ? 1 : 0, 0)) return;
+      __nanosleep(512);
+    }
+    TileCtx c;
+    tile_ctx<true>(p, blockIdx.x + j * (int)gridDim.x, c);
+    const bool need = (kAllStaged && !c.pair_local) ? c.kind != kEmpty
+                                                     : (c.kind != kLocal && c.kind != kEmpty);
+    bool ok = true;
+    if (need) {
+      const uint64_t w0 = globaltimer_ns();
+      for (;;) {
+        bool mine = true;
+        for (int g = lane; g < p.G; g += 32) {
+          const int idx = c.mb * p.G + g;
+          if (!flag_ok(p, idx) ||
+              ld_relaxed_gpu(p.flags + idx) < p.fbase + (uint64_t)chunk_boxes(p, g))
+            mine = false;
+        }
+        if (__all_sync(0xffffffffu, mine)) break;
+        bool stop = false;
+        if (lane == 0)
+          stop = *abort_flag != 0 || *itile > (uint32_t)j ||
+                 globaltimer_ns() - w0 > (uint64_t)p.pipe_timeout_ns || error_this_call(p);
+        if (__shfl_sync(0xffffffffu, stop ? 1 : 0, 0)) {
+          ok = false;
+          break;
+        }
+        __nanosleep(256);
+      }
+      if (ok) fence_acquire_gpu();  // each lane: the flags it read were released
+    }
+    __syncwarp();  // (orders every lane's acquire before lane 0's release)
+    if (ok && lane == 0) st_release_cta_shared(&ready[j & 1], (uint32_t)j + 1u);
+  }
+}
+
 __device__ __forceinline__ uint32_t pack2(float lo, float hi, int fp16) {
   if (fp16) {
     __half2 h = __floats2half2_rn(lo, hi);
@@ -801,6 +879,8 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
   volatile uint32_t* iseq = ring + kRing * kRingWords;  // issuer progress (chunks), a liveness signal
   uint32_t* tmem_slot = ring + kRing * kRingWords + 1;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint32_t* ready = tmem_slot + 2;                // [2] fused: tile readiness (readiness_loop)
+  volatile uint32_t* itile = tmem_slot + 4;       // fused: the A issuer's tile counter
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -825,6 +905,9 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
     mbar_init(drain, 1);
     *iseq = 0;
     *abort_flag = 0;
+    ready[0] = 0;
+    ready[1] = 0;
+    *itile = 0;
     fence_mbarrier_init();
     prefetch_tensormap(&p.tm_a);
     prefetch_tensormap(&p.tm_b);
@@ -876,6 +959,10 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
       int t = blockIdx.x, gi = 0;
       int pre = 0, cur_pre = 0;
       uint64_t cur_peek = 0;
+      // Fused: this CTA's tile counter (mirrored in *itile for the readiness
+      // warp) and whether that warp has reported the current tile ready.
+      uint32_t tj = 0;
+      bool tile_fast = false;
       if (t < p.num_tiles) {
         tile_ctx<kFused>(p, t, cur);
         const int g0 = order_at(p, 0, cur.ws, cur.we);
@@ -936,12 +1023,20 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
           // the shard.
           // (Owned chunks were handed to the copiers at the tile start.)
           const bool staged_ahead = cur.owns(g) && g - cur.ws < cur_pre;
+          if (!tile_fast && ld_acquire_cta_shared(&ready[tj & 1]) == tj + 1u) {
+            // Every flag of this tile is published and acquired (readiness_loop):
+            // one proxy fence orders that before all of the tile's loads.
+            tile_fast = true;
+            fence_proxy_async_global();
+          }
           if (kind == kLocal && (!kAllStaged || cur.pair_local)) {
             direct = true;
           } else if (kind == kEmpty) {
             // rows past M: the gathered copy's maps read zeros there
           } else if (kind == kDirect && cur.owns(g) && !staged_ahead && !kAllStaged) {
             direct = true;
+          } else if (tile_fast) {
+            // published: read the staged copy
           } else {
             const uint64_t target = p.fbase + (uint64_t)nbox;
             if (cur_peek >= target) {
@@ -1018,7 +1113,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
         const int n_pre = new_tile ? pre : cur_pre;
         uint64_t nxt_peek = 0;
         bool nxt_follow = false;
-        if (kFused && nt < p.num_tiles) {
+        if (kFused && nt < p.num_tiles && (new_tile || !tile_fast)) {
           const int ng = order_at(p, ngi, n_ws, n_we);
           nxt_follow = (kAllStaged && !n_pl)
                            ? n_kind != kEmpty
@@ -1114,10 +1209,16 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
           cur_pre = pre;
           pre = 0;
           if (t + (int)gridDim.x < p.num_tiles) tile_ctx<kFused>(p, t + gridDim.x, nxt);
+          if (kFused) {
+            ++tj;
+            tile_fast = false;
+            *itile = tj;
+          }
         }
         if (nxt_follow) cur_peek = nxt_peek;
         if (kFused) *iseq = (uint32_t)seq;
       }
+      if (kFused) *itile = 0x7fffffffu;  // done: the readiness warp has nothing left to do
       if (kFused && wait_bar(p, &rfree[rslot], rphase ^ 1u, abort_flag, kSiteRing)) {
         // End of stream (if the slot does not free, the abort flag is set and
         // the copiers leave on it).
@@ -1408,6 +1509,8 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
       }
     }
     regfetch_loop(p, lane, kLayoutM);
+    __syncwarp();
+    readiness_loop<kAllStaged>(p, lane, my_tiles, ready, itile, abort_flag);
     __syncwarp();
   } else if (kFused) {
     // ---------------------------------------------------------- copiers
