@@ -1126,55 +1126,68 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
 
         const int r0 = cur.r0;
         const bool one_shard = cur.one_shard;
-        for (int j = 0; j < nbox; ++j) {
-          const int kb = g * p.kpf + j;
-          if (!wait_bar(p, &empty[stage], phase ^ 1u, abort_flag, kSiteEmpty)) {
-            aborted = true;
-            break;
+        // The chunk's loads.  One loop per kind of A box, so that nothing in
+        // the per-stage path branches on the chunk's kind: the issuer's time
+        // per stage bounds how far ahead of the MMA it keeps the ring.
+        auto stage_loop = [&](auto&& load_a) {
+          for (int j = 0; j < nbox; ++j) {
+            const int kb = g * p.kpf + j;
+            if (!wait_bar(p, &empty[stage], phase ^ 1u, abort_flag, kSiteEmpty)) {
+              aborted = true;
+              return;
+            }
+            info[stage] = bits;
+            uint8_t* a_dst = smem + stage * kStageBytes;
+            const uint32_t bar_c = full_c + 8u * (uint32_t)stage;
+            if (!kPair || rank == 0)
+              mbar_arrive_expect_tx(&full[stage], kPair ? 2 * kAStageBytes : kAStageBytes);
+            load_a(a_dst, &full[stage], bar_c, kb * kBK);
+            issued_mask |= 1u << stage;
+            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+            ++seq;
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
-          info[stage] = bits;
-          uint8_t* a_dst = smem + stage * kStageBytes;
-          const uint32_t bar_c = full_c + 8u * (uint32_t)stage;
-          if (!kPair || rank == 0)
-            mbar_arrive_expect_tx(&full[stage], kPair ? 2 * kAStageBytes : kAStageBytes);
-          if (direct) {
-            if (one_shard) {
-              stage_load_2d<kPair>(a_dst, &p.tm_shard[r0], &full[stage], bar_c, kb * kBK,
-                                   mb * kBM - r0 * p.mps);
-            } else {
-              // Walk the row groups (2^sh_log2 rows, which divides both 128
-              // and m_per_shard, so no group straddles a boundary) across the
-              // shards without a division per group.  Past the last shard the
-              // row stays out of range: TMA zero-fills it.
-              const int h = 1 << p.sh_log2;
-              int r = r0, lr = mb * kBM - r0 * p.mps;
+        };
+        if (direct && one_shard) {
+          const CUtensorMap* m = &p.tm_shard[r0];
+          const int y = mb * kBM - r0 * p.mps;
+          stage_loop([&](uint8_t* a_dst, uint64_t* fb, uint32_t bar_c, int x) {
+            stage_load_2d<kPair>(a_dst, m, fb, bar_c, x, y);
+          });
+        } else if (direct) {
+          // Walk the row groups (2^sh_log2 rows, which divides both 128 and
+          // m_per_shard, so no group straddles a boundary) across the shards
+          // without a division per group.  Past the last shard the row stays
+          // out of range: TMA zero-fills it.
+          stage_loop([&](uint8_t* a_dst, uint64_t* fb, uint32_t bar_c, int x) {
+            const int h = 1 << p.sh_log2;
+            int r = r0, lr = mb * kBM - r0 * p.mps;
 #pragma unroll 1
-              for (int q = 0; q < (kBM >> p.sh_log2); ++q) {
-                stage_load_2d<kPair>(a_dst + q * h * 128, &p.tm_shard8[r], &full[stage], bar_c,
-                                     kb * kBK, lr);
-                lr += h;
-                if (lr >= p.mps && r < p.D - 1) {
-                  lr -= p.mps;
-                  ++r;
-                }
+            for (int q = 0; q < (kBM >> p.sh_log2); ++q) {
+              stage_load_2d<kPair>(a_dst + q * h * 128, &p.tm_shard8[r], fb, bar_c, x, lr);
+              lr += h;
+              if (lr >= p.mps && r < p.D - 1) {
+                lr -= p.mps;
+                ++r;
               }
             }
-          } else if (kLayoutM) {
-            stage_load_2d<kPair>(a_dst, &p.tm_a_mk, &full[stage], bar_c, mb * kBM, kb * kBK);
-            stage_load_2d<kPair>(a_dst + kMnChunkBytes, &p.tm_a_mk, &full[stage], bar_c,
-                                 mb * kBM + 64, kb * kBK);
-          } else if (!kFused && p.seg_blocks) {
-            stage_load_3d<kPair>(a_dst, &p.tm_a, &full[stage], bar_c, kb * kBK, cur.sy, cur.sd);
-          } else {
-            stage_load_2d<kPair>(a_dst, &p.tm_a, &full[stage], bar_c, kb * kBK, mb * kBM);
-          }
-          issued_mask |= 1u << stage;
-          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-          ++seq;
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          });
+        } else if (kLayoutM) {
+          stage_loop([&](uint8_t* a_dst, uint64_t* fb, uint32_t bar_c, int x) {
+            stage_load_2d<kPair>(a_dst, &p.tm_a_mk, fb, bar_c, mb * kBM, x);
+            stage_load_2d<kPair>(a_dst + kMnChunkBytes, &p.tm_a_mk, fb, bar_c, mb * kBM + 64, x);
+          });
+        } else if (!kFused && p.seg_blocks) {
+          stage_loop([&](uint8_t* a_dst, uint64_t* fb, uint32_t bar_c, int x) {
+            stage_load_3d<kPair>(a_dst, &p.tm_a, fb, bar_c, x, cur.sy, cur.sd);
+          });
+        } else {
+          stage_loop([&](uint8_t* a_dst, uint64_t* fb, uint32_t bar_c, int x) {
+            stage_load_2d<kPair>(a_dst, &p.tm_a, fb, bar_c, x, mb * kBM);
+          });
         }
         if (p.trace)  // b: k-group | 1 << 16 if loaded from a shard | 2 << 16 if staged here
           trace_rec(p.trace, p.trace_words, kTraceIssue, mb,
