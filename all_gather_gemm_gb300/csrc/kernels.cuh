@@ -7,40 +7,41 @@
 // onto persistent sm_103a CTA pairs (clusters of two; one CTA per SM) with
 // specialised warps:
 //
-//   warp 0      A issuer: the A loads and the ready-flag protocol.  Every
-//               (row block, k-group) chunk has an owner: the column block
-//               whose tile starts its k-loop there (tiles of one row block
-//               start at evenly spread k-groups).  The owner has the chunk
-//               staged (a tile ahead, where it can) and loads it; the other
-//               tiles of the row block follow: they wait on the chunk's
-//               ready flag (read one chunk ahead) and load the staged copy.
-//               Chunks of the local shard are read straight from it and
-//               never waited on.
+//   warp 0      A loads.  Barrier GEMM: the A issuer.  Fused: the A loader,
+//               which issues each chunk's loads from the descriptor the
+//               protocol warp (warp 7) wrote for it.
 //   warp 1      MMA issuer (the pair's even CTA): tcgen05.mma.cta_group::2
 //               256 x 256 x 16 (bf16/fp16; FP8 E4M3: x 32) with fp32
 //               accumulation into one of two TMEM accumulators.
 //   warps 2-5   epilogue: tcgen05.ld, (FP8: x scale) + fp32 bias, round to
 //               16 bits, 128-byte-swizzled shared memory, TMA store.
 //   warp 6      B loader: b's k-blocks in the A issuer's order.
-//   warp 7      register fetcher (fused only): copies chunks that TMA cannot
-//               load from a single shard (a row block straddling shards whose
-//               row count is not a multiple of 8) and publishes them.  When A
-//               is small it first asks L2 for the CTA's share of the shards.
-//               Then it works out, a tile ahead of the A issuer, when every
-//               flag of the issuer's next tile is published (readiness_loop),
-//               so that the issuer reads such a tile with no flag reads or
-//               fences of its own.
-//   warps 8-11  copiers (fused only), off the MMA pipeline.  The A issuer
-//               hands a chunk's record to them through a ring in shared
+//   warp 7      protocol (fused only): the ready-flag protocol, a few chunks
+//               ahead of the A loader.  Every (row block, k-group) chunk has
+//               an owner: the column block whose tile starts its k-loop there
+//               (tiles of one row block start at evenly spread k-groups).  The
+//               owner has the chunk staged (a tile ahead, where it can) and
+//               loads it; the other tiles of the row block follow: they wait
+//               on the chunk's ready flag (read one chunk ahead) and load the
+//               staged copy.  Chunks of the local shard are read straight
+//               from it and never waited on.  Flag reads, waits, take-overs
+//               and hand-offs all happen here, so none of them delays a load.
+//               When A is small this warp first asks L2 for the CTA's share of
+//               the shards.
+//   warps 8-11  copiers (fused only), off the MMA pipeline.  The protocol
+//               warp hands a chunk's record to them through a ring in shared
 //               memory; they copy the chunk's boxes (spread over the four
 //               warps) from its shard into a_gathered (the k-contiguous
 //               staging) -- and, for the m-contiguous layout, transposed into
 //               the [K, M] staging, which is what followers then read -- with
 //               16-byte global loads and stores, and the last of them to
-//               finish publishes the chunk.
+//               finish publishes the chunk.  The first copier starts as the
+//               register fetcher: it copies the chunks that TMA cannot load
+//               from a single shard (a row block straddling shards whose row
+//               count is not a multiple of 8) and publishes them.
 //
 // Each staged box is therefore read from its shard once, and no atomic sits
-// on the issuer's path.  If a follower finds a chunk unpublished while its owner
+// on the load path.  If a follower finds a chunk unpublished while its owner
 // tile has not started yet (its CTA is still busy with an earlier tile, or the
 // grid is small), it takes the chunk over: one atom.max decides between
 // competing followers, and the winner loads, stages and publishes it.  A chunk
@@ -90,11 +91,11 @@ enum Mode : int { kGemmK = 0, kGemmM = 1, kFusedK = 2, kFusedM = 3 };
 
 __host__ __device__ constexpr bool mode_fused(int m) { return m >= kFusedK; }
 __host__ __device__ constexpr bool mode_layout_m(int m) { return m == kGemmM || m == kFusedM; }
-// Warp roles: 0 A loads (and, fused, the ready-flag protocol), 1 MMA (pair:
-// the even CTA's), 2..5 epilogue, 6 B loads; fused: 7 register fetcher, 8..11
-// copiers.
+// Warp roles: 0 A loads, 1 MMA (pair: the even CTA's), 2..5 epilogue, 6 B
+// loads; fused: 7 the ready-flag protocol, 8..11 copiers (8 also the register
+// fetcher).
 constexpr int kBWarp = 2 + kEpiWarps;
-constexpr int kRegWarp = 3 + kEpiWarps;
+constexpr int kProtoWarp = 3 + kEpiWarps;
 constexpr int kCopyWarp0 = 4 + kEpiWarps;
 __host__ __device__ constexpr int mode_threads(int m) {
   return 32 * (3 + kEpiWarps + (mode_fused(m) ? 1 + kCopyWarps : 0));
@@ -112,6 +113,14 @@ constexpr uint32_t kInfoEnd = 8u;      // chunk record: the issuer is done, the 
 constexpr int kRing = 8;
 constexpr int kRingWords = 8;
 
+// Chunk descriptors handed from the protocol warp to the A loader (fused):
+// {kind bits | bits << 8, row block, k-group | boxes << 16, first shard}.
+constexpr int kDRing = 4;
+constexpr uint32_t kDescDirect = 1u;    // load from a shard (else from the staging)
+constexpr uint32_t kDescOneShard = 2u;  // ... from one shard map (else row groups across shards)
+constexpr uint32_t kDescFence = 4u;     // staged data behind a flag: proxy fence before the loads
+constexpr uint32_t kDescEnd = 8u;       // no more chunks
+
 // Pipeline shape.  One CTA per output tile (kPair = false): 4 stages of A
 // (128 x 64) + B (64 x 256).  A CTA pair per 256 x 256 tile (kPair = true):
 // each CTA stages its own 128 rows of A and half of B's 256 columns, so a
@@ -124,12 +133,12 @@ struct Pipe {
   static constexpr int kStageBytes = kAStageBytes + kBStageBytes;
   static constexpr int kData = kStages * kStageBytes + kEpiWarps * kEpiBufs * kEpiBufBytes;
   // full, empty [kStages]; tmem_full, tmem_empty [2]; drain; rfull, rfree
-  // [kRing]; pro (fetch prologue done)
-  static constexpr int kBars = 2 * kStages + 4 + 1 + 2 * kRing + 1;
-  // (+ the issuer's progress word, the TMEM address, the abort word, the two
-  // tile-readiness words and the issuer's tile counter: 32 bytes)
-  static constexpr int kSmemBytes =
-      1024 + kData + 8 * kBars + 4 * kStages + 4 * kRing * kRingWords + 32 + 64;
+  // [kRing]; pro (fetch prologue done); dfull, dfree [kDRing]
+  static constexpr int kBars = 2 * kStages + 4 + 1 + 2 * kRing + 1 + 2 * kDRing;
+  // (+ the chunk descriptors, the issuer's progress word, the TMEM address and
+  // the abort word)
+  static constexpr int kSmemBytes = 1024 + kData + 8 * kBars + 4 * kStages +
+                                    4 * kRing * kRingWords + 16 * kDRing + 16 + 64;
   static_assert(kSmemBytes <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
 };
 
@@ -142,7 +151,7 @@ constexpr uint32_t kDbgFlag = 1, kDbgStarted = 2, kDbgShardRow = 3, kDbgGathered
 // Sites reported with a pipeline timeout (ready-flag timeouts report the flag index).
 constexpr uint32_t kSiteEmpty = 0xF00001, kSiteFull = 0xF00002, kSiteTmemEmpty = 0xF00003,
                    kSiteTmemFull = 0xF00004, kSiteRing = 0xF00005, kSiteCopy = 0xF00006,
-                   kSitePro = 0xF00007;
+                   kSitePro = 0xF00007, kSiteDesc = 0xF00008;
 
 // Trace roles (see include/agmm.h).
 constexpr uint32_t kTraceClaim = 1, kTraceWait = 2, kTraceTile = 3, kTraceGather = 4,
@@ -705,78 +714,6 @@ __device__ __forceinline__ void regfetch_loop(const GemmParams& p, int lane, boo
   }
 }
 
-// Tile readiness, worked out ahead of the A issuer (fused kernels, the
-// register-fetch warp once its own chunks are done).  For each of the CTA's
-// tiles in order, the warp polls every ready flag the issuer could wait on in
-// that tile -- all non-empty chunks of the tile's row block except the
-// local-shard ones it reads straight from the shard (m-contiguous pairs: all
-// but those of pairs wholly in the local shard), the tile's own window
-// included -- until all are published, then takes them with an acquire fence
-// and tells the issuer with ready[j & 1] = j + 1 (release, CTA scope).  The
-// issuer, seeing that (acquire), issues one proxy fence and reads the rest of
-// the tile's chunks with no flag reads or fences of its own.  The warp works
-// on tile j only once the issuer has reached tile j - 1 (`itile`; one word per
-// tile parity, so it never overwrites the word of a tile still in use), and
-// gives up on a tile the issuer has already left behind.  Every exit decision
-// is voted, so the warp stays converged; every wait is bounded, and whatever
-// the warp does not report the issuer checks chunk by chunk itself.
-template <bool kAllStaged>
-__device__ __forceinline__ void readiness_loop(const GemmParams& p, int lane, int my_tiles,
-                                               uint32_t* ready, volatile uint32_t* itile,
-                                               volatile int* abort_flag) {
-  for (int j = 0; j < my_tiles; ++j) {
-    // Throttle: until the issuer is at tile j - 1 (bounded; the limit restarts
-    // whenever the issuer moves on).
-    uint32_t seen = *itile;
-    uint64_t t0 = globaltimer_ns();
-    for (;;) {
-      const uint32_t now_tile = __shfl_sync(0xffffffffu, *itile, 0);
-      if (now_tile + 1 >= (uint32_t)j) break;
-      bool stop = false;
-      if (lane == 0) {
-        const uint64_t now = globaltimer_ns();
-        if (now_tile != seen) {
-          seen = now_tile;
-          t0 = now;
-        }
-        stop = *abort_flag != 0 || now - t0 > (uint64_t)p.pipe_timeout_ns;
-      }
-      if (__shfl_sync(0xffffffffu, stop ? 1 : 0, 0)) return;
-      __nanosleep(512);
-    }
-    TileCtx c;
-    tile_ctx<true>(p, blockIdx.x + j * (int)gridDim.x, c);
-    const bool need = (kAllStaged && !c.pair_local) ? c.kind != kEmpty
-                                                     : (c.kind != kLocal && c.kind != kEmpty);
-    bool ok = true;
-    if (need) {
-      const uint64_t w0 = globaltimer_ns();
-      for (;;) {
-        bool mine = true;
-        for (int g = lane; g < p.G; g += 32) {
-          const int idx = c.mb * p.G + g;
-          if (!flag_ok(p, idx) ||
-              ld_relaxed_gpu(p.flags + idx) < p.fbase + (uint64_t)chunk_boxes(p, g))
-            mine = false;
-        }
-        if (__all_sync(0xffffffffu, mine)) break;
-        bool stop = false;
-        if (lane == 0)
-          stop = *abort_flag != 0 || *itile > (uint32_t)j ||
-                 globaltimer_ns() - w0 > (uint64_t)p.pipe_timeout_ns || error_this_call(p);
-        if (__shfl_sync(0xffffffffu, stop ? 1 : 0, 0)) {
-          ok = false;
-          break;
-        }
-        __nanosleep(256);
-      }
-      if (ok) fence_acquire_gpu();  // each lane: the flags it read were released
-    }
-    __syncwarp();  // (orders every lane's acquire before lane 0's release)
-    if (ok && lane == 0) st_release_cta_shared(&ready[j & 1], (uint32_t)j + 1u);
-  }
-}
-
 __device__ __forceinline__ uint32_t pack2(float lo, float hi, int fp16) {
   if (fp16) {
     __half2 h = __floats2half2_rn(lo, hi);
@@ -829,6 +766,91 @@ __device__ __forceinline__ void drain_loads(uint64_t* full, uint32_t issued_mask
     }
 }
 
+// The A side of the stage ring, as the thread that loads A sees it.
+struct ARing {
+  int stage = 0;
+  uint32_t phase = 0;
+  uint32_t issued_mask = 0, issued_parity = 0;  // for drain_loads after an abort
+};
+
+// One chunk's A loads: `nbox` k-blocks from k-block `kb0` of row block `mb`,
+// each into the next stage of the ring once the MMA has freed it; `bits`
+// goes to the stage record.  One loop per kind of A box (shard map, shard row
+// groups, [K, M] staging, segmented or plain gathered map), so that nothing in
+// the per-stage path branches on the chunk's kind: the loading thread's time
+// per stage bounds how far ahead of the MMA it keeps the ring.  False on
+// abort or timeout.
+template <bool kPair, bool kFused, bool kLayoutM>
+__device__ __forceinline__ bool a_chunk_loads(const GemmParams& p, ARing& ar, uint8_t* smem,
+                                              uint64_t* full, uint64_t* empty, uint32_t* info,
+                                              uint32_t full_c, uint32_t rank,
+                                              volatile int* abort_flag, uint32_t bits,
+                                              bool direct, bool one_shard, int r0, int mb,
+                                              int kb0, int nbox, int sy, int sd) {
+  constexpr int kStages = Pipe<kPair>::kStages;
+  constexpr int kStageBytes = Pipe<kPair>::kStageBytes;
+  bool ok = true;
+  auto stage_loop = [&](auto&& load_a) {
+    for (int j = 0; j < nbox; ++j) {
+      if (!wait_bar(p, &empty[ar.stage], ar.phase ^ 1u, abort_flag, kSiteEmpty)) {
+        ok = false;
+        return;
+      }
+      info[ar.stage] = bits;
+      uint8_t* a_dst = smem + ar.stage * kStageBytes;
+      const uint32_t bar_c = full_c + 8u * (uint32_t)ar.stage;
+      if (!kPair || rank == 0)
+        mbar_arrive_expect_tx(&full[ar.stage], kPair ? 2 * kAStageBytes : kAStageBytes);
+      load_a(a_dst, &full[ar.stage], bar_c, (kb0 + j) * kBK);
+      ar.issued_mask |= 1u << ar.stage;
+      ar.issued_parity = (ar.issued_parity & ~(1u << ar.stage)) | (ar.phase << ar.stage);
+      if (++ar.stage == kStages) {
+        ar.stage = 0;
+        ar.phase ^= 1u;
+      }
+    }
+  };
+  if (direct && one_shard) {
+    const CUtensorMap* m = &p.tm_shard[r0];
+    const int y = mb * kBM - r0 * p.mps;
+    stage_loop([&](uint8_t* a_dst, uint64_t* fb, uint32_t bar_c, int x) {
+      stage_load_2d<kPair>(a_dst, m, fb, bar_c, x, y);
+    });
+  } else if (direct) {
+    // Walk the row groups (2^sh_log2 rows, which divides both 128 and
+    // m_per_shard, so no group straddles a boundary) across the shards
+    // without a division per group.  Past the last shard the row stays out of
+    // range: TMA zero-fills it.
+    stage_loop([&](uint8_t* a_dst, uint64_t* fb, uint32_t bar_c, int x) {
+      const int h = 1 << p.sh_log2;
+      int r = r0, lr = mb * kBM - r0 * p.mps;
+#pragma unroll 1
+      for (int q = 0; q < (kBM >> p.sh_log2); ++q) {
+        stage_load_2d<kPair>(a_dst + q * h * 128, &p.tm_shard8[r], fb, bar_c, x, lr);
+        lr += h;
+        if (lr >= p.mps && r < p.D - 1) {
+          lr -= p.mps;
+          ++r;
+        }
+      }
+    });
+  } else if (kLayoutM) {
+    stage_loop([&](uint8_t* a_dst, uint64_t* fb, uint32_t bar_c, int x) {
+      stage_load_2d<kPair>(a_dst, &p.tm_a_mk, fb, bar_c, mb * kBM, x);
+      stage_load_2d<kPair>(a_dst + kMnChunkBytes, &p.tm_a_mk, fb, bar_c, mb * kBM + 64, x);
+    });
+  } else if (!kFused && p.seg_blocks) {
+    stage_loop([&](uint8_t* a_dst, uint64_t* fb, uint32_t bar_c, int x) {
+      stage_load_3d<kPair>(a_dst, &p.tm_a, fb, bar_c, x, sy, sd);
+    });
+  } else {
+    stage_loop([&](uint8_t* a_dst, uint64_t* fb, uint32_t bar_c, int x) {
+      stage_load_2d<kPair>(a_dst, &p.tm_a, fb, bar_c, x, mb * kBM);
+    });
+  }
+  return ok;
+}
+
 // ------------------------------------------------------------------ the kernel
 
 // kPair: launched in clusters of two CTAs; the even CTA (rank 0, the leader)
@@ -874,13 +896,14 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
   uint64_t* rfull = drain + 1;               // [kRing] fused: chunk record written
   uint64_t* rfree = rfull + kRing;           // [kRing] fused: every copier is done with it
   uint64_t* pro_bar = rfree + kRing;         // [1] fused: this CTA's fetch prologue is done
-  uint32_t* info = reinterpret_cast<uint32_t*>(pro_bar + 1);  // [kStages]
+  uint64_t* dfull = pro_bar + 1;             // [kDRing] fused: chunk descriptor written
+  uint64_t* dfree = dfull + kDRing;          // [kDRing] fused: the A loader has read it
+  uint32_t* info = reinterpret_cast<uint32_t*>(dfree + kDRing);  // [kStages]
   uint32_t* ring = info + kStages;                // [kRing][kRingWords] chunk records
-  volatile uint32_t* iseq = ring + kRing * kRingWords;  // issuer progress (chunks), a liveness signal
-  uint32_t* tmem_slot = ring + kRing * kRingWords + 1;
+  uint32_t* dring = ring + kRing * kRingWords;    // [kDRing][4] chunk descriptors
+  volatile uint32_t* iseq = dring + kDRing * 4;   // issuer progress (chunks), a liveness signal
+  uint32_t* tmem_slot = dring + kDRing * 4 + 1;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  uint32_t* ready = tmem_slot + 2;                // [2] fused: tile readiness (readiness_loop)
-  volatile uint32_t* itile = tmem_slot + 4;       // fused: the A issuer's tile counter
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -897,6 +920,10 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
       mbar_init(&rfree[r], kCopyWarps);
     }
     mbar_init(pro_bar, kProWarps);
+    for (int d = 0; d < kDRing; ++d) {
+      mbar_init(&dfull[d], 1);
+      mbar_init(&dfree[d], 1);
+    }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tmem_full[b], 1);
       // one arrive per epilogue warp (pair: the leader's barrier takes both CTAs')
@@ -905,9 +932,6 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
     mbar_init(drain, 1);
     *iseq = 0;
     *abort_flag = 0;
-    ready[0] = 0;
-    ready[1] = 0;
-    *itile = 0;
     fence_mbarrier_init();
     prefetch_tensormap(&p.tm_a);
     prefetch_tensormap(&p.tm_b);
@@ -927,13 +951,35 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
   // Pair: the leader's `full` barriers, where both CTAs' loads count their bytes.
   const uint32_t full_c = kPair ? mapa_shared(smem_u32(&full[0]), 0) : 0u;
 
-  if (warp == 0) {
-    // ---------------------------------------------------------- A issuer
+  if (warp == (kFused ? kProtoWarp : 0)) {
+    // ---------------------------------------------------------- A issuer / protocol
+    // The barrier GEMM's warp 0 issues its A loads here.  In the fused kernel
+    // this warp runs the ready-flag protocol and hands each chunk's decision
+    // to the A loader (warp 0) as a descriptor, so that flag reads, waits,
+    // fences and hand-offs never delay a load.
+    if (kFused && p.l2_prefetch) {
+      // Small A (the host's choice): every CTA first asks L2 for its share of
+      // the shards' rows, so that the owners' and copiers' first reads of A
+      // hit L2, as the GEMM's do after the barrier path's gather.  Pieces of
+      // 32 KB, in bounds of each shard, 16-byte aligned (K % 8 == 0).
+      const int rows_per = (p.M + (int)gridDim.x - 1) / (int)gridDim.x;
+      int r0 = min(p.M, (int)blockIdx.x * rows_per);
+      const int r1 = min(p.M, r0 + rows_per);
+      while (r0 < r1) {
+        const int s = r0 / p.mps;
+        const int lr = r0 - s * p.mps;
+        const int n = min(r1 - r0, p.mps - lr);
+        const char* base = reinterpret_cast<const char*>(p.shards[s] + (int64_t)lr * p.K);
+        const int64_t bytes = (int64_t)n * p.K * 2;
+        for (int64_t off = (int64_t)lane * 32768; off < bytes; off += 32 * 32768)
+          prefetch_l2_bulk(base + off, (uint32_t)(bytes - off < 32768 ? bytes - off : 32768));
+        r0 += n;
+      }
+    }
     if (lane == 0) {
-      uint32_t issued_mask = 0, issued_parity = 0;
+      ARing ar;             // barrier GEMM: the A loads issued here
       bool aborted = false;
-      int stage = 0, seq = 0;
-      uint32_t phase = 0;
+      int seq = 0;          // boxes so far (fused: handed to the A loader)
       int rslot = 0;        // fused: next ring slot for a chunk record
       uint32_t rphase = 0;  // ... and the parity of its use
       // Chunk cursor over this CTA's (tile, k-group) sequence.  Tile (mb, nb)
@@ -959,10 +1005,8 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
       int t = blockIdx.x, gi = 0;
       int pre = 0, cur_pre = 0;
       uint64_t cur_peek = 0;
-      // Fused: this CTA's tile counter (mirrored in *itile for the readiness
-      // warp) and whether that warp has reported the current tile ready.
-      uint32_t tj = 0;
-      bool tile_fast = false;
+      int dslot = 0;        // fused: next descriptor slot
+      uint32_t dphase = 0;  // ... and the parity of its use
       if (t < p.num_tiles) {
         tile_ctx<kFused>(p, t, cur);
         const int g0 = order_at(p, 0, cur.ws, cur.we);
@@ -1016,6 +1060,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
         const int nbox = g == p.G - 1 ? last_nbox : p.kpf;
         const int kind = cur.kind;
         bool direct = false;  // A straight from a shard (else from the staging)
+        bool need_fence = false;
         uint32_t bits = 0;
         if (kFused) {
           // A window chunk staged ahead is read like a follower's: from the
@@ -1023,20 +1068,12 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
           // the shard.
           // (Owned chunks were handed to the copiers at the tile start.)
           const bool staged_ahead = cur.owns(g) && g - cur.ws < cur_pre;
-          if (!tile_fast && ld_acquire_cta_shared(&ready[tj & 1]) == tj + 1u) {
-            // Every flag of this tile is published and acquired (readiness_loop):
-            // one proxy fence orders that before all of the tile's loads.
-            tile_fast = true;
-            fence_proxy_async_global();
-          }
           if (kind == kLocal && (!kAllStaged || cur.pair_local)) {
             direct = true;
           } else if (kind == kEmpty) {
             // rows past M: the gathered copy's maps read zeros there
           } else if (kind == kDirect && cur.owns(g) && !staged_ahead && !kAllStaged) {
             direct = true;
-          } else if (tile_fast) {
-            // published: read the staged copy
           } else {
             const uint64_t target = p.fbase + (uint64_t)nbox;
             if (cur_peek >= target) {
@@ -1072,7 +1109,9 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
               }
               if (p.trace) trace_rec(p.trace, p.trace_words, kTraceWait, mb, g, t0, globaltimer_ns());
             }
-            if (!direct) fence_proxy_async_global();
+            // The loader orders this acquire before its TMA loads of the
+            // staged data with a proxy fence.
+            need_fence = !direct;
           }
           if ((bits & kInfoStage) && p.trace) {
             const uint64_t now = globaltimer_ns();
@@ -1113,7 +1152,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
         const int n_pre = new_tile ? pre : cur_pre;
         uint64_t nxt_peek = 0;
         bool nxt_follow = false;
-        if (kFused && nt < p.num_tiles && (new_tile || !tile_fast)) {
+        if (kFused && nt < p.num_tiles) {
           const int ng = order_at(p, ngi, n_ws, n_we);
           nxt_follow = (kAllStaged && !n_pl)
                            ? n_kind != kEmpty
@@ -1124,76 +1163,39 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
             nxt_peek = ld_relaxed_gpu(p.flags + n_mb * p.G + ng);
         }
 
-        const int r0 = cur.r0;
-        const bool one_shard = cur.one_shard;
-        // The chunk's loads.  One loop per kind of A box, so that nothing in
-        // the per-stage path branches on the chunk's kind: the issuer's time
-        // per stage bounds how far ahead of the MMA it keeps the ring.
-        auto stage_loop = [&](auto&& load_a) {
-          for (int j = 0; j < nbox; ++j) {
-            const int kb = g * p.kpf + j;
-            if (!wait_bar(p, &empty[stage], phase ^ 1u, abort_flag, kSiteEmpty)) {
-              aborted = true;
-              return;
-            }
-            info[stage] = bits;
-            uint8_t* a_dst = smem + stage * kStageBytes;
-            const uint32_t bar_c = full_c + 8u * (uint32_t)stage;
-            if (!kPair || rank == 0)
-              mbar_arrive_expect_tx(&full[stage], kPair ? 2 * kAStageBytes : kAStageBytes);
-            load_a(a_dst, &full[stage], bar_c, kb * kBK);
-            issued_mask |= 1u << stage;
-            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-            ++seq;
-            if (++stage == kStages) {
-              stage = 0;
-              phase ^= 1u;
-            }
+        if constexpr (kFused) {
+          // Hand the chunk to the A loader (warp 0).
+          if (!wait_bar(p, &dfree[dslot], dphase ^ 1u, abort_flag, kSiteDesc)) {
+            aborted = true;
+            break;
           }
-        };
-        if (direct && one_shard) {
-          const CUtensorMap* m = &p.tm_shard[r0];
-          const int y = mb * kBM - r0 * p.mps;
-          stage_loop([&](uint8_t* a_dst, uint64_t* fb, uint32_t bar_c, int x) {
-            stage_load_2d<kPair>(a_dst, m, fb, bar_c, x, y);
-          });
-        } else if (direct) {
-          // Walk the row groups (2^sh_log2 rows, which divides both 128 and
-          // m_per_shard, so no group straddles a boundary) across the shards
-          // without a division per group.  Past the last shard the row stays
-          // out of range: TMA zero-fills it.
-          stage_loop([&](uint8_t* a_dst, uint64_t* fb, uint32_t bar_c, int x) {
-            const int h = 1 << p.sh_log2;
-            int r = r0, lr = mb * kBM - r0 * p.mps;
-#pragma unroll 1
-            for (int q = 0; q < (kBM >> p.sh_log2); ++q) {
-              stage_load_2d<kPair>(a_dst + q * h * 128, &p.tm_shard8[r], fb, bar_c, x, lr);
-              lr += h;
-              if (lr >= p.mps && r < p.D - 1) {
-                lr -= p.mps;
-                ++r;
-              }
-            }
-          });
-        } else if (kLayoutM) {
-          stage_loop([&](uint8_t* a_dst, uint64_t* fb, uint32_t bar_c, int x) {
-            stage_load_2d<kPair>(a_dst, &p.tm_a_mk, fb, bar_c, mb * kBM, x);
-            stage_load_2d<kPair>(a_dst + kMnChunkBytes, &p.tm_a_mk, fb, bar_c, mb * kBM + 64, x);
-          });
-        } else if (!kFused && p.seg_blocks) {
-          stage_loop([&](uint8_t* a_dst, uint64_t* fb, uint32_t bar_c, int x) {
-            stage_load_3d<kPair>(a_dst, &p.tm_a, fb, bar_c, x, cur.sy, cur.sd);
-          });
+          uint32_t* d = dring + dslot * 4;
+          d[0] = (direct ? kDescDirect : 0u) | (cur.one_shard ? kDescOneShard : 0u) |
+                 (need_fence ? kDescFence : 0u) | (bits << 8);
+          d[1] = (uint32_t)mb;
+          d[2] = (uint32_t)g | ((uint32_t)nbox << 16);
+          d[3] = (uint32_t)cur.r0;
+          mbar_arrive(&dfull[dslot]);  // (release: the loader reads the record after its wait)
+          if (++dslot == kDRing) {
+            dslot = 0;
+            dphase ^= 1u;
+          }
+          seq += nbox;
         } else {
-          stage_loop([&](uint8_t* a_dst, uint64_t* fb, uint32_t bar_c, int x) {
-            stage_load_2d<kPair>(a_dst, &p.tm_a, fb, bar_c, x, mb * kBM);
-          });
+          if (!a_chunk_loads<kPair, kFused, kLayoutM>(p, ar, smem, full, empty, info, full_c, rank,
+                                                       abort_flag, bits, direct, cur.one_shard,
+                                                       cur.r0, mb, g * p.kpf, nbox, cur.sy,
+                                                       cur.sd)) {
+            aborted = true;
+            break;
+          }
+          seq += nbox;
         }
         if (p.trace)  // b: k-group | 1 << 16 if loaded from a shard | 2 << 16 if staged here
           trace_rec(p.trace, p.trace_words, kTraceIssue, mb,
                     (uint32_t)g | (direct ? 1u << 16 : 0u) | ((bits & kInfoStage) ? 2u << 16 : 0u),
                     t_chunk, globaltimer_ns());
-        if (kFused && !aborted && !new_tile && t + (int)gridDim.x < p.num_tiles &&
+        if (kFused && !new_tile && t + (int)gridDim.x < p.num_tiles &&
             (nxt.kind == kLocal || nxt.kind == kDirect) && pre < nxt.we - nxt.ws &&
             gi >= p.stage_from &&
             mbar_test_wait(&rfree[rslot], rphase ^ 1u)) {
@@ -1222,23 +1224,62 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
           cur_pre = pre;
           pre = 0;
           if (t + (int)gridDim.x < p.num_tiles) tile_ctx<kFused>(p, t + gridDim.x, nxt);
-          if (kFused) {
-            ++tj;
-            tile_fast = false;
-            *itile = tj;
-          }
         }
         if (nxt_follow) cur_peek = nxt_peek;
         if (kFused) *iseq = (uint32_t)seq;
       }
-      if (kFused) *itile = 0x7fffffffu;  // done: the readiness warp has nothing left to do
-      if (kFused && wait_bar(p, &rfree[rslot], rphase ^ 1u, abort_flag, kSiteRing)) {
-        // End of stream (if the slot does not free, the abort flag is set and
-        // the copiers leave on it).
-        ring[rslot * kRingWords] = kInfoEnd;
-        mbar_arrive(&rfull[rslot]);
+      if constexpr (kFused) {
+        // End of stream, for the A loader and for the copiers (if a slot does
+        // not free, the abort flag is set and they leave on it).
+        if (wait_bar(p, &dfree[dslot], dphase ^ 1u, abort_flag, kSiteDesc)) {
+          dring[dslot * 4] = kDescEnd;
+          mbar_arrive(&dfull[dslot]);
+        }
+        if (wait_bar(p, &rfree[rslot], rphase ^ 1u, abort_flag, kSiteRing)) {
+          ring[rslot * kRingWords] = kInfoEnd;
+          mbar_arrive(&rfull[rslot]);
+        }
+      } else {
+        if (aborted || *abort_flag) drain_loads<kPair>(full, ar.issued_mask, ar.issued_parity, rank);
       }
-      if (aborted || *abort_flag) drain_loads<kPair>(full, issued_mask, issued_parity, rank);
+    }
+    __syncwarp();
+  } else if (kFused && warp == 0) {
+    // ---------------------------------------------------------- A loader (fused)
+    // Takes the protocol warp's chunk descriptors in order and issues each
+    // chunk's A loads.  A descriptor marked kDescFence follows the protocol
+    // warp's acquire of the chunk's ready flag; the descriptor barrier carries
+    // that acquire here (release/acquire at CTA scope), and the proxy fence
+    // then orders it before the TMA loads of the staged data.
+    if (lane == 0) {
+      ARing ar;
+      bool aborted = false;
+      int dslot = 0;
+      uint32_t dphase = 0;
+      for (;;) {
+        if (!wait_bar(p, &dfull[dslot], dphase, abort_flag, kSiteDesc)) {
+          aborted = true;
+          break;
+        }
+        const uint32_t* d = dring + dslot * 4;
+        const uint32_t d0 = d[0], d1 = d[1], d2 = d[2], d3 = d[3];
+        mbar_arrive(&dfree[dslot]);
+        if (++dslot == kDRing) {
+          dslot = 0;
+          dphase ^= 1u;
+        }
+        if (d0 & kDescEnd) break;
+        if (d0 & kDescFence) fence_proxy_async_global();
+        const int mb = (int)d1, g = (int)(d2 & 0xFFFFu), nbox = (int)(d2 >> 16);
+        if (!a_chunk_loads<kPair, kFused, kLayoutM>(p, ar, smem, full, empty, info, full_c, rank,
+                                                     abort_flag, d0 >> 8, (d0 & kDescDirect) != 0,
+                                                     (d0 & kDescOneShard) != 0, (int)d3, mb,
+                                                     g * p.kpf, nbox, 0, 0)) {
+          aborted = true;
+          break;
+        }
+      }
+      if (aborted || *abort_flag) drain_loads<kPair>(full, ar.issued_mask, ar.issued_parity, rank);
     }
     __syncwarp();
   } else if (warp == 1 && kPair && rank != 0) {
@@ -1500,31 +1541,6 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
       if (aborted || *abort_flag) drain_loads<kPair>(full, issued_mask, issued_parity, rank);
     }
     __syncwarp();
-  } else if (kFused && warp == kRegWarp) {
-    // ---------------------------------------------------------- register fetcher
-    if (p.l2_prefetch) {
-      // Small A (the host's choice): every CTA first asks L2 for its share of
-      // the shards' rows, so that the owners' and copiers' first reads of A
-      // hit L2, as the GEMM's do after the barrier path's gather.  Pieces of
-      // 32 KB, in bounds of each shard, 16-byte aligned (K % 8 == 0).
-      const int rows_per = (p.M + (int)gridDim.x - 1) / (int)gridDim.x;
-      int r0 = min(p.M, (int)blockIdx.x * rows_per);
-      const int r1 = min(p.M, r0 + rows_per);
-      while (r0 < r1) {
-        const int s = r0 / p.mps;
-        const int lr = r0 - s * p.mps;
-        const int n = min(r1 - r0, p.mps - lr);
-        const char* base = reinterpret_cast<const char*>(p.shards[s] + (int64_t)lr * p.K);
-        const int64_t bytes = (int64_t)n * p.K * 2;
-        for (int64_t off = (int64_t)lane * 32768; off < bytes; off += 32 * 32768)
-          prefetch_l2_bulk(base + off, (uint32_t)(bytes - off < 32768 ? bytes - off : 32768));
-        r0 += n;
-      }
-    }
-    regfetch_loop(p, lane, kLayoutM);
-    __syncwarp();
-    readiness_loop<kAllStaged>(p, lane, my_tiles, ready, itile, abort_flag);
-    __syncwarp();
   } else if (kFused) {
     // ---------------------------------------------------------- copiers
     // Take the issuer's chunk records in order.  Box j of a chunk whose first
@@ -1539,6 +1555,11 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
     // scope), so the flag follows every copier's writes.
     const int w = warp - kCopyWarp0;
     if constexpr (!kLayoutM) fetch_prologue(p, w, lane, pro_bar);
+    // The first copier also runs the register fetcher first: it copies the
+    // chunks that TMA cannot load from a single shard (row blocks straddling
+    // shards whose row count is not a multiple of 8) and publishes them; it
+    // waits on nobody, so every such chunk is published whatever else runs.
+    if (w == 0) regfetch_loop(p, lane, kLayoutM);
     const int ch = lane & 7;  // 16-byte column chunk of a 128-byte box row
     for (uint32_t n = 0;; ++n) {
       const int slot = (int)(n % kRing);
