@@ -996,7 +996,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
       // counts the chunks of nxt handed so far (window order), `cur_pre`
       // those of the current tile, which it then loads without staging.  The
       // hand-off starts at position p.stage_from of the current tile (the
-      // plan sets it half-way through for calls of four or more waves), so
+      // plan sets it three quarters through for calls of four or more waves), so
       // the staged copy is still in L2 when the next wave reads it.  The
       // next tile is marked started only once its whole window is handed:
       // until then a follower may still take its chunks over, as for any
