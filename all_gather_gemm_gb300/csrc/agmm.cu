@@ -456,24 +456,27 @@ int plan_launch(GemmParams& p, const Shape& s, int cap, int pair_clusters, bool 
   }
   // Calls of four or more waves: every tile runs k ascending (the tiles of a
   // row block then read each A k-slice at about the same time, as in the
-  // barrier GEMM, and share it in L2); with the k-contiguous staging a CTA
-  // also hands its next tile's window to the copiers only late in the
-  // current tile (from three quarters of its k-groups, counted where the
-  // protocol warp is, which runs a few chunks ahead of the loads), so that
-  // staged chunks are still in L2 when the next wave reads them.  Measured
-  // at M=16384 N=3584 K=8192 (ncu, per fused launch, hand-off from half-way
-  // with the protocol still in the loading thread): DRAM reads 1293 -> 1069
-  // MB, 589 -> 579 us; interleaved timing 609 -> 601 us.  With the protocol
-  // warp, three quarters instead of half: -3 us, FP8 -4 us.  On one to three waves ascending order cost 2-7 us (the
+  // barrier GEMM, and share it in L2), and a CTA hands its next tile's
+  // window to the copiers only late in the current tile -- from three
+  // quarters of its k-groups, counted where the protocol warp is, a few
+  // chunks ahead of the loads -- so that staged chunks are still in L2 when
+  // the next wave reads them.  Measured at M=16384 N=3584 K=8192 (ncu, per
+  // fused launch, hand-off from half-way with the protocol still in the
+  // loading thread): DRAM reads 1293 -> 1069 MB, 589 -> 579 us; interleaved
+  // timing 609 -> 601 us.  With the protocol warp, three quarters instead of
+  // half: -3 us, FP8 -4 us; the m-contiguous staging, which gained nothing
+  // from a later hand-off while the protocol ran in the loading thread, now
+  // gains 4.5 us.  On one to three waves ascending order cost 2-7 us (the
   // first wave waits on the owners' copiers) and the later hand-off 2 us at
-  // cube 4096, and with the m-contiguous staging the later hand-off did not
-  // help: those keep the owned window first / hand off at once.  The order
-  // depends on the shape only, so every rank and both layouts of a call get
-  // the same per-tile order (and, with k ascending, the barrier GEMM's
-  // results bit for bit).
+  // cube 4096: those keep the owned window first and hand off at once (with
+  // the protocol warp, ascending order from three waves on still cost 4 us
+  // at cube 3968 and 8 us with FP8 at cube 4096).  The order depends on the
+  // shape only, so every rank and both layouts of a call get the same
+  // per-tile order (and, with k ascending, the barrier GEMM's results bit
+  // for bit).
   if (fused && p.w0 > 0 && tiles >= 4 * grid_units) {
     p.k_asc = 1;
-    if (!layout_m) p.stage_from = (3 * p.G) / 4;
+    p.stage_from = (3 * p.G) / 4;
     // m-contiguous on CTA pairs: pairs whose rows all lie in the local shard
     // read them K-major from the shard instead of MN-major from the [K, M]
     // staging, so those chunks are neither written transposed nor waited on.
