@@ -15,7 +15,7 @@
 //               accumulation into one of two TMEM accumulators.
 //   warps 2-5   epilogue: tcgen05.ld, (FP8: x scale) + fp32 bias, round to
 //               16 bits, 128-byte-swizzled shared memory, TMA store.
-//   warp 6      B loader: b's k-blocks in the A issuer's order.
+//   warp 6      B loader: b's k-blocks in the chunk order of the A loads.
 //   warp 7      protocol (fused only): the ready-flag protocol, a few chunks
 //               ahead of the A loader.  Every (row block, k-group) chunk has
 //               an owner: the column block whose tile starts its k-loop there
@@ -106,9 +106,9 @@ __host__ __device__ constexpr int mode_threads(int m) {
 constexpr uint32_t kInfoStage = 1u;    // chunk: to be written into a_gathered
 constexpr uint32_t kInfoPublish = 2u;  // chunk: ... and published once written
 constexpr uint32_t kInfoAmn = 4u;      // stage: the A box in shared memory is MN-major
-constexpr uint32_t kInfoEnd = 8u;      // chunk record: the issuer is done, the copiers leave
+constexpr uint32_t kInfoEnd = 8u;      // chunk record: no more chunks, the copiers leave
 
-// Chunk records handed from the issuer to the copiers:
+// Chunk records handed from the protocol warp to the copiers:
 // {bits, mb, first k-block, boxes, flag index, box sequence index, done count, -}.
 constexpr int kRing = 8;
 constexpr int kRingWords = 8;
@@ -135,7 +135,7 @@ struct Pipe {
   // full, empty [kStages]; tmem_full, tmem_empty [2]; drain; rfull, rfree
   // [kRing]; pro (fetch prologue done); dfull, dfree [kDRing]
   static constexpr int kBars = 2 * kStages + 4 + 1 + 2 * kRing + 1 + 2 * kDRing;
-  // (+ the chunk descriptors, the issuer's progress word, the TMEM address and
+  // (+ the chunk descriptors, the protocol's progress word, the TMEM address and
   // the abort word)
   static constexpr int kSmemBytes = 1024 + kData + 8 * kBars + 4 * kStages +
                                     4 * kRing * kRingWords + 16 * kDRing + 16 + 64;
@@ -169,7 +169,7 @@ struct GemmParams {
   uint16_t* staging_mk;
   const float* bias;
   uint64_t* flags;          // [num_mb * G]
-  uint64_t* started;        // [num_tiles]: epoch once the tile's issuer began it
+  uint64_t* started;        // [num_tiles]: epoch once the tile's protocol began it
   unsigned long long* err;  // [2]: epoch of newest error, code << 32 | info
   uint64_t* trace;
   int64_t trace_words;
@@ -378,7 +378,7 @@ __device__ __forceinline__ int chunk_boxes(const GemmParams& p, int g) {
   return min(p.kpf, p.num_kb - g * p.kpf);
 }
 
-// Per-tile facts the A issuer needs for every chunk, computed once per tile.
+// Per-tile facts the chunk loop needs for every chunk, computed once per tile.
 struct TileCtx {
   int mb, nb;
   int sd, sy;      // segmented barrier GEMM: segment and first row of the block in it
@@ -465,9 +465,9 @@ __device__ __forceinline__ void hand_chunk(uint32_t* rec, uint64_t* rfull_bar, u
 }
 
 // Copier side of the hand-off: waits for phase `n` of a ring slot's `rfull`
-// barrier (the issuer's n-th record in that slot).  False on abort or
+// barrier (the protocol warp's n-th record in that slot).  False on abort or
 // timeout.  Copiers may idle for as long as their CTA has nothing to stage,
-// so the time limit restarts whenever the issuer makes progress (`iseq`).
+// so the time limit restarts whenever the protocol warp makes progress (`iseq`).
 __device__ __forceinline__ bool wait_handoff(const GemmParams& p, uint64_t* bar, uint32_t n,
                                              volatile uint32_t* iseq, volatile int* abort_flag) {
   const uint32_t parity = n & 1u;
@@ -901,7 +901,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
   uint32_t* info = reinterpret_cast<uint32_t*>(dfree + kDRing);  // [kStages]
   uint32_t* ring = info + kStages;                // [kRing][kRingWords] chunk records
   uint32_t* dring = ring + kRing * kRingWords;    // [kDRing][4] chunk descriptors
-  volatile uint32_t* iseq = dring + kDRing * 4;   // issuer progress (chunks), a liveness signal
+  volatile uint32_t* iseq = dring + kDRing * 4;   // protocol progress (boxes), a liveness signal
   uint32_t* tmem_slot = dring + kDRing * 4 + 1;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -989,7 +989,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
       // follower's flag is read one chunk ahead, so its latency overlaps the
       // current chunk's loads.
       //
-      // Staging ahead (fused): while it works on a tile, the issuer hands the
+      // Staging ahead (fused): while it works on a tile, the protocol hands the
       // window of its next tile (nxt) to the copiers, one chunk per chunk it
       // issues and only when a ring slot is free at once, so that tile's
       // followers in other CTAs find those chunks published early.  `pre`
@@ -1133,7 +1133,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
         if (!direct && kLayoutM) bits |= kInfoAmn;
 
         // Next chunk in sequence.  Only a follower chunk reads its flag; owner
-        // and local chunks never touch it, so the issuer never stalls on a
+        // and local chunks never touch it, so the protocol never stalls on a
         // load it does not need.
         int nt = t, ngi = gi + 1;
         bool new_tile = false;
@@ -1490,7 +1490,7 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
     __syncwarp();
   } else if (warp == kBWarp) {
     // ---------------------------------------------------------- B loader
-    // The tile's B k-blocks in the A issuer's order (owned window first):
+    // The tile's B k-blocks in the order of its A chunks (owned window first):
     // one thread issuing both operands' loads could not keep up with the
     // tensor pipe.  Each loader arrives on `full` for its own bytes.
     if (lane == 0) {
@@ -1543,9 +1543,9 @@ __global__ void __launch_bounds__(mode_threads(kMode), 1)
     __syncwarp();
   } else if (kFused) {
     // ---------------------------------------------------------- copiers
-    // Take the issuer's chunk records in order.  Box j of a chunk whose first
-    // box has sequence index q goes to warp (q + j) % kCopyWarps, so the
-    // boxes of consecutive chunks spread evenly over the warps.  A box is
+    // Take the protocol warp's chunk records in order.  Box j of a chunk
+    // whose first box has sequence index q goes to warp (q + j) % kCopyWarps,
+    // so the boxes of consecutive chunks spread evenly over the warps.  A box is
     // copied in 8-row groups: lane = (row group, 16-byte column chunk), 8 rows
     // of 16 bytes per lane, two groups (16 loads) in flight; for the
     // m-contiguous layout a published box is also written transposed (8x8
