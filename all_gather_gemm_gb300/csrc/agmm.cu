@@ -433,7 +433,7 @@ int plan_launch(GemmParams& p, const Shape& s, int cap, int pair_clusters, bool 
   const int grid_units = std::max(1, std::min(units, tiles));
   p.pro_cta0 = -1;  // fetch prologue off unless chosen below
   // A small enough to be read from L2 soon after the start: the fused kernel
-  // asks L2 for all of it first (see the register fetcher).
+  // asks L2 for all of it first (the protocol warp, before its first chunk).
   p.l2_prefetch = fused && s.M * (int64_t)s.num_kb * kBK * 2 <= kL2PrefetchMaxBytes ? 1 : 0;
   // Fetch prologue.  When a k-contiguous fused call takes two or three waves
   // and the last one is partial, the units with one tile fewer than the rest

@@ -339,9 +339,10 @@ int ag_matmul_noalloc(const void** a_shards, int D, int m_per_shard, int K, cons
 #define AG_TRACE_TILE 3u     /* epilogue stored an output tile (a = row block, b = column block) */
 #define AG_TRACE_GATHER 4u   /* barrier path: a gather-kernel CTA ran (a = CTA, b = 0) */
 #define AG_TRACE_REGFETCH 5u /* a chunk TMA cannot address was copied by registers (a, b) */
-#define AG_TRACE_ISSUE 6u    /* the A issuer (TMA loads of A) handled one chunk, flag checks included
-                                (a = block, b = k-group | 1 << 16 if read straight from a
-                                shard | 2 << 16 if this CTA staged it) */
+#define AG_TRACE_ISSUE 6u    /* one chunk's A loads were decided (barrier GEMM: issued; fused:
+                                the protocol warp handed the chunk to the A loader, flag checks
+                                included) (a = block, b = k-group | 1 << 16 if read straight
+                                from a shard | 2 << 16 if this CTA staged it) */
 
 #ifdef __cplusplus
 }
