@@ -6,7 +6,7 @@ buffer (word 0 is an atomic counter); ``meta = role << 56 | cta << 40 | a << 20
 flags, chunk staging, tile completion) and writes a Chrome trace-event JSON
 timeline (one row per CTA) that shows the gather/GEMM overlap.
 
-Tracing costs the issuer a global atomic per record, so traced runs are
+Tracing costs the recording warp a global atomic per record, so traced runs are
 slower than untraced ones; use them for the shape of the timeline, not for
 absolute times.
 
