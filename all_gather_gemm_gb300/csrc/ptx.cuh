@@ -245,18 +245,6 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
 
 // Turns an earlier relaxed read of a flag into an acquire (fence pattern).
 // The acquire-only fence does not wait for this thread's earlier stores.
-// A shared-memory word read with acquire / written with release semantics at
-// CTA scope (a hand-over between two warps of one CTA).
-__device__ __forceinline__ uint32_t ld_acquire_cta_shared(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void st_release_cta_shared(uint32_t* p, uint32_t v) {
-  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
-}
-
 __device__ __forceinline__ void fence_acquire_gpu() {
   asm volatile("fence.acquire.gpu;" ::: "memory");
 }
